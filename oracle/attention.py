@@ -1,0 +1,287 @@
+"""Plain float64 NumPy oracle for blockwise ring attention (test infrastructure).
+
+Only tests, the smoke check and the bench's CPU-baseline leg use this module.
+No blocking, fusion or reordering beyond what each docstring states.
+
+Notation (the glossary page's toy uses the same names): N devices (blocks),
+block = S / N tokens, dim = D.  q is [B, Hq, S, D]; k and v are [B, Hkv, S, D];
+query head h reads key/value head h // (Hq // Hkv) (grouped-query attention,
+the thienlv.com page's "compatible with GQA"; contiguous grouping is this
+oracle's reading).  scale defaults to 1/sqrt(D) (the toy's ``dim**0.5``).
+
+Layouts.  *Token order* is the sequence order.  *Shard-major* order is how N
+devices hold the sequence: rows [i*Sb, (i+1)*Sb) belong to device i.  With the
+contiguous layout shard-major equals token order; with the striped layout
+(token t on device t mod N, the glossary page's Striped Attention remark, read
+as round-robin assignment) row r of device i holds token r*N + i.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+FULL, INCL, STRICT = 0, 1, 2  # fold kinds: all pairs visible / u<=t diagonal / u<t diagonal
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact upcast of bfloat16 words (uint16) to float64."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------- layouts
+def positions(S: int, N: int, striped: bool) -> np.ndarray:
+    """Token position held by each shard-major row (length S, int64).
+
+    Contiguous sharding (aiunderstanding.org, "Immersione profonda": each
+    device owns a contiguous block of tokens): row p holds token p.
+    Striped (glossary page, Striped Attention: tokens spread evenly over the
+    devices, read as token t -> device t mod N, local row t div N): row
+    i*Sb + r holds token r*N + i.
+    """
+    if S % N:
+        raise ValueError("S must be a multiple of N")
+    Sb = S // N
+    p = np.arange(S, dtype=np.int64)
+    if not striped:
+        return p
+    i, r = p // Sb, p % Sb
+    return r * N + i
+
+
+def stripe_perm(S: int, N: int) -> np.ndarray:
+    """perm[p] = token held by shard-major row p under the striped layout."""
+    return positions(S, N, True)
+
+
+def to_shard_major(x_tok: np.ndarray, N: int, striped: bool) -> np.ndarray:
+    """Token order -> shard-major order along axis -2."""
+    return x_tok[..., positions(x_tok.shape[-2], N, striped), :]
+
+
+def to_token_order(x_sm: np.ndarray, N: int, striped: bool) -> np.ndarray:
+    """Shard-major order -> token order along axis -2 (inverse of to_shard_major)."""
+    pos = positions(x_sm.shape[-2], N, striped)
+    out = np.empty_like(x_sm)
+    out[..., pos, :] = x_sm
+    return out
+
+
+def _scale(D: int, scale) -> float:
+    return 1.0 / math.sqrt(D) if scale is None or scale <= 0 else float(scale)
+
+
+# ------------------------------------------------------- plain definition
+def attend_rows(qrows, qpos, k, v, kpos, causal: bool, scale: float):
+    """Exact softmax attention for a set of query rows (the plain definition).
+
+    For each query row t with position qpos[t], keys u with kpos[u] <= qpos[t]
+    are visible when ``causal`` (standard inclusive causal mask; the pages do
+    not state the convention, this is the oracle's reading), all keys
+    otherwise.  Returns
+        O[t]   = sum_u softmax_u(scale * q_t . k_u) v_u
+        lse[t] = ln sum_u exp(scale * q_t . k_u)
+    computed with the maximum subtracted before exp (the glossary page notes
+    production kernels do so; it changes nothing mathematically).  A row with
+    no visible key gets O = 0, lse = -inf.
+    """
+    qrows = np.asarray(qrows, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    s = (qrows @ k.T) * scale  # [R, Sk]
+    if causal:
+        vis = np.asarray(kpos)[None, :] <= np.asarray(qpos)[:, None]
+        s = np.where(vis, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    p = np.exp(s - m_safe)
+    l = p.sum(axis=1, keepdims=True)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        o = np.where(l > 0, (p @ v) / np.where(l > 0, l, 1.0), 0.0)
+        lse = np.where(l[:, 0] > 0, m_safe[:, 0] + np.log(l[:, 0]), -np.inf)
+    return o, lse
+
+
+def full_attention(q, k, v, causal: bool, scale=None, chunk: int = 512):
+    """Full softmax(scale * Q K^T) V over token-order tensors, float64.
+
+    q [B, Hq, S, D], k and v [B, Hkv, S, D].  Query rows are processed in
+    chunks of ``chunk`` rows only to bound memory; each chunk is the plain
+    definition (``attend_rows``).  Returns O [B, Hq, S, D], lse [B, Hq, S].
+    """
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    sc = _scale(D, scale)
+    o = np.empty((B, Hq, S, v.shape[-1]), dtype=np.float64)
+    lse = np.empty((B, Hq, S), dtype=np.float64)
+    pos = np.arange(S, dtype=np.int64)
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, h // g], v[b, h // g]
+            for r0 in range(0, S, chunk):
+                r1 = min(S, r0 + chunk)
+                hi = r1 if causal else S  # keys beyond the last row are invisible
+                o[b, h, r0:r1], lse[b, h, r0:r1] = attend_rows(
+                    q[b, h, r0:r1], pos[r0:r1], kh[:hi], vh[:hi], pos[:hi], causal, sc)
+    return o, lse
+
+
+# ------------------------------------------------------- ring-order loop
+def ring_attention(q, k, v, N: int, causal: bool, striped: bool, scale=None):
+    """Blockwise ring attention over shard-major tensors, float64.
+
+    Follows the glossary page ("Como funciona a atencao em anel") and the
+    aiunderstanding.org "Approfondimento tecnico" section: device i keeps
+    query block Q_i; at step s = 0..N-1 it holds key/value block
+    j = (i - s) mod N (received from the previous device, so step 0 is its
+    own block).  For each block it forms the scores scale * Q_i K_j^T, masks
+    pairs whose key position is after the query position (causal), and folds
+    them into a running max m, running normaliser l and numerator acc:
+        m'  = max(m, rowmax(scores))
+        acc = exp(m - m') * acc + exp(scores - m') @ V_j
+        l   = exp(m - m') * l   + rowsum(exp(scores - m'))
+    (with exp(m - m') taken as 0 while m = -inf).  Blocks with no visible
+    pair are skipped.  After the N steps O_i = acc / l and lse = m + ln l.
+    Returns O and lse in shard-major order.
+    """
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    Sb = S // N
+    sc = _scale(D, scale)
+    pos = positions(S, N, striped)
+    o = np.zeros((B, Hq, S, v.shape[-1]), dtype=np.float64)
+    lse = np.full((B, Hq, S), -np.inf, dtype=np.float64)
+    for b in range(B):
+        for h in range(Hq):
+            Q = np.asarray(q[b, h], dtype=np.float64)
+            K = np.asarray(k[b, h // g], dtype=np.float64)
+            V = np.asarray(v[b, h // g], dtype=np.float64)
+            for i in range(N):
+                qi = slice(i * Sb, (i + 1) * Sb)
+                m = np.full(Sb, -np.inf)
+                l = np.zeros(Sb)
+                acc = np.zeros((Sb, V.shape[1]))
+                for s in range(N):
+                    j = (i - s) % N
+                    kj = slice(j * Sb, (j + 1) * Sb)
+                    scores = (Q[qi] @ K[kj].T) * sc
+                    if causal:
+                        vis = pos[kj][None, :] <= pos[qi][:, None]
+                        if not vis.any():
+                            continue
+                        scores = np.where(vis, scores, -np.inf)
+                    m_new = np.maximum(m, scores.max(axis=1))
+                    m_use = np.where(np.isfinite(m_new), m_new, 0.0)
+                    alpha = np.where(np.isfinite(m), np.exp(m - m_use), 0.0)
+                    p = np.exp(scores - m_use[:, None])
+                    acc = alpha[:, None] * acc + p @ V[kj]
+                    l = alpha * l + p.sum(axis=1)
+                    m = m_new
+                with np.errstate(invalid="ignore", divide="ignore"):
+                    o[b, h, qi] = np.where(l[:, None] > 0, acc / np.where(l > 0, l, 1)[:, None], 0)
+                    lse[b, h, qi] = np.where(l > 0, m + np.log(np.where(l > 0, l, 1)), -np.inf)
+    return o, lse
+
+
+def merge(o_a, lse_a, o_b, lse_b):
+    """Combine two partial results over disjoint key sets A and B.
+
+    With lse_X = ln sum_{u in X} exp(score_u) and O_X the normalised partial
+    output, the result over A u B is the log-sum-exp weighting (the same
+    rescale-and-add the pages' online softmax performs when a block arrives):
+        lse = ln(exp(lse_a) + exp(lse_b))
+        O   = exp(lse_a - lse) O_a + exp(lse_b - lse) O_b
+    A partial over no visible key has lse = -inf and contributes nothing; if
+    both are empty the result is O = 0, lse = -inf.
+    """
+    lse_a = np.asarray(lse_a, dtype=np.float64)
+    lse_b = np.asarray(lse_b, dtype=np.float64)
+    mx = np.maximum(lse_a, lse_b)
+    mx_safe = np.where(np.isfinite(mx), mx, 0.0)
+    wa = np.exp(lse_a - mx_safe)
+    wb = np.exp(lse_b - mx_safe)
+    tot = wa + wb
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(tot > 0, mx_safe + np.log(np.where(tot > 0, tot, 1)), -np.inf)
+        ca = np.where(tot > 0, wa / np.where(tot > 0, tot, 1), 0.0)
+        cb = np.where(tot > 0, wb / np.where(tot > 0, tot, 1), 0.0)
+    o = ca[..., None] * np.asarray(o_a, np.float64) + cb[..., None] * np.asarray(o_b, np.float64)
+    return o, lse
+
+
+# ------------------------------------------------------------- schedule
+def fold_schedule(S: int, N: int, causal: bool, striped: bool, Tq: int, Tk: int,
+                  i_list=None, qt_list=None):
+    """Brute-force fold order of every query tile, from explicit positions.
+
+    For query shard i, query tile qt (rows [qt*Tq, (qt+1)*Tq) of the shard)
+    and ring step s = 0..N-1 with j = (i - s) mod N, walk the key tiles kt of
+    shard j in ascending order and classify the Tq x Tk pairs from their
+    token positions: no visible pair -> skipped (not listed); all visible ->
+    FULL; exactly the pairs with local key row <= local query row -> INCL;
+    exactly those with local key row < local query row -> STRICT.  Any other
+    pattern raises (the tile sizes do not fit the layout).
+
+    Returns a list of (i, qt, s, j, kt, kind) in fold order.
+    """
+    Sb = S // N
+    pos = positions(S, N, striped)
+    nq, nk = -(-Sb // Tq), -(-Sb // Tk)
+    out = []
+    for i in (range(N) if i_list is None else i_list):
+        for qt in (range(nq) if qt_list is None else qt_list):
+            r0, r1 = i * Sb + qt * Tq, i * Sb + min(Sb, (qt + 1) * Tq)
+            rl = np.arange(r1 - r0)
+            for s in range(N):
+                j = (i - s) % N
+                for kt in range(nk):
+                    c0, c1 = j * Sb + kt * Tk, j * Sb + min(Sb, (kt + 1) * Tk)
+                    cl = np.arange(c1 - c0)
+                    if causal:
+                        vis = pos[c0:c1][None, :] <= pos[r0:r1][:, None]
+                    else:
+                        vis = np.ones((r1 - r0, c1 - c0), dtype=bool)
+                    if not vis.any():
+                        continue
+                    if vis.all():
+                        kind = FULL
+                    elif (r1 - r0 == c1 - c0) and np.array_equal(vis, cl[None, :] <= rl[:, None]):
+                        kind = INCL
+                    elif (r1 - r0 == c1 - c0) and np.array_equal(vis, cl[None, :] < rl[:, None]):
+                        kind = STRICT
+                    else:
+                        raise ValueError(f"unclassifiable tile i={i} qt={qt} j={j} kt={kt}")
+                    out.append((i, qt, s, j, kt, kind))
+    return out
+
+
+# ----------------------------------------------------- the pages' toy
+def toy_ring_no_max(q, k, v, n_devices: int):
+    """The glossary page's four-device simulation, as its text describes it.
+
+    q, k, v are [n_devices * block, dim] in token order.  Device i keeps its
+    query block; at each step it takes the key/value block j = (i - step) mod
+    n_devices, adds exp(Q_i K_j^T / sqrt(dim)) @ V_j to a numerator and the
+    row sums of exp(...) to a denominator, and finally divides.  No running
+    maximum is subtracted (the page's simulation omits it).  float64.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    S, dim = q.shape
+    blk = S // n_devices
+    outs = []
+    for i in range(n_devices):
+        num = np.zeros((blk, v.shape[1]))
+        den = np.zeros((blk, 1))
+        Qi = q[i * blk:(i + 1) * blk]
+        for step in range(n_devices):
+            j = (i - step) % n_devices
+            e = np.exp(Qi @ k[j * blk:(j + 1) * blk].T / math.sqrt(dim))
+            num += e @ v[j * blk:(j + 1) * blk]
+            den += e.sum(axis=1, keepdims=True)
+        outs.append(num / den)
+    return np.concatenate(outs, axis=0)

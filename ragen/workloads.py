@@ -1,0 +1,72 @@
+"""The named attention workloads and their input recipe.
+
+Every workload draws q, k and v i.i.d. N(0, 1) from ``ragen`` with
+seed = 1000 * workload index and tensor ids 0 (q), 1 (k), 2 (v); bf16
+workloads round each sample to bfloat16 (nearest even).  Tensors are laid out
+shard-major: q is [B, Hq, S, D], k and v are [B, Hkv, S, D], and virtual
+device i of N owns rows [i*S/N, (i+1)*S/N) of every (b, h) slice.  Under the
+striped layout, row r of shard i holds token r*N + i.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+TENSOR_Q, TENSOR_K, TENSOR_V = 0, 1, 2
+
+
+@dataclass(frozen=True)
+class Workload:
+    index: int
+    name: str
+    dtype: str  # "f32" or "bf16"
+    B: int
+    Hq: int
+    Hkv: int
+    S: int
+    N: int
+    D: int
+    causal: bool
+    striped: bool
+
+    @property
+    def seed(self) -> int:
+        return 1000 * self.index
+
+    @property
+    def Sb(self) -> int:
+        return self.S // self.N
+
+    def flops(self) -> float:
+        """Attention FLOPs by the metric's convention: 4*B*Hq*S^2*D, halved if causal."""
+        f = 4.0 * self.B * self.Hq * self.S * self.S * self.D
+        return f / 2 if self.causal else f
+
+    def flops_exact(self) -> float:
+        """FLOPs over the visible (query, key) pairs only: S(S+1)/2 pairs if causal."""
+        pairs = self.S * (self.S + 1) / 2 if self.causal else float(self.S) * self.S
+        return 4.0 * self.B * self.Hq * pairs * self.D
+
+    def shapes(self):
+        return ((self.B, self.Hq, self.S, self.D), (self.B, self.Hkv, self.S, self.D))
+
+    def describe(self) -> dict:
+        return {
+            "workload": self.name, "dtype": self.dtype, "B": self.B, "Hq": self.Hq,
+            "Hkv": self.Hkv, "S": self.S, "N": self.N, "Sb": self.Sb, "D": self.D,
+            "causal": self.causal, "layout": "striped" if self.striped else "contiguous",
+        }
+
+
+WORKLOADS = {
+    "toy_f32": Workload(0, "toy_f32_N4_S32_D16", "f32", 1, 1, 1, 32, 4, 16, False, False),
+    "noncausal_8k": Workload(1, "bf16_noncausal_B1_H8_S8192_N8_D128", "bf16",
+                             1, 8, 8, 8192, 8, 128, False, False),
+    "causal_32k_contig": Workload(2, "bf16_causal_B2_H32_S32768_N8_D128_contiguous", "bf16",
+                                  2, 32, 32, 32768, 8, 128, True, False),
+    "causal_32k_striped": Workload(2, "bf16_causal_B2_H32_S32768_N8_D128_striped", "bf16",
+                                   2, 32, 32, 32768, 8, 128, True, True),
+    "gqa_128k": Workload(3, "bf16_causal_gqa_B1_Hq32_Hkv8_S131072_N16_D128_striped", "bf16",
+                         1, 32, 8, 131072, 16, 128, True, True),
+    "long_1m": Workload(4, "bf16_causal_gqa_B1_Hq8_Hkv1_S1048576_N64_D128_striped", "bf16",
+                        1, 8, 1, 1048576, 64, 128, True, True),
+}

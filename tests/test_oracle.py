@@ -1,0 +1,287 @@
+"""Pins for the CPU oracle: each checks it against something other than itself.
+
+* brute force on tiny inputs (pure-Python loops, no matrix ops);
+* closed forms (Q = 0 gives the mean of the visible values and lse = ln count;
+  V = 1 gives O = 1; a dominant key gives that key's value);
+* a library routine (torch scaled_dot_product_attention on CPU in float64);
+* the pages' worked example (the glossary page's four-device toy);
+* the pages' central claim (ring order == full attention), invariances
+  (permutation equivariance without a mask, striped vs contiguous);
+* the log-sum-exp merge identity;
+* tile-count closed forms for the fold schedule and exact pair coverage.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle.attention import FULL, INCL, STRICT
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def brute(q, k, v, causal, scale):
+    """Pure-Python triple loop over token-order [S, D] inputs of one head."""
+    S, D = len(q), len(q[0])
+    out, lses = [], []
+    for t in range(S):
+        sc = []
+        for u in range(S):
+            if causal and u > t:
+                continue
+            sc.append((u, scale * sum(q[t][d] * k[u][d] for d in range(D))))
+        mx = max(x for _, x in sc)
+        w = [(u, math.exp(x - mx)) for u, x in sc]
+        z = sum(x for _, x in w)
+        out.append([sum(wu * v[u][d] for u, wu in w) / z for d in range(len(v[0]))])
+        lses.append(mx + math.log(z))
+    return np.array(out), np.array(lses)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (4, 2), (3, 1)])
+def test_full_matches_brute_force(causal, Hq, Hkv):
+    S, D = 12, 5
+    q, k, v = rnd((1, Hq, S, D), 1), rnd((1, Hkv, S, D), 2), rnd((1, Hkv, S, D), 3)
+    o, lse = oracle.full_attention(q, k, v, causal, chunk=5)
+    g = Hq // Hkv
+    for h in range(Hq):
+        ob, lb = brute(q[0, h].tolist(), k[0, h // g].tolist(), v[0, h // g].tolist(),
+                       causal, 1 / math.sqrt(D))
+        np.testing.assert_allclose(o[0, h], ob, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[0, h], lb, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("striped", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_matches_brute_force(causal, striped):
+    S, D, N = 16, 4, 4
+    q, k, v = rnd((1, 2, S, D), 4), rnd((1, 1, S, D), 5), rnd((1, 1, S, D), 6)
+    qs, ks, vs = (oracle.to_shard_major(x, N, striped) for x in (q, k, v))
+    o_sm, lse_sm = oracle.ring_attention(qs, ks, vs, N, causal, striped)
+    o = oracle.to_token_order(o_sm, N, striped)
+    lse = oracle.to_token_order(lse_sm[..., None], N, striped)[..., 0]
+    for h in range(2):
+        ob, lb = brute(q[0, h].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), causal, 0.5)
+        np.testing.assert_allclose(o[0, h], ob, atol=1e-12, rtol=0)
+        np.testing.assert_allclose(lse[0, h], lb, atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("striped", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_query_closed_form(causal, striped):
+    """Q = 0 makes every visible key equally likely: O is the mean of the
+    visible values (the prefix mean under the causal mask) and lse = ln(count)."""
+    S, D, N = 24, 8, 4
+    q = np.zeros((1, 1, S, D))
+    k, v = rnd((1, 1, S, D), 7), rnd((1, 1, S, D), 8)
+    qs, ks, vs = (oracle.to_shard_major(x, N, striped) for x in (q, k, v))
+    o_sm, lse_sm = oracle.ring_attention(qs, ks, vs, N, causal, striped)
+    o = oracle.to_token_order(o_sm, N, striped)[0, 0]
+    lse = oracle.to_token_order(lse_sm[..., None], N, striped)[0, 0, :, 0]
+    o_f, lse_f = oracle.full_attention(q, k, v, causal)
+    for t in range(S):
+        cnt = t + 1 if causal else S
+        exp_o = v[0, 0, :cnt].mean(axis=0)
+        np.testing.assert_allclose(o[t], exp_o, atol=1e-13)
+        np.testing.assert_allclose(o_f[0, 0, t], exp_o, atol=1e-13)
+        assert abs(lse[t] - math.log(cnt)) < 1e-13
+        assert abs(lse_f[0, 0, t] - math.log(cnt)) < 1e-13
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_sum_to_one(causal):
+    """V = 1: attention weights of every row sum to 1, so O = 1 exactly-ish."""
+    S, D, N = 32, 8, 4
+    q, k = rnd((2, 2, S, D), 9) * 3, rnd((2, 2, S, D), 10) * 3
+    v = np.ones((2, 2, S, D))
+    for striped in (False, True):
+        o, _ = oracle.ring_attention(q, k, v, N, causal, striped)
+        np.testing.assert_allclose(o, 1.0, atol=1e-13)
+    o, _ = oracle.full_attention(q, k, v, causal)
+    np.testing.assert_allclose(o, 1.0, atol=1e-13)
+
+
+def test_dominant_key_selects_its_value():
+    """k_u = c * q_t with large c: row t attends (almost) only to key u."""
+    S, D = 16, 8
+    q, k, v = rnd((1, 1, S, D), 11), rnd((1, 1, S, D), 12) * 0.01, rnd((1, 1, S, D), 13)
+    t, u = 11, 4
+    k[0, 0, u] = 200.0 * q[0, 0, t]
+    o, lse = oracle.full_attention(q, k, v, causal=True)
+    np.testing.assert_allclose(o[0, 0, t], v[0, 0, u], atol=1e-9)
+    expect = 200.0 * float(q[0, 0, t] @ q[0, 0, t]) / math.sqrt(D)
+    assert abs(lse[0, 0, t] - expect) < 1e-6
+    o2, _ = oracle.ring_attention(q, k, v, 4, True, False)
+    np.testing.assert_allclose(o2[0, 0, t], v[0, 0, u], atol=1e-9)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_library_sdpa_crosscheck(causal):
+    """torch's CPU scaled_dot_product_attention in float64 (GQA by repeating kv heads)."""
+    torch = pytest.importorskip("torch")
+    B, Hq, Hkv, S, D = 2, 4, 2, 40, 16
+    q, k, v = rnd((B, Hq, S, D), 14), rnd((B, Hkv, S, D), 15), rnd((B, Hkv, S, D), 16)
+    o, _ = oracle.full_attention(q, k, v, causal, chunk=16)
+    tk = torch.from_numpy(k).repeat_interleave(Hq // Hkv, dim=1)
+    tv = torch.from_numpy(v).repeat_interleave(Hq // Hkv, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), tk, tv, is_causal=causal).numpy()
+    np.testing.assert_allclose(o, ref, atol=1e-12, rtol=0)
+    for striped in (False, True):
+        qs, ks, vs = (oracle.to_shard_major(x, 5, striped) for x in (q, k, v))
+        o_sm, _ = oracle.ring_attention(qs, ks, vs, 5, causal, striped)
+        np.testing.assert_allclose(oracle.to_token_order(o_sm, 5, striped), ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 8])
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])
+def test_ring_equals_full(N, causal, striped):
+    """The pages' central claim: the ring-order blockwise fold equals full attention."""
+    S, D = 48, 8
+    q, k, v = rnd((1, 4, S, D), 17), rnd((1, 2, S, D), 18), rnd((1, 2, S, D), 19)
+    o_f, lse_f = oracle.full_attention(q, k, v, causal)
+    qs, ks, vs = (oracle.to_shard_major(x, N, striped) for x in (q, k, v))
+    o_sm, lse_sm = oracle.ring_attention(qs, ks, vs, N, causal, striped)
+    np.testing.assert_allclose(oracle.to_token_order(o_sm, N, striped), o_f, atol=1e-12)
+    lse_tok = oracle.to_token_order(lse_sm[..., None], N, striped)[..., 0]
+    np.testing.assert_allclose(lse_tok, lse_f, atol=1e-12)
+
+
+def test_permutation_equivariance_noncausal():
+    """Without a mask: permuting keys/values jointly changes nothing, and
+    permuting queries permutes the output rows."""
+    S, D = 32, 8
+    q, k, v = rnd((1, 1, S, D), 20), rnd((1, 1, S, D), 21), rnd((1, 1, S, D), 22)
+    pq = np.random.default_rng(0).permutation(S)
+    pk = np.random.default_rng(1).permutation(S)
+    o, lse = oracle.ring_attention(q, k, v, 4, False, False)
+    o2, lse2 = oracle.ring_attention(q[..., pq, :], k[..., pk, :], v[..., pk, :], 4, False, False)
+    np.testing.assert_allclose(o2, o[..., pq, :], atol=1e-12)
+    np.testing.assert_allclose(lse2, lse[..., pq], atol=1e-12)
+
+
+def test_striped_equals_contiguous_after_unpermuting():
+    S, D, N = 64, 8, 8
+    q, k, v = rnd((1, 2, S, D), 23), rnd((1, 1, S, D), 24), rnd((1, 1, S, D), 25)
+    o_c, lse_c = oracle.ring_attention(q, k, v, N, True, False)  # token order == contiguous
+    qs, ks, vs = (oracle.to_shard_major(x, N, True) for x in (q, k, v))
+    o_s, lse_s = oracle.ring_attention(qs, ks, vs, N, True, True)
+    np.testing.assert_allclose(oracle.to_token_order(o_s, N, True), o_c, atol=1e-12)
+    np.testing.assert_allclose(oracle.to_token_order(lse_s[..., None], N, True)[..., 0], lse_c,
+                               atol=1e-12)
+
+
+def test_stripe_permutation_examples():
+    """token t sits on device t mod N at local row t div N."""
+    assert oracle.stripe_perm(8, 4).tolist() == [0, 4, 1, 5, 2, 6, 3, 7]
+    assert oracle.stripe_perm(6, 2).tolist() == [0, 2, 4, 1, 3, 5]
+    assert oracle.stripe_perm(5, 1).tolist() == [0, 1, 2, 3, 4]
+    x = rnd((2, 3, 24, 2), 26)
+    for striped in (False, True):
+        np.testing.assert_array_equal(
+            oracle.to_token_order(oracle.to_shard_major(x, 4, striped), 4, striped), x)
+
+
+def test_merge_identity():
+    """merge(partial over keys A, partial over keys B) == result over A u B."""
+    S, D = 20, 6
+    q, k, v = rnd((S, D), 27), rnd((S, D), 28), rnd((S, D), 29)
+    pos = np.arange(S)
+    rng = np.random.default_rng(3)
+    maskA = rng.random(S) < 0.5
+    A, Bm = np.where(maskA)[0], np.where(~maskA)[0]
+    oa, la = oracle.attend_rows(q, pos, k[A], v[A], A, True, 0.4)
+    ob, lb = oracle.attend_rows(q, pos, k[Bm], v[Bm], Bm, True, 0.4)
+    o, l = oracle.merge(oa, la, ob, lb)
+    of, lf = oracle.attend_rows(q, pos, k, v, pos, True, 0.4)
+    np.testing.assert_allclose(o, of, atol=1e-12)
+    np.testing.assert_allclose(l, lf, atol=1e-12)
+    # some rows saw nothing in A or in B (lse = -inf partials)
+    assert np.isneginf(la).any() or np.isneginf(lb).any()
+    # both empty -> (0, -inf); commutative
+    z, zl = oracle.merge(np.zeros((1, D)), [-np.inf], np.zeros((1, D)), [-np.inf])
+    assert np.all(z == 0) and np.isneginf(zl).all()
+    o2, l2 = oracle.merge(ob, lb, oa, la)
+    np.testing.assert_allclose(o2, o, atol=1e-15)
+    np.testing.assert_allclose(l2, l, atol=1e-15)
+
+
+def test_toy_worked_example():
+    """The glossary page's four-device simulation: blockwise == full at atol 1e-5."""
+    torch = pytest.importorskip("torch")
+    with open(os.path.join(GOLDEN, "toy_glossary_page.json")) as f:
+        g = json.load(f)
+    n, blk, dim = g["n_devices"], g["block"], g["dim"]
+    torch.manual_seed(g["torch_seed"])
+    q, k, v = torch.randn(3, n * blk, dim)
+    full = (torch.softmax(q @ k.T / dim ** 0.5, dim=-1) @ v).numpy()
+    toy = oracle.toy_ring_no_max(q.numpy(), k.numpy(), v.numpy(), n)
+    assert np.allclose(toy, full, atol=g["atol"]) == g["matches_full_attention"]
+    ring, _ = oracle.ring_attention(q.numpy()[None, None], k.numpy()[None, None],
+                                    v.numpy()[None, None], n, False, False)
+    assert np.allclose(ring[0, 0], full, atol=g["atol"]) == g["matches_full_attention"]
+    np.testing.assert_allclose(ring[0, 0], toy, atol=1e-12)
+    assert [blk, blk] == g["largest_score_block_per_device"]
+    assert [n * blk, n * blk] == g["full_score_matrix"]
+
+
+# ----------------------------------------------------------------- schedule
+def _covered_pairs(S, N, causal, striped, T, sched):
+    pos = oracle.positions(S, N, striped)
+    Sb = S // N
+    cover = np.zeros((S, S), dtype=np.int64)
+    for (i, qt, s, j, kt, kind) in sched:
+        assert j == (i - s) % N
+        r = np.arange(i * Sb + qt * T, i * Sb + (qt + 1) * T)
+        c = np.arange(j * Sb + kt * T, j * Sb + (kt + 1) * T)
+        rl, cl = np.arange(T)[:, None], np.arange(T)[None, :]
+        vis = {FULL: np.ones((T, T), bool), INCL: cl <= rl, STRICT: cl < rl}[kind]
+        cover[np.ix_(r, c)] += vis
+    want = (pos[None, :] <= pos[:, None]) if causal else np.ones((S, S), bool)
+    return cover, want
+
+
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])
+def test_schedule_covers_each_visible_pair_once(causal, striped):
+    S, N, T = 256, 4, 16
+    sched = oracle.fold_schedule(S, N, causal, striped, T, T)
+    cover, want = _covered_pairs(S, N, causal, striped, T, sched)
+    np.testing.assert_array_equal(cover, want.astype(np.int64))
+    # fold order: ring steps ascending, key tiles ascending within a step
+    by_tile = {}
+    for e in sched:
+        by_tile.setdefault(e[:2], []).append((e[2], e[4]))
+    for lst in by_tile.values():
+        assert lst == sorted(lst)
+
+
+def test_schedule_tile_counts_closed_form():
+    """Live tiles per (b, h): contiguous causal n(n+1)/2 with n = S/T; striped
+    causal N^2 * m(m+1)/2 with m = Sb/T; non-causal (S/T)^2."""
+    S, N, T = 2048, 8, 32
+    n, m = S // T, S // N // T
+    assert len(oracle.fold_schedule(S, N, True, False, T, T)) == n * (n + 1) // 2
+    assert len(oracle.fold_schedule(S, N, True, True, T, T)) == N * N * m * (m + 1) // 2
+    assert len(oracle.fold_schedule(S, N, False, False, T, T)) == n * n
+    # the 32K-token, 8-device layouts at 128-token tiles, from one query shard per
+    # kind of pair to keep it fast: shard 3 (contiguous) sees 3 full blocks + diagonal
+    S, N, T = 32768, 8, 128
+    m = S // N // T
+    c3 = oracle.fold_schedule(S, N, True, False, T, T, i_list=[3])
+    assert len(c3) == 3 * m * m + m * (m + 1) // 2
+    s3 = oracle.fold_schedule(S, N, True, True, T, T, i_list=[3], qt_list=[0, 5, 31])
+    assert len(s3) == sum(N * (qt + 1) for qt in (0, 5, 31))
+    kinds = {(e[3] <= 3, e[4] == e[1]): e[5] for e in s3}
+    assert kinds[(True, True)] == INCL and kinds[(False, True)] == STRICT
+    assert kinds[(True, False)] == FULL and kinds[(False, False)] == FULL
+    # and the per-(b, h) totals of the 32K layouts follow from the formulas above
+    assert 8 * m * (m + 1) // 2 + 28 * m * m == 32896
+    assert N * N * m * (m + 1) // 2 == 33792
