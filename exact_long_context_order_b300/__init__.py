@@ -1,0 +1,231 @@
+"""Ring attention (exact blockwise self-attention over N virtual ring devices)
+on one B300, as a C-ABI shared library with a thin ctypes binding.
+
+The functions named ``ra_*`` mirror ``include/ra.h`` one to one: plain
+integers and pointers in, an RA_* status out; they only marshal arguments.
+``forward``, ``merge``, ``stripe`` and ``plan`` are conveniences over them
+for torch CUDA tensors (PyTorch is used only for device memory and streams);
+every step of the computation runs in the library's CUDA kernels.
+
+If ``libra.so`` has not been built, every call raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libra.so")
+
+RA_OK, RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED, RA_ERR_ALIGN = 0, 1, 2, 3
+RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_ERR_BOUNDS, RA_ERR_CAPACITY = 4, 5, 6, 7
+RA_BF16, RA_F32 = 0, 1
+RA_KERNEL_AUTO, RA_KERNEL_TC, RA_KERNEL_SIMT = 0, 1, 2
+RA_FOLD_FULL, RA_FOLD_INCL, RA_FOLD_STRICT = 0, 1, 2
+
+_c = ctypes
+_vp, _i32, _i64, _f32 = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_float
+_SIGNATURES = {
+    "ra_forward": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
+                    _f32, _i32, _vp], _i32),
+    "ra_forward_ex": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
+                       _f32, _i32, _i32, _vp], _i32),
+    "ra_merge": ([_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp], _i32),
+    "ra_stripe": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _vp], _i32),
+    "ra_plan": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)], _i32),
+    "ra_fold_log": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
+                     _f32, _vp, _vp, _i32, _vp], _i32),
+    "ra_check": ([_vp], _i32),
+    "ra_strerror": ([_i32], _c.c_char_p),
+    "ra_tile_config": ([_c.POINTER(_i32), _c.POINTER(_i32)], _i32),
+    "ra_version": ([], _i32),
+}
+
+_lib = None
+
+
+class RAError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {ra_strerror(code)} (status {code})")
+
+
+def lib():
+    """The loaded libra.so (raises if it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -m exact_long_context_order_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------ raw C ABI
+def ra_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, dtype, stream):
+    return lib().ra_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale,
+                            dtype, stream)
+
+
+def ra_forward_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, dtype, kernel,
+                  stream):
+    return lib().ra_forward_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale,
+                               dtype, kernel, stream)
+
+
+def ra_merge(out_a, lse_a, out_b, lse_b, rows, D, dtype, stream):
+    return lib().ra_merge(out_a, lse_a, out_b, lse_b, rows, D, dtype, stream)
+
+
+def ra_stripe(src, dst, BH, S, N, row_bytes, inverse, stream):
+    return lib().ra_stripe(src, dst, BH, S, N, row_bytes, inverse, stream)
+
+
+def ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items):
+    return lib().ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items)
+
+
+def ra_fold_log(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, log, counts,
+                max_entries, stream):
+    return lib().ra_fold_log(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, log,
+                             counts, max_entries, stream)
+
+
+def ra_check(stream):
+    return lib().ra_check(stream)
+
+
+def ra_strerror(code: int) -> str:
+    return lib().ra_strerror(code).decode()
+
+
+def ra_tile_config():
+    tq, tk = _i32(), _i32()
+    lib().ra_tile_config(ctypes.byref(tq), ctypes.byref(tk))
+    return tq.value, tk.value
+
+
+def ra_version() -> int:
+    return lib().ra_version()
+
+
+# ------------------------------------------------------------ torch helpers
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != RA_OK:
+        raise RAError(rc, where)
+
+
+_KERNELS = {"auto": RA_KERNEL_AUTO, "tc": RA_KERNEL_TC, "simt": RA_KERNEL_SIMT}
+
+
+def forward(q, k, v, N: int, causal: bool = False, striped: bool = False, scale=None, out=None,
+            lse=None, want_lse: bool = True, kernel: str = "auto", stream=None):
+    """Ring attention over shard-major torch CUDA tensors.
+
+    q [B, Hq, S, D], k and v [B, Hkv, S, D], all bf16 or all float32,
+    contiguous, on the current device.  Returns (out, lse): out like q, lse
+    [B, Hq, S] float32 (None when want_lse is False and lse is None).
+    """
+    import torch
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if q.dtype == torch.bfloat16:
+        dtype = RA_BF16
+    elif q.dtype == torch.float32:
+        dtype = RA_F32
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    for t in (k, v):
+        if t.dtype != q.dtype or t.shape != (B, Hkv, S, D) or not t.is_contiguous():
+            raise ValueError("k and v must be contiguous [B, Hkv, S, D] of q's dtype")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    rc = ra_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, N,
+                       int(causal), int(striped), float(scale or 0.0), dtype, _KERNELS[kernel],
+                       _stream_handle(stream))
+    _check(rc, "ra_forward")
+    return out, lse
+
+
+def fold_log(q, k, v, N: int, causal: bool, striped: bool, scale=None, stream=None):
+    """Runs the logging variant of the tensor-core kernel.
+
+    Returns (out, lse, log, counts): log is int32 [tiles, N*Sb/128, 4] with
+    (s, j, kt, kind) per live fold of each query tile, tiles indexed
+    ((b*Hq + h)*N + i)*(Sb/128) + qt; counts int32 [tiles].
+    """
+    import torch
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    nt = S // N // 128
+    tiles = B * Hq * N * nt
+    max_entries = N * nt
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    log = torch.full((tiles, max_entries, 4), -1, dtype=torch.int32, device=q.device)
+    counts = torch.full((tiles,), -1, dtype=torch.int32, device=q.device)
+    rc = ra_fold_log(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, S, D, N,
+                     int(causal), int(striped), float(scale or 0.0), _ptr(log), _ptr(counts),
+                     max_entries, _stream_handle(stream))
+    _check(rc, "ra_fold_log")
+    return out, lse, log, counts
+
+
+def merge(out_a, lse_a, out_b, lse_b, stream=None):
+    """In place: (out_a, lse_a) <- merge of the two partials (torch CUDA tensors)."""
+    import torch
+    D = out_a.shape[-1]
+    rows = out_a.numel() // D
+    dtype = RA_BF16 if out_a.dtype == torch.bfloat16 else RA_F32
+    rc = ra_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), rows, D, dtype,
+                  _stream_handle(stream))
+    _check(rc, "ra_merge")
+    return out_a, lse_a
+
+
+def stripe(x, N: int, inverse: bool = False, out=None, stream=None):
+    """Token order <-> striped shard-major order along dim -2 of [..., S, D]."""
+    import torch
+    S = x.shape[-2]
+    row_bytes = x.shape[-1] * x.element_size()
+    BH = x.numel() // (S * x.shape[-1])
+    if out is None:
+        out = torch.empty_like(x)
+    rc = ra_stripe(_ptr(x), _ptr(out), BH, S, N, row_bytes, int(inverse), _stream_handle(stream))
+    _check(rc, "ra_stripe")
+    return out
+
+
+def plan(S: int, N: int, causal: bool, striped: bool, i: int, qt: int, tile: int = 128):
+    """Host-side fold list of query tile (i, qt): list of (s, j, kt, kind)."""
+    n = _i64()
+    _check(ra_plan(S, N, int(causal), int(striped), tile, i, qt, None, 0, ctypes.byref(n)),
+           "ra_plan")
+    buf = (ctypes.c_int32 * (4 * max(1, n.value)))()
+    _check(ra_plan(S, N, int(causal), int(striped), tile, i, qt, buf, n.value, ctypes.byref(n)),
+           "ra_plan")
+    return [tuple(buf[4 * e:4 * e + 4]) for e in range(n.value)]
+
+
+def check(stream=None):
+    """Synchronise and raise if a kernel recorded a device-side failure."""
+    _check(ra_check(_stream_handle(stream)), "ra_check")

@@ -1,0 +1,42 @@
+// Internal launch interface between the C-ABI layer (ra_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace ra {
+
+// Bits of the device status word (one per device, read by ra_check).
+enum : unsigned int { kStatusTimeout = 1u, kStatusBounds = 2u };
+
+struct FwdProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    float* lse;
+    int B, Hq, Hkv;
+    int64_t S;
+    int D, N, causal, striped;
+    float scale;  // resolved (> 0)
+    int dtype;    // RA_BF16 / RA_F32
+};
+
+struct FoldLog {
+    int32_t* log;
+    int32_t* counts;
+    int max_entries;
+};
+
+// Returns 0 on success or an RA_ERR_* code.  status: device pointer to this
+// device's status word.  sm_count: multiprocessors of the current device.
+int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, int sm_count,
+              cudaStream_t stream);
+bool tc_supported(const FwdProblem& p);
+int launch_simt(const FwdProblem& p, unsigned int* status, cudaStream_t stream);
+int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
+                 int D, int dtype, cudaStream_t stream);
+int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
+                  int inverse, cudaStream_t stream);
+
+}  // namespace ra

@@ -1,0 +1,242 @@
+// C ABI of the ring-attention library: argument validation, the per-device
+// status word, kernel dispatch and the host-side fold planner.  Every entry
+// point returns an RA_* status and never throws.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ra.h"
+#include "schedule.cuh"
+
+namespace {
+
+// One status word per device, set by kernels (bounded waits that ran out,
+// bounds checks) and read/cleared by ra_check.
+__device__ unsigned int g_ra_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
+thread_local char g_cuda_msg[256] = "";
+
+void note_cuda(cudaError_t e) {
+    snprintf(g_cuda_msg, sizeof(g_cuda_msg), "%s", cudaGetErrorString(e));
+}
+
+// Resolves this device's status word address, SM count and architecture.
+int device_state(unsigned int** status, int* sm_count) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { note_cuda(e); return RA_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
+            note_cuda(e);
+            return RA_ERR_CUDA;
+        }
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_arch_ok[dev] != 1) return RA_ERR_UNSUPPORTED;
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_ra_status)) != cudaSuccess) { note_cuda(e); return RA_ERR_CUDA; }
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    if (status) *status = g_status_ptr[dev];
+    if (sm_count) *sm_count = g_sm_count[dev];
+    return RA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int64_t S, int D, int N, int dtype) {
+    if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
+    if (S % N != 0 || Hq % Hkv != 0) return RA_ERR_INVALID_ARG;
+    if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_INVALID_ARG;
+    if (D > 256) return RA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_ALIGN;
+    if (lse && !aligned16(lse)) return RA_ERR_ALIGN;
+    return RA_OK;
+}
+
+ra::FwdProblem make_problem(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int B, int Hq, int Hkv, int64_t S, int D, int N, int causal,
+                            int striped, float scale, int dtype) {
+    ra::FwdProblem p;
+    p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.N = N;
+    p.causal = causal ? 1 : 0;
+    p.striped = striped ? 1 : 0;
+    p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
+    p.dtype = dtype;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                  int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
+                  int dtype, int kernel, void* stream) {
+    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, dtype);
+    if (rc) return rc;
+    if (kernel != RA_KERNEL_AUTO && kernel != RA_KERNEL_TC && kernel != RA_KERNEL_SIMT)
+        return RA_ERR_INVALID_ARG;
+    unsigned int* status = nullptr;
+    int sms = 0;
+    if ((rc = device_state(&status, &sms))) return rc;
+    const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
+                                          scale, dtype);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool tc_ok = ra::tc_supported(p);
+    if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
+    if (kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok))
+        rc = ra::launch_tc(p, nullptr, status, sms, st);
+    else
+        rc = ra::launch_simt(p, status, st);
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
+int ra_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+               int Hkv, int64_t S, int D, int N, int causal, int striped, float scale, int dtype,
+               void* stream) {
+    return ra_forward_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, dtype,
+                         RA_KERNEL_AUTO, stream);
+}
+
+int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
+                int32_t* log, int32_t* counts, int max_entries, void* stream) {
+    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16);
+    if (rc) return rc;
+    if (!log || !counts || !aligned16(log) || ((uintptr_t)counts & 3u)) return RA_ERR_INVALID_ARG;
+    const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
+                                          scale, RA_BF16);
+    if (!ra::tc_supported(p)) return RA_ERR_UNSUPPORTED;
+    if ((int64_t)max_entries < (int64_t)N * (S / N / 128)) return RA_ERR_CAPACITY;
+    unsigned int* status = nullptr;
+    int sms = 0;
+    if ((rc = device_state(&status, &sms))) return rc;
+    ra::FoldLog fl{log, counts, max_entries};
+    rc = ra::launch_tc(p, &fl, status, sms, static_cast<cudaStream_t>(stream));
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
+int ra_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
+             int D, int dtype, void* stream) {
+    if (rows < 0 || D <= 0 || D > 1024) return RA_ERR_INVALID_ARG;
+    if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_INVALID_ARG;
+    if (rows == 0) return RA_OK;
+    if (!out_a || !lse_a || !out_b || !lse_b) return RA_ERR_INVALID_ARG;
+    if (!aligned16(out_a) || !aligned16(out_b) || ((uintptr_t)lse_a & 3u) || ((uintptr_t)lse_b & 3u))
+        return RA_ERR_ALIGN;
+    int rc = device_state(nullptr, nullptr);
+    if (rc) return rc;
+    rc = ra::launch_merge(out_a, lse_a, out_b, lse_b, rows, D, dtype, static_cast<cudaStream_t>(stream));
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
+int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
+              int inverse, void* stream) {
+    if (BH < 0 || S < 0 || N <= 0 || row_bytes <= 0 || row_bytes % 4) return RA_ERR_INVALID_ARG;
+    if (S % N) return RA_ERR_INVALID_ARG;
+    if (BH == 0 || S == 0) return RA_OK;
+    if (!src || !dst) return RA_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return RA_ERR_ALIGN;
+    const char* s = static_cast<const char*>(src);
+    char* d = static_cast<char*>(dst);
+    const int64_t bytes = BH * S * row_bytes;
+    if (s < d + bytes && d < s + bytes) return RA_ERR_INVALID_ARG;  // overlap
+    int rc = device_state(nullptr, nullptr);
+    if (rc) return rc;
+    rc = ra::launch_stripe(src, dst, BH, S, N, row_bytes, inverse ? 1 : 0,
+                           static_cast<cudaStream_t>(stream));
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
+int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, int32_t* items,
+            int64_t cap, int64_t* n_items) {
+    if (!n_items || S <= 0 || N <= 0 || tile < 2 || S % N) return RA_ERR_INVALID_ARG;
+    const int64_t Sb = S / N;
+    if (Sb % tile) return RA_ERR_INVALID_ARG;
+    const int64_t nt = Sb / tile;
+    if (nt > 0x7fffffff || i < 0 || i >= N || qt < 0 || qt >= nt) return RA_ERR_INVALID_ARG;
+    ra::RingGeom g{N, (int)nt, causal ? 1 : 0, striped ? 1 : 0};
+    int64_t n = 0;
+    for (int s = 0; s < N; ++s) {
+        const int j = ((i - s) % N + N) % N;
+        int nk = 0, dk = 0;
+        ra::shard_span(g, i, j, qt, &nk, &dk);
+        for (int kt = 0; kt < nk; ++kt) {
+            if (items && n < cap) {
+                int32_t* e = items + n * 4;
+                e[0] = s;
+                e[1] = j;
+                e[2] = kt;
+                e[3] = ra::fold_kind(g, i, j, qt, kt);
+            }
+            ++n;
+        }
+    }
+    *n_items = n;
+    return (items && n > cap) ? RA_ERR_CAPACITY : RA_OK;
+}
+
+int ra_check(void* stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { note_cuda(e); return RA_ERR_CUDA; }
+    unsigned int* status = nullptr;
+    int rc = device_state(&status, nullptr);
+    if (rc) return rc;
+    unsigned int st = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&st, g_ra_status, sizeof(st))) != cudaSuccess ||
+        (e = cudaMemcpyToSymbol(g_ra_status, &zero, sizeof(zero))) != cudaSuccess) {
+        note_cuda(e);
+        return RA_ERR_CUDA;
+    }
+    if (st & ra::kStatusTimeout) return RA_ERR_TIMEOUT;
+    if (st & ra::kStatusBounds) return RA_ERR_BOUNDS;
+    return RA_OK;
+}
+
+const char* ra_strerror(int code) {
+    switch (code) {
+        case RA_OK: return "ok";
+        case RA_ERR_INVALID_ARG: return "invalid argument";
+        case RA_ERR_UNSUPPORTED: return "unsupported shape, dtype or device";
+        case RA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case RA_ERR_CUDA: return g_cuda_msg[0] ? g_cuda_msg : "CUDA runtime error";
+        case RA_ERR_TIMEOUT: return "a kernel wait timed out";
+        case RA_ERR_BOUNDS: return "a kernel bounds check failed";
+        case RA_ERR_CAPACITY: return "output array too small";
+        default: return "unknown status";
+    }
+}
+
+int ra_tile_config(int* tq, int* tk) {
+    if (tq) *tq = 128;
+    if (tk) *tk = 128;
+    return RA_OK;
+}
+
+int ra_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+// Memory-bound helpers around the ring fold:
+//  * merge  -- fold one partial attention result (O_b, lse_b) over a disjoint
+//              key set into another (O_a, lse_a): the log-sum-exp weighted
+//              rescale-and-add that the online softmax performs when a new
+//              block arrives (aiunderstanding.org, "Approfondimento
+//              tecnico"; glossary page, running-max remark).
+//  * stripe -- bit-exact row permutation between token order and the striped
+//              shard-major order, token t <-> row (t mod N)*Sb + t div N
+//              (glossary page, Striped Attention).
+// Both are one warp per row, 16-byte vector accesses where the row allows.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ra.h"
+
+namespace ra {
+namespace aux {
+
+constexpr int kBlock = 256;
+
+template <typename T>
+struct Vec;  // 16-byte vector of T
+template <>
+struct Vec<float> {
+    static constexpr int n = 4;
+    __device__ static void fma2(uint4& a, const uint4& b, float ca, float cb) {
+        a.x = __float_as_uint(ca * __uint_as_float(a.x) + cb * __uint_as_float(b.x));
+        a.y = __float_as_uint(ca * __uint_as_float(a.y) + cb * __uint_as_float(b.y));
+        a.z = __float_as_uint(ca * __uint_as_float(a.z) + cb * __uint_as_float(b.z));
+        a.w = __float_as_uint(ca * __uint_as_float(a.w) + cb * __uint_as_float(b.w));
+    }
+};
+__device__ __forceinline__ uint32_t mix_bf16x2(uint32_t a, uint32_t b, float ca, float cb) {
+    __nv_bfloat162 va = *reinterpret_cast<__nv_bfloat162*>(&a);
+    __nv_bfloat162 vb = *reinterpret_cast<__nv_bfloat162*>(&b);
+    float2 fa = __bfloat1622float2(va), fb = __bfloat1622float2(vb);
+    __nv_bfloat162 r = __floats2bfloat162_rn(ca * fa.x + cb * fb.x, ca * fa.y + cb * fb.y);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int n = 8;
+    __device__ static void fma2(uint4& a, const uint4& b, float ca, float cb) {
+        a.x = mix_bf16x2(a.x, b.x, ca, cb);
+        a.y = mix_bf16x2(a.y, b.y, ca, cb);
+        a.z = mix_bf16x2(a.z, b.z, ca, cb);
+        a.w = mix_bf16x2(a.w, b.w, ca, cb);
+    }
+};
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f(float& d, float x) { d = x; }
+__device__ __forceinline__ void from_f(__nv_bfloat16& d, float x) { d = __float2bfloat16_rn(x); }
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kBlock) merge_kernel(T* __restrict__ oa, float* __restrict__ la,
+                                                       const T* __restrict__ ob,
+                                                       const float* __restrict__ lb, int64_t rows,
+                                                       int D) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (kBlock / 32);
+    for (int64_t row = (int64_t)blockIdx.x * (kBlock / 32) + threadIdx.x / 32; row < rows;
+         row += warps) {
+        const float a = la[row], b = lb[row];
+        const float mx = fmaxf(a, b);
+        float ca = 0.f, cb = 0.f, lse = -INFINITY;
+        if (mx != -INFINITY) {
+            const float wa = expf(a - mx), wb = expf(b - mx);  // exp(-inf) = 0
+            const float tot = wa + wb;
+            lse = mx + logf(tot);
+            ca = wa / tot;
+            cb = wb / tot;
+        }
+        T* ra_ = oa + row * D;
+        const T* rb = ob + row * D;
+        if (VEC) {
+            constexpr int n = Vec<T>::n;
+            uint4* va = reinterpret_cast<uint4*>(ra_);
+            const uint4* vb = reinterpret_cast<const uint4*>(rb);
+            for (int e = lane; e < D / n; e += 32) {
+                uint4 x = va[e];
+                const uint4 y = vb[e];
+                Vec<T>::fma2(x, y, ca, cb);
+                va[e] = x;
+            }
+        } else {
+            for (int e = lane; e < D; e += 32) from_f(ra_[e], ca * to_f(ra_[e]) + cb * to_f(rb[e]));
+        }
+        __syncwarp();
+        if (lane == 0) la[row] = lse;
+    }
+}
+
+template <typename V>
+__global__ void __launch_bounds__(kBlock) stripe_kernel(const V* __restrict__ src, V* __restrict__ dst,
+                                                        int64_t BH, int64_t S, int64_t N,
+                                                        int64_t row_vecs, int inverse) {
+    const int lane = threadIdx.x & 31;
+    const int64_t Sb = S / N;
+    const int64_t total = BH * S;
+    const int64_t warps = (int64_t)gridDim.x * (kBlock / 32);
+    for (int64_t wr = (int64_t)blockIdx.x * (kBlock / 32) + threadIdx.x / 32; wr < total;
+         wr += warps) {
+        const int64_t bh = wr / S, p = wr % S;  // p: destination row within the slice
+        int64_t sp;
+        if (!inverse) {  // dst row p = i*Sb + r holds token r*N + i
+            const int64_t i = p / Sb, r = p % Sb;
+            sp = r * N + i;
+        } else {  // dst row p = token t = r*N + i comes from row i*Sb + r
+            const int64_t i = p % N, r = p / N;
+            sp = i * Sb + r;
+        }
+        const V* s = src + (bh * S + sp) * row_vecs;
+        V* d = dst + (bh * S + p) * row_vecs;
+        for (int64_t e = lane; e < row_vecs; e += 32) d[e] = s[e];
+    }
+}
+
+static unsigned grid_for(int64_t rows) {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t need = (rows + (kBlock / 32) - 1) / (kBlock / 32);
+    const int64_t cap = (int64_t)sms * 16;
+    return (unsigned)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+}  // namespace aux
+
+int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
+                 int D, int dtype, cudaStream_t stream) {
+    if (rows == 0) return RA_OK;
+    const unsigned grid = aux::grid_for(rows);
+    if (dtype == RA_BF16) {
+        auto* a = static_cast<__nv_bfloat16*>(out_a);
+        auto* b = static_cast<const __nv_bfloat16*>(out_b);
+        if (D % 8 == 0)
+            aux::merge_kernel<__nv_bfloat16, true><<<grid, aux::kBlock, 0, stream>>>(a, lse_a, b, lse_b, rows, D);
+        else
+            aux::merge_kernel<__nv_bfloat16, false><<<grid, aux::kBlock, 0, stream>>>(a, lse_a, b, lse_b, rows, D);
+    } else {
+        auto* a = static_cast<float*>(out_a);
+        auto* b = static_cast<const float*>(out_b);
+        if (D % 4 == 0)
+            aux::merge_kernel<float, true><<<grid, aux::kBlock, 0, stream>>>(a, lse_a, b, lse_b, rows, D);
+        else
+            aux::merge_kernel<float, false><<<grid, aux::kBlock, 0, stream>>>(a, lse_a, b, lse_b, rows, D);
+    }
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
+                  int inverse, cudaStream_t stream) {
+    const int64_t rows = BH * S;
+    if (rows == 0) return RA_OK;
+    const unsigned grid = aux::grid_for(rows);
+    if (row_bytes % 16 == 0)
+        aux::stripe_kernel<uint4><<<grid, aux::kBlock, 0, stream>>>(
+            static_cast<const uint4*>(src), static_cast<uint4*>(dst), BH, S, N, row_bytes / 16, inverse);
+    else
+        aux::stripe_kernel<uint32_t><<<grid, aux::kBlock, 0, stream>>>(
+            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), BH, S, N, row_bytes / 4, inverse);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+}  // namespace ra

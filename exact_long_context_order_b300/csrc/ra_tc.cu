@@ -1,0 +1,555 @@
+// Tensor-core (tcgen05) ring-attention forward kernel for sm_103a, bf16 in,
+// fp32 accumulate.
+//
+// What it computes (the pages' method): each 128-row query tile of shard i
+// folds the key/value shards j = (i - s) mod N, s = 0..N-1, one 128-key tile
+// at a time, into a running row max m, running normaliser l and an
+// unnormalised numerator O held in tensor memory; O / l is written at the end
+// ("Ring Attention" glossary page, "Como funciona a atencao em anel";
+// aiunderstanding.org, "Approfondimento tecnico").  Whole shards and key tiles
+// with no visible pair are never visited (the schedule in schedule.cuh).
+//
+// How (B300 design):
+//  * Persistent grid, one CTA per SM (512 TMEM columns, ~193 KB smem).  A CTA
+//    works on items of two query tiles ("slots") that share each K/V tile.
+//  * warp 0, lane 0 -- TMA producer: Q tiles once per item, then K and V
+//    tiles into a ring of smem stages (128B-swizzled, 2 boxes of 64 columns).
+//  * warp 1, lane 0 -- MMA issuer: S_t = Q_t K^T (SS, M=128 N=128 K=16 steps)
+//    into TMEM, and O_t += P_t V (P read from TMEM, V MN-major from smem).
+//    Per key tile the order is PV_0(n-1), S_0(n), PV_1(n-1), S_1(n): while one
+//    softmax warpgroup works, the tensor core runs the other slot's MMAs.
+//  * warp 2 owns the TMEM allocation.
+//  * warps 4-7 / 8-11 -- softmax for slot 0 / 1, one thread per query row
+//    (row r = TMEM lane r): load the S row, mask the diagonal tile, update
+//    the running max, exp2, write P (bf16) over the S columns, and rescale
+//    O only when the max grew by more than 2^8 (the fold stays exact: the
+//    same stale max is used for numerator and normaliser).  They also run
+//    the epilogue O / l and lse = m + ln l.
+//  * Every mbarrier wait is bounded; on time-out the kernel records
+//    kStatusTimeout in the device status word, drains its in-flight copies
+//    and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "ra.h"
+#include "schedule.cuh"
+
+namespace ra {
+namespace tc {
+
+constexpr int kT = 128;             // query and key tile size
+constexpr int kThreads = 384;       // 12 warps
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // per wait
+constexpr uint64_t kDrainNs = 200000000ull;
+
+template <int D>
+struct Cfg {
+    static constexpr int kTileBytes = kT * D * 2;
+    static constexpr int kStages = (D == 128) ? 4 : 8;
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kQOff = 0;
+    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
+    // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
+    // o_full[2], o_empty[2], drain
+    static constexpr int kNumBars = 2 + 2 * kStages + 9;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+    static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+    static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+    static constexpr uint32_t kTmemCols = 512;
+    // barrier indices
+    static constexpr int bQFull = 0, bQEmpty = 1, bKVFull = 2, bKVEmpty = 2 + kStages,
+                         bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
+                         bOEmpty = bOFull + 2, bDrain = bOEmpty + 2;
+};
+
+struct Params {
+    ItemGeom G;
+    int64_t S;
+    int Sb;
+    float sl2;  // scale * log2(e)
+    __nv_bfloat16* out;
+    float* lse;
+    unsigned int* status;
+    int32_t* log;
+    int32_t* counts;
+    int max_entries;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag,
+                                         unsigned int* status) {
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t it = 0;
+    for (;;) {
+        if (mbar_try_wait(b, parity)) return true;
+        if ((++it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kTimeoutNs) {
+                *abort_flag = 1;
+                atomicOr(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+// Short bounded wait used only while draining after an abort.
+__device__ __forceinline__ void drain_wait(uint32_t b, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(b, parity)) {
+        if (globaltimer_ns() - t0 > kDrainNs) return;
+    }
+}
+
+template <int D, bool LOG>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBarOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    auto bar = [&](int idx) -> uint32_t { return base + C::kBarOff + idx * 8; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const ItemGeom& G = p.G;
+
+    if (tid == 0) {
+        mbar_init(bar(C::bQFull), 1);
+        mbar_init(bar(C::bQEmpty), 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(bar(C::bKVFull + s), 1);
+            mbar_init(bar(C::bKVEmpty + s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(C::bSFull + t), 1);
+            mbar_init(bar(C::bPFull + t), 4);
+            mbar_init(bar(C::bOFull + t), 1);
+            mbar_init(bar(C::bOEmpty + t), 4);
+        }
+        mbar_init(bar(C::bDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_q = policy_evict_first();
+            const uint64_t pol_kv = policy_evict_last();
+            uint32_t kv_pos = 0;
+            int k = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; item < G.n_items; item += gridDim.x, ++k) {
+                const Item it = decode_item(G, item);
+                if (k > 0 && !(ok = wait_bar(bar(C::bQEmpty), (k - 1) & 1, abort_flag, p.status)))
+                    break;
+                mbar_arrive_expect_tx(bar(C::bQFull), 2 * C::kTileBytes);
+                for (int t = 0; t < 2; ++t) {
+                    const int row = (int)((int64_t)(it.b * G.Hq + it.h[t]) * p.S +
+                                          (int64_t)it.i * p.Sb + (int64_t)it.qt[t] * kT);
+                    for (int bx = 0; bx < C::kBoxes; ++bx)
+                        tma_load_2d(base + C::kQOff + t * C::kTileBytes + bx * (kT * 128), &tm_q,
+                                    bx * 64, row, bar(C::bQFull), pol_q);
+                }
+                const int64_t kvrow0 = (int64_t)(it.b * G.Hkv + it.kvh) * p.S;
+                TileWalk w;
+                for (w.start(G.rg, it); !w.done(G.rg) && ok; w.next(G.rg, it)) {
+                    const int row = (int)(kvrow0 + (int64_t)w.j * p.Sb + (int64_t)w.kt * kT);
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint32_t st = kv_pos % C::kStages, use = kv_pos / C::kStages;
+                        if (use > 0 && !(ok = wait_bar(bar(C::bKVEmpty + st), (use - 1) & 1,
+                                                       abort_flag, p.status)))
+                            break;
+                        mbar_arrive_expect_tx(bar(C::bKVFull + st), C::kTileBytes);
+                        const CUtensorMap* tm = kv ? &tm_v : &tm_k;
+                        for (int bx = 0; bx < C::kBoxes; ++bx)
+                            tma_load_2d(base + C::kKVOff + st * C::kTileBytes + bx * (kT * 128), tm,
+                                        bx * 64, row, bar(C::bKVFull + st), pol_kv);
+                        ++kv_pos;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (!ok) {
+                // let every copy that may still be in flight land before exit
+                if (k > 0 || G.n_items > blockIdx.x) drain_wait(bar(C::bQFull), k & 1);
+                const uint32_t first = kv_pos > (uint32_t)C::kStages ? kv_pos - C::kStages : 0;
+                for (uint32_t pos = first; pos < kv_pos; ++pos)
+                    drain_wait(bar(C::bKVFull + pos % C::kStages), (pos / C::kStages) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
+            constexpr uint32_t idesc_o = make_idesc_bf16(128, D, false, true);
+            auto issue_s = [&](int t, uint32_t stK) {
+                const uint32_t qa = base + C::kQOff + t * C::kTileBytes;
+                const uint32_t ka = base + C::kKVOff + stK * C::kTileBytes;
+                const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * (kT * 128) + (kk % 4) * 32;
+                    umma_ss(d, make_sdesc(qa + off, 16, 1024, kLayoutSW128),
+                            make_sdesc(ka + off, 16, 1024, kLayoutSW128), idesc_s, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int t, uint32_t stV, bool acc) {
+                const uint32_t va = base + C::kKVOff + stV * C::kTileBytes;
+                const uint32_t pa = tmem + (t ? C::kColS1 : C::kColS0);
+                const uint32_t o = tmem + (t ? C::kColO1 : C::kColO0);
+#pragma unroll
+                for (int kk = 0; kk < kT / 16; ++kk)
+                    umma_ts(o, pa + kk * 8, make_sdesc(va + kk * 2048, kT * 128, 1024, kLayoutSW128),
+                            idesc_o, (kk > 0 || acc) ? 1u : 0u);
+            };
+            uint32_t kv_pos = 0, gt = 0;
+            int k = 0;
+            bool ok = true;
+            for (long long item = blockIdx.x; item < G.n_items && ok; item += gridDim.x, ++k) {
+                const Item it = decode_item(G, item);
+                if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status))) break;
+                tc_fence_after();
+                TileWalk w;
+                uint32_t n = 0;
+                for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n) {
+                    const uint32_t stK = kv_pos % C::kStages;
+                    if (!(ok = wait_bar(bar(C::bKVFull + stK), (kv_pos / C::kStages) & 1,
+                                        abort_flag, p.status)))
+                        break;
+                    uint32_t stV = 0;
+                    if (n > 0) {
+                        const uint32_t vp = kv_pos - 1;
+                        stV = vp % C::kStages;
+                        if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1,
+                                            abort_flag, p.status)))
+                            break;
+                    }
+                    tc_fence_after();
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (n > 0) {
+                            if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag,
+                                                p.status)))
+                                break;
+                            if (n == 1 && k > 0 &&
+                                !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag,
+                                                p.status)))
+                                break;
+                            tc_fence_after();
+                            issue_pv(t, stV, n > 1);
+                            if (t == 1) umma_commit(bar(C::bKVEmpty + stV));
+                        }
+                        issue_s(t, stK);
+                        umma_commit(bar(C::bSFull + t));
+                        if (t == 1) umma_commit(bar(C::bKVEmpty + stK));
+                    }
+                    if (!ok) break;
+                    kv_pos += 2;
+                    ++gt;
+                }
+                if (!ok) break;
+                umma_commit(bar(C::bQEmpty));  // every S MMA of this item has been issued
+                const uint32_t vp = kv_pos - 1, stV = vp % C::kStages;
+                if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1, abort_flag,
+                                    p.status)))
+                    break;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag, p.status)))
+                        break;
+                    if (n == 1 && k > 0 &&
+                        !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag, p.status)))
+                        break;
+                    tc_fence_after();
+                    issue_pv(t, stV, n > 1);
+                    umma_commit(bar(C::bOFull + t));
+                    if (t == 1) umma_commit(bar(C::bKVEmpty + stV));
+                }
+            }
+            if (!ok) {
+                umma_commit(bar(C::bDrain));
+                drain_wait(bar(C::bDrain), 0);
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax
+        const int t = (warp - 4) >> 2;
+        const int r = tid - 128 * (1 + t);  // query row of the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_tm = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
+        const uint32_t o_tm = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
+        const float sl2 = p.sl2;
+        uint32_t gt = 0;
+        int k = 0;
+        bool ok = true;
+        for (long long item = blockIdx.x; item < G.n_items && ok; item += gridDim.x, ++k) {
+            const Item it = decode_item(G, item);
+            const int qt = it.qt[t];
+            const bool valid = (t == 0) || it.valid1;
+            float m_used = -INFINITY, l = 0.f;
+            int n_logged = 0;
+            TileWalk w;
+            uint32_t n = 0;
+            for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n, ++gt) {
+                const int kind = fold_kind(G.rg, it.i, w.j, qt, w.kt);
+                ok = wait_bar(bar(C::bSFull + t), gt & 1, abort_flag, p.status);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t pk[2][32];
+                if (kind == kNone) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) pk[c][e] = 0u;
+                } else {
+                    uint32_t sr[4][32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(s_tm + c * 32, sr[c]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
+                    if (kind != kFull) {
+                        const int lim = (kind == kIncl) ? r : r - 1;  // visible iff col <= lim
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
+                    }
+                    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        mx0 = fmaxf(mx0, fmaxf(__uint_as_float(sr[0][e]), __uint_as_float(sr[1][e])));
+                        mx1 = fmaxf(mx1, fmaxf(__uint_as_float(sr[2][e]), __uint_as_float(sr[3][e])));
+                        mx2 = fmaxf(mx2, fmaxf(__uint_as_float(sr[0][e + 1]), __uint_as_float(sr[1][e + 1])));
+                        mx3 = fmaxf(mx3, fmaxf(__uint_as_float(sr[2][e + 1]), __uint_as_float(sr[3][e + 1])));
+                        mx0 = fmaxf(mx0, fmaxf(__uint_as_float(sr[0][e + 2]), __uint_as_float(sr[1][e + 2])));
+                        mx1 = fmaxf(mx1, fmaxf(__uint_as_float(sr[2][e + 2]), __uint_as_float(sr[3][e + 2])));
+                        mx2 = fmaxf(mx2, fmaxf(__uint_as_float(sr[0][e + 3]), __uint_as_float(sr[1][e + 3])));
+                        mx3 = fmaxf(mx3, fmaxf(__uint_as_float(sr[2][e + 3]), __uint_as_float(sr[3][e + 3])));
+                    }
+                    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                    const float m_new = fmaxf(m_used, mx);
+                    // rescale only when the max grew by more than 2^8 (in exp2 units)
+                    const bool need = (m_new - m_used) * sl2 > 8.0f;
+                    if (__any_sync(0xffffffffu, need)) {
+                        float alpha = 1.f;
+                        if (need) {
+                            alpha = ex2_approx((m_used - m_new) * sl2);
+                            m_used = m_new;
+                        }
+                        l *= alpha;
+                        if (n > 0) {
+#pragma unroll
+                            for (int c = 0; c < D / 32; ++c) {
+                                uint32_t o[32];
+                                tmem_ld32(o_tm + c * 32, o);
+                                tmem_wait_ld();
+                                reg_fence(o);
+#pragma unroll
+                                for (int e = 0; e < 32; ++e)
+                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                                tmem_st32(o_tm + c * 32, o);
+                            }
+                        }
+                    }
+                    const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
+                    float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, -mb));
+                            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -mb));
+                            const float p2 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 2]), sl2, -mb));
+                            const float p3 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 3]), sl2, -mb));
+                            sum0 += p0;
+                            sum1 += p1;
+                            sum2 += p2;
+                            sum3 += p3;
+                            pk[c >> 1][(c & 1) * 16 + e / 2] = pack_bf16x2(p0, p1);
+                            pk[c >> 1][(c & 1) * 16 + e / 2 + 1] = pack_bf16x2(p2, p3);
+                        }
+                    }
+                    l += (sum0 + sum1) + (sum2 + sum3);
+                }
+                tmem_st32(s_tm + 0, pk[0]);
+                tmem_st32(s_tm + 32, pk[1]);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::bPFull + t));
+                if (LOG && valid && kind != kNone && r == 0) {
+                    const int64_t unit =
+                        ((int64_t)(it.b * G.Hq + it.h[t]) * G.rg.N + it.i) * G.rg.nt + qt;
+                    if (n_logged < p.max_entries) {
+                        int32_t* e = p.log + (unit * p.max_entries + n_logged) * 4;
+                        e[0] = w.s;
+                        e[1] = w.j;
+                        e[2] = w.kt;
+                        e[3] = kind;
+                    } else {
+                        atomicOr(p.status, kStatusBounds);
+                    }
+                    ++n_logged;
+                }
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue
+            ok = wait_bar(bar(C::bOFull + t), k & 1, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            if (valid) {
+                const int64_t row = (int64_t)(it.b * G.Hq + it.h[t]) * p.S + (int64_t)it.i * p.Sb +
+                                    (int64_t)qt * kT + r;
+                const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+                uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(o_tm + c * 32, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v4;
+                        v4.x = pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+                        v4.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+                        v4.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
+                        v4.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
+                        orow[c * 4 + e / 8] = v4;
+                    }
+                }
+                if (p.lse)
+                    p.lse[row] = (l > 0.f) ? (m_used * sl2 + lg2_approx(l)) * 0.69314718055994531f
+                                           : -INFINITY;
+                if (LOG && r == 0) {
+                    const int64_t unit =
+                        ((int64_t)(it.b * G.Hq + it.h[t]) * G.rg.N + it.i) * G.rg.nt + qt;
+                    p.counts[unit] = n_logged;
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::bOEmpty + t));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// rows x D bf16 row-major, box of 128 rows x 64 columns, 128-byte swizzle
+static bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int D) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kT};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool LOG>
+static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* status,
+                       int sm_count, cudaStream_t stream) {
+    using C = Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
+    if (!encode_rows(&mq, pr.q, q_rows, D) || !encode_rows(&mk, pr.k, kv_rows, D) ||
+        !encode_rows(&mv, pr.v, kv_rows, D))
+        return RA_ERR_CUDA;
+    Params P;
+    const int Sb = (int)(pr.S / pr.N);
+    P.G = make_item_geom(pr.B, pr.Hq, pr.Hkv, pr.N, Sb / kT, pr.causal, pr.striped);
+    P.S = pr.S;
+    P.Sb = Sb;
+    P.sl2 = (float)((double)pr.scale * 1.4426950408889634);
+    P.out = static_cast<__nv_bfloat16*>(pr.out);
+    P.lse = pr.lse;
+    P.status = status;
+    P.log = flog ? flog->log : nullptr;
+    P.counts = flog ? flog->counts : nullptr;
+    P.max_entries = flog ? flog->max_entries : 0;
+    if (P.G.n_items <= 0) return RA_OK;
+    auto kern = fwd_kernel<D, LOG>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return RA_ERR_CUDA;
+    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
+    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, P);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+}  // namespace tc
+
+bool tc_supported(const FwdProblem& p) {
+    if (p.dtype != RA_BF16 || (p.D != 64 && p.D != 128)) return false;
+    if (p.S % p.N) return false;
+    const int64_t Sb = p.S / p.N;
+    if (Sb % tc::kT) return false;
+    if ((int64_t)p.B * p.Hq * p.S >= (1ll << 31) || (int64_t)p.B * p.Hkv * p.S >= (1ll << 31))
+        return false;
+    return true;
+}
+
+int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, int sm_count,
+              cudaStream_t stream) {
+    if (!tc_supported(p)) return RA_ERR_UNSUPPORTED;
+    if (p.D == 128)
+        return flog ? tc::launch_impl<128, true>(p, flog, status, sm_count, stream)
+                    : tc::launch_impl<128, false>(p, flog, status, sm_count, stream);
+    return flog ? tc::launch_impl<64, true>(p, flog, status, sm_count, stream)
+                : tc::launch_impl<64, false>(p, flog, status, sm_count, stream);
+}
+
+}  // namespace ra

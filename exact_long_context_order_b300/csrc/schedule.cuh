@@ -1,0 +1,166 @@
+// Ring fold schedule and persistent work decomposition, shared by the host
+// planner (ra_plan) and the kernels.
+//
+// Ring schedule ("Ring Attention" glossary page, "Como funciona a atencao em
+// anel"): query shard i folds key/value shard j = (i - s) mod N at step s.
+// Within a shard pair the key tiles are folded in ascending order.  With
+// 128-token tiles and equal query/key tile sizes the causal mask reduces to a
+// closed form per (i, j, qt, kt):
+//   non-causal            every key tile of every shard, FULL
+//   causal, contiguous    j < i: every key tile FULL; j == i: kt < qt FULL,
+//                         kt == qt INCL (local key row <= local query row);
+//                         j > i: nothing
+//   causal, striped       (token t on shard t mod N, local row t div N): for
+//                         every j, kt < qt FULL and kt == qt INCL if j <= i,
+//                         STRICT (local key row < local query row) if j > i
+// since token r*N + i sees token c*N + j iff c < r, or c == r and j <= i.
+#pragma once
+#include <cstdint>
+
+#ifndef RA_HD
+#define RA_HD __host__ __device__ __forceinline__
+#endif
+
+namespace ra {
+
+enum FoldKind : int { kFull = 0, kIncl = 1, kStrict = 2, kNone = 3 };
+
+struct RingGeom {
+    int N;        // virtual devices (shards)
+    int nt;       // tiles per shard (Sb / tile)
+    int causal;
+    int striped;
+};
+
+// Live key tiles of shard j for query tile qt of shard i: kt in [0, *nk); the
+// tile kt == qt (when *diag_kind != kNone) is the masked diagonal tile.
+RA_HD void shard_span(const RingGeom& g, int i, int j, int qt, int* nk, int* diag_kind) {
+    if (!g.causal) {
+        *nk = g.nt;
+        *diag_kind = kNone;
+    } else if (!g.striped) {
+        if (j < i) { *nk = g.nt; *diag_kind = kNone; }
+        else if (j == i) { *nk = qt + 1; *diag_kind = kIncl; }
+        else { *nk = 0; *diag_kind = kNone; }
+    } else {
+        *nk = qt + 1;
+        *diag_kind = (j <= i) ? kIncl : kStrict;
+    }
+}
+
+RA_HD int fold_kind(const RingGeom& g, int i, int j, int qt, int kt) {
+    int nk, dk;
+    shard_span(g, i, j, qt, &nk, &dk);
+    if (kt >= nk) return kNone;
+    return (kt == qt && dk != kNone) ? dk : kFull;
+}
+
+// Persistent work items of the tensor-core kernel.  An item is two 128-row
+// query tiles ("slots") that share every key/value tile they stream:
+//  * pair_heads = 1 (Hq/Hkv even): query heads 2m and 2m+1 of one GQA group at
+//    the same query tile -- identical fold lists;
+//  * pair_heads = 0: query tiles 2p and 2p+1 of one head -- slot 0 treats the
+//    extra diagonal tile of slot 1 as fully masked (kNone).
+// Items are numbered group-major ((b, kv head) outer), then by "level" in
+// decreasing cost (longest work first), then within a level.
+struct ItemGeom {
+    RingGeom rg;
+    int B, Hq, Hkv, g;
+    int pair_heads;
+    int L, W;  // levels per group, items per level
+    long long n_items;
+};
+
+RA_HD ItemGeom make_item_geom(int B, int Hq, int Hkv, int N, int nt, int causal, int striped) {
+    ItemGeom G;
+    G.rg.N = N; G.rg.nt = nt; G.rg.causal = causal; G.rg.striped = striped;
+    G.B = B; G.Hq = Hq; G.Hkv = Hkv; G.g = Hq / Hkv;
+    G.pair_heads = (G.g % 2 == 0) ? 1 : 0;
+    const bool contig_causal = causal && !striped;
+    if (G.pair_heads) {
+        int hp = G.g / 2;
+        G.L = contig_causal ? N * nt : nt;
+        G.W = contig_causal ? hp : N * hp;
+    } else {
+        int nt2 = (nt + 1) / 2;
+        G.L = contig_causal ? N * nt2 : nt2;
+        G.W = contig_causal ? G.g : N * G.g;
+    }
+    G.n_items = (long long)B * Hkv * G.L * G.W;
+    return G;
+}
+
+struct Item {
+    int b, kvh, i;
+    int h[2], qt[2];
+    int valid1;  // slot 1 holds a real query tile
+};
+
+RA_HD Item decode_item(const ItemGeom& G, long long item) {
+    Item it;
+    long long per_group = (long long)G.L * G.W;
+    long long grp = item / per_group, rem = item % per_group;
+    int lam = (int)(rem / G.W), w = (int)(rem % G.W);
+    it.b = (int)(grp / G.Hkv);
+    it.kvh = (int)(grp % G.Hkv);
+    const int N = G.rg.N, nt = G.rg.nt;
+    const bool contig_causal = G.rg.causal && !G.rg.striped;
+    if (G.pair_heads) {
+        int hp_count = G.g / 2, hp, qt;
+        if (contig_causal) {
+            int gt = N * nt - 1 - lam;
+            it.i = gt / nt; qt = gt % nt; hp = w;
+        } else {
+            qt = nt - 1 - lam; it.i = w / hp_count; hp = w % hp_count;
+        }
+        it.h[0] = it.kvh * G.g + 2 * hp;
+        it.h[1] = it.h[0] + 1;
+        it.qt[0] = it.qt[1] = qt;
+        it.valid1 = 1;
+    } else {
+        int nt2 = (nt + 1) / 2, p, hh;
+        if (contig_causal) {
+            int gp = N * nt2 - 1 - lam;
+            it.i = gp / nt2; p = gp % nt2; hh = w;
+        } else {
+            p = nt2 - 1 - lam; it.i = w / G.g; hh = w % G.g;
+        }
+        it.h[0] = it.h[1] = it.kvh * G.g + hh;
+        it.qt[0] = 2 * p;
+        it.qt[1] = 2 * p + 1;
+        it.valid1 = (2 * p + 1 < nt) ? 1 : 0;
+        if (!it.valid1) it.qt[1] = it.qt[0];  // slot 1 recomputes slot 0's tile, never stored
+    }
+    return it;
+}
+
+// Walks the union fold list of an item: ring steps s ascending, key tiles of
+// shard j = (i - s) mod N ascending, over the key tiles either slot needs.
+struct TileWalk {
+    int s, j, kt, nk;
+    RA_HD void start(const RingGeom& g, const Item& it) {
+        s = -1; kt = 0; nk = 0; j = it.i;
+        advance_shard(g, it);
+    }
+    RA_HD void advance_shard(const RingGeom& g, const Item& it) {
+        // move to the next ring step with at least one live key tile
+        for (;;) {
+            ++s;
+            if (s >= g.N) return;
+            j = it.i - s;
+            if (j < 0) j += g.N;
+            int nk0, nk1, d;
+            shard_span(g, it.i, j, it.qt[0], &nk0, &d);
+            shard_span(g, it.i, j, it.qt[1], &nk1, &d);
+            nk = nk0 > nk1 ? nk0 : nk1;
+            kt = 0;
+            if (nk > 0) return;
+        }
+    }
+    RA_HD bool done(const RingGeom& g) const { return s >= g.N; }
+    RA_HD void next(const RingGeom& g, const Item& it) {
+        if (++kt >= nk) advance_shard(g, it);
+    }
+};
+
+}  // namespace ra

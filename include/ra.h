@@ -1,0 +1,191 @@
+/*
+ * ra.h -- C ABI of the ring-attention library (libra.so), sm_103a.
+ *
+ * The library computes exact blockwise ring attention on one GPU.  The
+ * sequence of S tokens is held by N virtual ring devices (shards) that live
+ * side by side in device memory; query shard i visits the key/value shards
+ * in ring order j = (i - s) mod N, s = 0..N-1, and folds every block into an
+ * online-softmax state (running max, running normaliser, rescaled
+ * numerator), so the result equals full softmax attention.
+ *   Method: "Ring Attention" glossary page (ultralytics.com), section "Como
+ *   funciona a atencao em anel" (ring schedule j = (i - step) mod N,
+ *   accumulated exponentiated scores and weighted values, divided at the
+ *   end; running-max subtraction in production kernels; causal masking and
+ *   Striped Attention); "Sequence parallelism and ring attention"
+ *   (aiunderstanding.org), sections "Immersione profonda" (contiguous token
+ *   blocks, K/V passed around the ring) and "Approfondimento tecnico"
+ *   (online softmax, exact result); "Ring Attention la gi?" (thienlv.com),
+ *   section "Uu Diem" (GQA compatibility).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor arguments are DEVICE pointers to memory the caller owns; the
+ *   library never frees or keeps them.  The library allocates no device
+ *   memory for its kernels except one status word per device (a static
+ *   __device__ variable created with the module).
+ * - Layout is "shard-major": q and out are [B, Hq, S, D], k and v are
+ *   [B, Hkv, S, D], lse is [B, Hq, S]; all row-major and contiguous.  Shard i
+ *   owns rows [i*Sb, (i+1)*Sb) of every (b, h) slice, Sb = S / N.  With
+ *   striped = 0 row p holds token p (contiguous sharding).  With striped = 1
+ *   row r of shard i holds token r*N + i (token t lives on shard t mod N).
+ *   ra_stripe converts between token order and the striped shard-major order.
+ * - Query head h reads key/value head h / (Hq / Hkv) (grouped-query
+ *   attention; Hq must be a multiple of Hkv).
+ * - causal = 1 masks every key whose token position is after the query's
+ *   (inclusive causal: a query sees its own key).
+ * - scale <= 0 selects 1/sqrt(D).
+ * - dtype: RA_BF16 (inputs/outputs bfloat16, fp32 accumulation) or RA_F32
+ *   (inputs/outputs float32, fp32 arithmetic, no TF32).
+ * - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every call that takes a stream is asynchronous on it: it validates its
+ *   arguments on the host, enqueues kernels and returns.  Device-side
+ *   failures (a bounded wait that ran out, a bounds check) are recorded in the
+ *   device status word and reported by ra_check.
+ * - Return value: RA_OK or one of the error codes below.  On an error
+ *   detected on the host nothing is enqueued and no output is touched.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, S % N, Hq % Hkv, ... */
+    RA_ERR_UNSUPPORTED = 2, /* shape/dtype/device the kernels do not handle */
+    RA_ERR_ALIGN = 3,       /* pointer not 16-byte aligned */
+    RA_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, ...) */
+    RA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (reported by ra_check) */
+    RA_ERR_BOUNDS = 6,      /* a kernel's bounds check failed (reported by ra_check) */
+    RA_ERR_CAPACITY = 7     /* a caller-provided output array is too small */
+};
+
+enum { RA_BF16 = 0, RA_F32 = 1 };
+
+/* Kernel selection for ra_forward_ex. */
+enum {
+    RA_KERNEL_AUTO = 0, /* tensor-core kernel when the shape allows it, else SIMT */
+    RA_KERNEL_TC = 1,   /* tcgen05 tensor-core kernel (bf16, D in {64,128}, Sb % 128 == 0) */
+    RA_KERNEL_SIMT = 2  /* fp32 SIMT kernel (any D <= 256, any Sb); f32 or bf16 */
+};
+
+/* Fold kinds reported by ra_plan / ra_fold_log. */
+enum { RA_FOLD_FULL = 0, RA_FOLD_INCL = 1, RA_FOLD_STRICT = 2 };
+
+/*
+ * ra_forward: out = softmax(scale * Q K^T [masked]) V over the ring.
+ *   q   [B, Hq, S, D]  (read)      k, v [B, Hkv, S, D]  (read)
+ *   out [B, Hq, S, D]  (written)   lse  [B, Hq, S] float32, natural log of the
+ *                                  softmax normaliser per query row
+ *                                  (written; may be NULL)
+ *   B, Hq, Hkv, S, D, N > 0; S % N == 0; Hq % Hkv == 0.
+ * Computes, for each query shard i, the fold over ring steps s = 0..N-1 of
+ * key/value shard j = (i - s) mod N (glossary page, "Como funciona": the
+ * schedule and the numerator/denominator fold; aiunderstanding.org,
+ * "Approfondimento tecnico": running max and normaliser with rescaling).
+ * Under causal masking whole shards and key tiles with no visible pair are
+ * skipped, never computed.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_ALIGN (q, k, v, out, lse not 16-byte
+ * aligned), RA_ERR_UNSUPPORTED (D > 256, device not sm_103), RA_ERR_CUDA.
+ */
+int ra_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+               int Hkv, int64_t S, int D, int N, int causal, int striped, float scale, int dtype,
+               void* stream);
+
+/* ra_forward with an explicit kernel choice (RA_KERNEL_*).  RA_KERNEL_TC
+ * returns RA_ERR_UNSUPPORTED when the shape is outside its envelope. */
+int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                  int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
+                  int dtype, int kernel, void* stream);
+
+/*
+ * ra_merge: fold partial result b into partial result a, in place.
+ *   out_a [rows, D] (read, written)   lse_a [rows] float32 (read, written)
+ *   out_b [rows, D] (read)            lse_b [rows] float32 (read)
+ * Each partial is a normalised attention output over a disjoint key set
+ * with its log-sum-exp; the result is the attention over the union:
+ *   lse = ln(e^lse_a + e^lse_b),  out_a = e^(lse_a-lse) out_a + e^(lse_b-lse) out_b
+ * (the same rescale-and-add the online softmax performs when a block arrives;
+ * aiunderstanding.org, "Approfondimento tecnico").  A partial with
+ * lse = -inf contributes nothing; two empty partials give out 0, lse -inf.
+ * dtype RA_BF16 or RA_F32 for out_a/out_b.  rows >= 0, 0 < D <= 1024.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_ALIGN, RA_ERR_CUDA.
+ */
+int ra_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
+             int D, int dtype, void* stream);
+
+/*
+ * ra_stripe: permute rows between token order and striped shard-major order.
+ *   src, dst: [BH, S, row_bytes] byte arrays (device; must not overlap).
+ *   inverse = 0: dst[i*Sb + r] = src[r*N + i]   (token order -> striped shards)
+ *   inverse = 1: dst[r*N + i] = src[i*Sb + r]   (striped shards -> token order)
+ * for every (bh) slice; Sb = S / N (glossary page, Striped Attention: tokens
+ * spread evenly over the devices, read as token t -> shard t mod N).
+ * row_bytes > 0 and a multiple of 4.  Bit-exact copy.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_ALIGN (pointers not 16-byte aligned),
+ * RA_ERR_CUDA.
+ */
+int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
+              int inverse, void* stream);
+
+/*
+ * ra_plan (host only, no GPU): the fold list of one query tile.
+ * For query shard i and query tile qt (rows [qt*tile, (qt+1)*tile) of the
+ * shard), writes n_items entries of 4 int32 each, (s, j, kt, kind), in fold
+ * order: ring steps s ascending (j = (i - s) mod N), key tiles kt of shard j
+ * ascending, only tiles that hold at least one visible (query, key) pair;
+ * kind is RA_FOLD_FULL (every pair visible), RA_FOLD_INCL (pairs with local
+ * key row <= local query row) or RA_FOLD_STRICT (local key row < local query
+ * row).  This is the exact order the tensor-core kernel folds the tile in.
+ *   items: int32[cap][4] or NULL (then only *n_items is set).
+ *   Requires tile >= 2 and Sb % tile == 0.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_CAPACITY (cap too small; *n_items is
+ * still set).
+ */
+int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, int32_t* items,
+            int64_t cap, int64_t* n_items);
+
+/*
+ * ra_fold_log: run the tensor-core kernel in its logging variant and record
+ * the order in which each query tile was folded.
+ *   Same tensor arguments as ra_forward (bf16 only).
+ *   log: device int32 buffer of B*Hq*S/128 * max_entries * 4 entries.  For the
+ *        query tile (b, h, i, qt), at index ((b*Hq + h)*N + i)*(Sb/128) + qt,
+ *        entry n is (s, j, kt, kind) of its n-th live fold; unused entries are
+ *        left as written by the caller.
+ *   counts: device int32[B*Hq*S/128]: number of live folds recorded per tile.
+ *   max_entries >= N * Sb / 128.
+ * The logging variant computes the same outputs as ra_forward.
+ * Errors: as ra_forward, plus RA_ERR_UNSUPPORTED outside the tensor-core
+ * kernel's envelope.
+ */
+int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
+                int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
+                int32_t* log, int32_t* counts, int max_entries, void* stream);
+
+/*
+ * ra_check: synchronise `stream`, then read and clear this device's status
+ * word.  Returns RA_OK, RA_ERR_TIMEOUT, RA_ERR_BOUNDS or RA_ERR_CUDA (the
+ * synchronisation itself failed; the CUDA error string is kept for
+ * ra_strerror(RA_ERR_CUDA)).
+ */
+int ra_check(void* stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* ra_strerror(int code);
+
+/* Query/key tile sizes of the tensor-core kernel (both 128). */
+int ra_tile_config(int* tq, int* tk);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int ra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

@@ -1,0 +1,104 @@
+"""C-ABI library checks that need no GPU: it loads, exports every function
+that include/ra.h declares, rejects bad arguments on the host before touching
+a device, and its fold planner equals the oracle's brute-force schedule."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_long_context_order_b300 as ra
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(ra_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_long_context_order_b300 import build
+    build.build()
+    return ra.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"ra_forward", "ra_merge", "ra_plan", "ra_check", "ra_strerror"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in ra._SIGNATURES, n
+
+
+def test_strerror_and_config(lib):
+    assert ra.ra_strerror(ra.RA_OK) == "ok"
+    for c in range(1, 8):
+        assert ra.ra_strerror(c) and ra.ra_strerror(c) != "unknown status"
+    assert ra.ra_strerror(99) == "unknown status"
+    assert ra.ra_tile_config() == (128, 128)
+    assert ra.ra_version() >= 100
+
+
+def test_host_validation_rejects_before_any_device_work(lib):
+    p = ctypes.c_void_p(16 * 1024)  # never dereferenced: validation fails first
+    args = dict(B=1, Hq=2, Hkv=1, S=256, D=128, N=2)
+
+    def call(q=p, k=p, v=p, out=p, **kw):
+        a = dict(args, **kw)
+        return ra.ra_forward(q, k, v, out, None, a["B"], a["Hq"], a["Hkv"], a["S"], a["D"],
+                             a["N"], 1, 0, 0.0, ra.RA_BF16, None)
+
+    assert call(q=None) == ra.RA_ERR_INVALID_ARG
+    assert call(S=255) == ra.RA_ERR_INVALID_ARG          # S % N
+    assert call(Hq=3, Hkv=2) == ra.RA_ERR_INVALID_ARG    # Hq % Hkv
+    assert call(B=0) == ra.RA_ERR_INVALID_ARG
+    assert call(D=512) == ra.RA_ERR_UNSUPPORTED
+    assert call(q=ctypes.c_void_p(16 * 1024 + 2)) == ra.RA_ERR_ALIGN
+    assert ra.ra_forward_ex(p, p, p, p, None, 1, 1, 1, 256, 128, 2, 0, 0, 0.0, ra.RA_BF16, 7,
+                            None) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_forward(p, p, p, p, None, 1, 1, 1, 256, 128, 2, 0, 0, 0.0, 5, None) == \
+        ra.RA_ERR_INVALID_ARG
+    assert ra.ra_merge(p, p, p, p, 10, 0, ra.RA_BF16, None) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_merge(p, p, p, p, -1, 8, ra.RA_BF16, None) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_merge(None, None, None, None, 0, 8, ra.RA_BF16, None) == ra.RA_OK  # empty
+    assert ra.ra_stripe(p, p, 1, 10, 3, 16, 0, None) == ra.RA_ERR_INVALID_ARG  # S % N
+    assert ra.ra_stripe(p, p, 1, 8, 2, 6, 0, None) == ra.RA_ERR_INVALID_ARG   # row_bytes % 4
+    assert ra.ra_stripe(p, ctypes.c_void_p(16 * 1024 + 64), 1, 8, 2, 16, 0, None) == \
+        ra.RA_ERR_INVALID_ARG  # overlapping buffers
+
+
+def test_plan_errors(lib):
+    n = ctypes.c_int64()
+    assert ra.ra_plan(256, 2, 1, 0, 128, 0, 0, None, 0, None) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(256, 2, 1, 0, 100, 0, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(256, 2, 1, 0, 128, 2, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(256, 2, 1, 0, 128, 0, 1, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(256, 2, 1, 0, 128, 1, 0, None, 0, ctypes.byref(n)) == ra.RA_OK
+    assert n.value == 2  # shard 1 of 2, contiguous causal: shard 0 full, own diagonal
+    buf = (ctypes.c_int32 * 4)()
+    assert ra.ra_plan(256, 2, 1, 0, 128, 1, 0, buf, 1, ctypes.byref(n)) == ra.RA_ERR_CAPACITY
+    assert n.value == 2
+
+
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("S,N,T", [(512, 4, 32), (768, 3, 64), (384, 1, 128), (1024, 8, 16),
+                                   (96, 6, 2)])
+def test_plan_equals_bruteforce_schedule(lib, causal, striped, S, N, T):
+    """Bit-exact: the library's closed-form fold list == oracle brute force."""
+    ref = oracle.fold_schedule(S, N, causal, striped, T, T)
+    by_tile = {}
+    for (i, qt, s, j, kt, kind) in ref:
+        by_tile.setdefault((i, qt), []).append((s, j, kt, kind))
+    nt = S // N // T
+    for i in range(N):
+        for qt in range(nt):
+            assert ra.plan(S, N, causal, striped, i, qt, tile=T) == by_tile.get((i, qt), []), \
+                (i, qt)
