@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark: exact ring attention (bf16, causal, striped, GQA) on B300.
+
+One step = one ra_forward over the whole workload (every query shard folds
+every key/value shard in ring order).  Default workload: B=1, 32 query heads
+sharing 8 KV heads, S = 131072 tokens in N = 16 striped shards of 8192, D = 128,
+causal.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
+device synchronise, each step bracketed by CUDA events on the launching
+stream; the inputs (1.5 GiB) are larger than L2, so no flush is needed.
+Multi-GPU: every rank runs its own replica of the workload (the path needs no
+exchange on one GPU per ring); value = FLOPs of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s & tokens/s (bf16, causal-adj) at S=128K; % of BF16 tensor peak"
+KERNEL_NAME = "ra::tc::fwd_kernel<128, false>"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="gqa_128k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("exact_long_context_order_b300/csrc/ra_tc.cu",
+                "exact_long_context_order_b300/csrc/ptx.cuh",
+                "exact_long_context_order_b300/csrc/schedule.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"tc_fwd_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(kernel source ([0-9a-f]+)\)", text)
+    if not m or m.group(2) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.dev = device_index
+
+    def start(self):
+        import tempfile
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(self.dev)
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:7]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        load = [r for r in rows if r[2] > 200.0] or rows  # samples under load (power)
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in load for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": float(np.median([r[0] for r in load])),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(load),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def cpu_oracle_sample(wl, seconds):
+    """Times the float64 oracle on a bounded, stratified sample of the
+    workload's query rows (each against every key it sees)."""
+    import oracle
+    import ragen
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from helpers import sample_rows
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = os.cpu_count()
+    B, Hq, Hkv, S, N, D = wl.B, wl.Hq, wl.Hkv, wl.S, wl.N, wl.D
+    g = Hq // Hkv
+    pos = oracle.positions(S, N, wl.striped)
+    rows = sample_rows(wl.seed + 7, B, Hq, S, N, 4096)
+    rng = np.random.default_rng(0)
+    rng.shuffle(rows)
+    flops = 0.0
+    done = 0
+    t_total = 0.0
+    kv_cache = {}
+    scale = 1.0 / math.sqrt(D)
+    for c0 in range(0, len(rows), 32):
+        if t_total >= seconds:
+            break
+        chunk = rows[c0:c0 + 32]
+        # group by kv head; inputs are regenerated outside the timed part
+        by = {}
+        for (b, h, p) in chunk:
+            by.setdefault((b, h // g), []).append((b, h, p))
+        for (b, kvh), rr in by.items():
+            if (b, kvh) not in kv_cache:
+                if len(kv_cache) * S * D * 16 > (8 << 30):
+                    kv_cache.clear()
+                base = (b * Hkv + kvh) * S * D
+                kk = oracle.bf16_bits_to_f64(ragen.normal_bf16(wl.seed, ragen.TENSOR_K, S * D, start=base))
+                vv = oracle.bf16_bits_to_f64(ragen.normal_bf16(wl.seed, ragen.TENSOR_V, S * D, start=base))
+                kv_cache[(b, kvh)] = (kk.reshape(S, D), vv.reshape(S, D))
+            kk, vv = kv_cache[(b, kvh)]
+            qidx = [(bb * Hq + hh) * S + pp for (bb, hh, pp) in rr]
+            qq = oracle.bf16_bits_to_f64(ragen.normal_bf16_rows(wl.seed, ragen.TENSOR_Q, qidx, D))
+            qpos = pos[[pp for (_, _, pp) in rr]]
+            t0 = time.perf_counter()
+            oracle.attend_rows(qq, qpos, kk, vv, pos, wl.causal, scale)
+            t_total += time.perf_counter() - t0
+            vis = (qpos + 1) if wl.causal else np.full(len(rr), S)
+            flops += float(4.0 * D * vis.sum())
+            done += len(rr)
+    return {"flops": flops, "seconds": t_total, "rows": done, "threads": threads}
+
+
+def reference_arm(args, wl):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    steps_t = []
+    tot_flops = 0.0
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))  # whole run within minutes
+    for s in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(wl, per_step)
+        if s >= args.warmup:
+            steps_t.append(r["seconds"])
+            tot_flops += r["flops"]
+            rows, threads = r["rows"], r["threads"]
+    t = sum(steps_t)
+    value = tot_flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wl.describe(), parallelism=f"replicas{args.gpus}"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"float64 NumPy oracle (plain softmax attention per row) on "
+                                   f"{rows} stratified query rows per step of {wl.name}, each "
+                                   f"against all keys it sees; FLOPs = 4*D*visible keys"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def main():
+    args = parse()
+    import ragen
+    wl = ragen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, wl)
+
+    import torch
+    import torch.distributed as dist
+    import exact_long_context_order_b300 as ra
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ra.lib()  # fail loudly if the library is missing
+
+    dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    qs, kvs = wl.shapes()
+    # inputs: generated on the host (same generator as the tests), pinned
+    hosts = []
+    for tid, shape in ((ragen.TENSOR_Q, qs), (ragen.TENSOR_K, kvs), (ragen.TENSOR_V, kvs)):
+        h = torch.empty(shape, dtype=torch.int16 if wl.dtype == "bf16" else torch.float32,
+                        pin_memory=True)
+        flat = h.numpy().reshape(-1)
+        if wl.dtype == "bf16":
+            ragen.normal_bf16(wl.seed, tid, h.numel(), out=flat.view(np.uint16))
+        else:
+            ragen.normal_f32(wl.seed, tid, h.numel(), out=flat)
+        hosts.append(h)
+    dev = [h.to("cuda").view(dtype) for h in hosts]
+    q, k, v = dev
+    out = torch.empty_like(q)
+    lse = torch.empty(qs[:3], dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    flops = wl.flops()
+    tokens = wl.B * wl.S
+
+    def step():
+        ra.forward(q, k, v, wl.N, causal=wl.causal, striped=wl.striped, out=out, lse=lse,
+                   stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ra.check(stream)
+
+    # ------------------------------------------------ device-resident timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        step()
+        ev[s][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    rc = ra.ra_check(ra._stream_handle(stream))
+    if rc != ra.RA_OK:
+        raise SystemExit(f"device status after timed region: {ra.ra_strerror(rc)}")
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    launch_avg_ms = float(np.mean(per_launch_ms))
+    t_max = total_ms
+    if world > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = world * flops * args.steps / (t_max * 1e-3) / 1e12
+    tok_s = world * tokens * args.steps / (t_max * 1e-3)
+
+    # ------------------------------------------------ end to end: host buffers through the C ABI
+    e2e = None
+    if not args.no_e2e:
+        out_h = torch.empty(qs, dtype=torch.int16 if wl.dtype == "bf16" else torch.float32,
+                            pin_memory=True)
+        lse_h = torch.empty(qs[:3], dtype=torch.float32, pin_memory=True)
+        qd = q.view(hosts[0].dtype)
+        kd = k.view(hosts[1].dtype)
+        vd = v.view(hosts[2].dtype)
+        od = out.view(out_h.dtype)
+        h2d = sum(h.numel() * h.element_size() for h in hosts)
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+
+        def e2e_step():
+            qd.copy_(hosts[0], non_blocking=True)
+            kd.copy_(hosts[1], non_blocking=True)
+            vd.copy_(hosts[2], non_blocking=True)
+            rc_ = ra.ra_forward(ra._ptr(q), ra._ptr(k), ra._ptr(v), ra._ptr(out), ra._ptr(lse),
+                                wl.B, wl.Hq, wl.Hkv, wl.S, wl.D, wl.N, int(wl.causal),
+                                int(wl.striped), 0.0,
+                                ra.RA_BF16 if wl.dtype == "bf16" else ra.RA_F32,
+                                ra._stream_handle(stream))
+            if rc_ != ra.RA_OK:
+                raise SystemExit(ra.ra_strerror(rc_))
+            out_h.copy_(od, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": world * flops * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms / args.steps}
+        # the e2e outputs must equal the device-resident run (same inputs)
+        if not torch.equal(out_h.to("cuda").view(dtype), out):
+            raise SystemExit("end-to-end output differs from the device-resident output")
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    achieved = flops / (launch_avg_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(wl.describe(), parallelism=f"replicas{world}",
+                       l2="inputs larger than L2 (no flush)",
+                       flops_per_step=flops, flops_exact_per_step=wl.flops_exact()),
+        "tokens_per_s": tok_s,
+        "frac_of_bf16_peak": value / world / peak,
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+                     "kernel": KERNEL_NAME, "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "frac_of_sustained": achieved / peak_sus},
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        r = cpu_oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["threads"],
+            "kind": "oracle",
+            "sample": f"float64 NumPy oracle (plain softmax attention per row) on {r['rows']} "
+                      f"stratified query rows of {wl.name}, each against all keys it sees; "
+                      f"FLOPs = 4*D*visible keys; {r['seconds']:.1f} s of CPU time"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -67,6 +67,9 @@ WORKLOADS = {
                                    2, 32, 32, 32768, 8, 128, True, True),
     "gqa_128k": Workload(3, "bf16_causal_gqa_B1_Hq32_Hkv8_S131072_N16_D128_striped", "bf16",
                          1, 32, 8, 131072, 16, 128, True, True),
+    # profiling case: same kernel shape as gqa_128k, inputs larger than L2 but under 1 GB
+    "prof_64k": Workload(5, "bf16_causal_gqa_B1_Hq16_Hkv4_S65536_N8_D128_striped", "bf16",
+                         1, 16, 4, 65536, 8, 128, True, True),
     "long_1m": Workload(4, "bf16_causal_gqa_B1_Hq8_Hkv1_S1048576_N64_D128_striped", "bf16",
                         1, 8, 1, 1048576, 64, 128, True, True),
 }
