@@ -47,6 +47,10 @@ constexpr int kT = 128;             // query and key tile size
 constexpr int kThreads = 384;       // 12 warps
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // per wait
 constexpr uint64_t kDrainNs = 200000000ull;
+// Register split: 384 threads launched at 168 registers (64512 in total);
+// warpgroup 0 (producer, MMA, TMEM owner) drops to 80, the two softmax
+// warpgroups rise to 208: 128*80 + 256*208 = 63488 <= 64512.
+constexpr uint32_t kRegsOther = 80, kRegsSoftmax = 208;
 
 template <int D>
 struct Cfg {
@@ -155,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    if (warp < 4) regs_dec<kRegsOther>();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -211,21 +216,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t qa = base + C::kQOff + t * C::kTileBytes;
                 const uint32_t ka = base + C::kKVOff + stK * C::kTileBytes;
                 const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+                const uint64_t dq = make_sdesc(qa, 16, 1024, kLayoutSW128);
+                const uint64_t dk = make_sdesc(ka, 16, 1024, kLayoutSW128);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (kT * 128) + (kk % 4) * 32;
-                    umma_ss(d, make_sdesc(qa + off, 16, 1024, kLayoutSW128),
-                            make_sdesc(ka + off, 16, 1024, kLayoutSW128), idesc_s, kk > 0);
+                    // start address advances in 16-byte units inside the descriptor
+                    const uint32_t off16 = ((kk / 4) * (kT * 128) + (kk % 4) * 32) >> 4;
+                    umma_ss(d, dq + off16, dk + off16, idesc_s, kk > 0);
                 }
             };
             auto issue_pv = [&](int t, uint32_t stV, bool acc) {
                 const uint32_t va = base + C::kKVOff + stV * C::kTileBytes;
                 const uint32_t pa = tmem + (t ? C::kColS1 : C::kColS0);
                 const uint32_t o = tmem + (t ? C::kColO1 : C::kColO0);
+                const uint64_t dv = make_sdesc(va, kT * 128, 1024, kLayoutSW128);
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
-                    umma_ts(o, pa + kk * 8, make_sdesc(va + kk * 2048, kT * 128, 1024, kLayoutSW128),
-                            idesc_o, (kk > 0 || acc) ? 1u : 0u);
+                    umma_ts(o, pa + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                            (kk > 0 || acc) ? 1u : 0u);
             };
             uint32_t kv_pos = 0, gt = 0;
             int k = 0;
@@ -294,14 +302,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 drain_wait(bar(C::bDrain), 0);
             }
         }
-    } else if (warp >= 4) {
+    } else if (warp < 4) {
+        // warps 2-3: TMEM owner / idle
+    } else {
         // ------------------------------------------------------------ softmax
+        regs_inc<kRegsSoftmax>();
         const int t = (warp - 4) >> 2;
         const int r = tid - 128 * (1 + t);  // query row of the tile == TMEM lane
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_tm = tmem + lane_off + (t ? C::kColS1 : C::kColS0);
         const uint32_t o_tm = tmem + lane_off + (t ? C::kColO1 : C::kColO0);
         const float sl2 = p.sl2;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
         uint32_t gt = 0;
         int k = 0;
         bool ok = true;
@@ -318,12 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait_bar(bar(C::bSFull + t), gt & 1, abort_flag, p.status);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t pk[2][32];
                 if (kind == kNone) {
+                    uint32_t z[32];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) pk[c][e] = 0u;
+                    for (int e = 0; e < 32; ++e) z[e] = 0u;
+                    tmem_st32(s_tm + 0, z);
+                    tmem_st32(s_tm + 32, z);
                 } else {
                     uint32_t sr[4][32];
 #pragma unroll
@@ -339,19 +351,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 32; ++e)
                                 if (c * 32 + e > lim) sr[c][e] = __float_as_uint(-INFINITY);
                     }
+                    // row max: four independent chains of three-input max
                     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        mx0 = fmaxf(mx0, fmaxf(__uint_as_float(sr[0][e]), __uint_as_float(sr[1][e])));
-                        mx1 = fmaxf(mx1, fmaxf(__uint_as_float(sr[2][e]), __uint_as_float(sr[3][e])));
-                        mx2 = fmaxf(mx2, fmaxf(__uint_as_float(sr[0][e + 1]), __uint_as_float(sr[1][e + 1])));
-                        mx3 = fmaxf(mx3, fmaxf(__uint_as_float(sr[2][e + 1]), __uint_as_float(sr[3][e + 1])));
-                        mx0 = fmaxf(mx0, fmaxf(__uint_as_float(sr[0][e + 2]), __uint_as_float(sr[1][e + 2])));
-                        mx1 = fmaxf(mx1, fmaxf(__uint_as_float(sr[2][e + 2]), __uint_as_float(sr[3][e + 2])));
-                        mx2 = fmaxf(mx2, fmaxf(__uint_as_float(sr[0][e + 3]), __uint_as_float(sr[1][e + 3])));
-                        mx3 = fmaxf(mx3, fmaxf(__uint_as_float(sr[2][e + 3]), __uint_as_float(sr[3][e + 3])));
+                    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8) {
+                            mx0 = max3f(mx0, __uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1]));
+                            mx1 = max3f(mx1, __uint_as_float(sr[c][e + 2]), __uint_as_float(sr[c][e + 3]));
+                            mx2 = max3f(mx2, __uint_as_float(sr[c][e + 4]), __uint_as_float(sr[c][e + 5]));
+                            mx3 = max3f(mx3, __uint_as_float(sr[c][e + 6]), __uint_as_float(sr[c][e + 7]));
+                        }
                     }
-                    const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                    const float mx = max3f(mx0, mx1, fmaxf(mx2, mx3));
                     const float m_new = fmaxf(m_used, mx);
                     // rescale only when the max grew by more than 2^8 (in exp2 units)
                     const bool need = (m_new - m_used) * sl2 > 8.0f;
@@ -363,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         l *= alpha;
                         if (n > 0) {
+                            const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
                             for (int c = 0; c < D / 32; ++c) {
                                 uint32_t o[32];
@@ -370,34 +383,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tmem_wait_ld();
                                 reg_fence(o);
 #pragma unroll
-                                for (int e = 0; e < 32; ++e)
-                                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                                for (int e = 0; e < 32; e += 2) {
+                                    float lo, hi;
+                                    f2_unpack(f2_mul(f2_pack_u(o[e], o[e + 1]), a2), lo, hi);
+                                    o[e] = __float_as_uint(lo);
+                                    o[e + 1] = __float_as_uint(hi);
+                                }
                                 tmem_st32(o_tm + c * 32, o);
                             }
                         }
                     }
                     const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
-                    float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+                    const uint64_t nmb2 = f2_pack(-mb, -mb);
+                    uint64_t acc0 = 0, acc1 = 0;  // packed fp32 pairs (0.0f, 0.0f)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int h = 0; h < 2; ++h) {  // P half h: keys [64h, 64h + 64)
+                        uint32_t pk[32];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4) {
-                            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c][e]), sl2, -mb));
-                            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -mb));
-                            const float p2 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 2]), sl2, -mb));
-                            const float p3 = ex2_approx(fmaf(__uint_as_float(sr[c][e + 3]), sl2, -mb));
-                            sum0 += p0;
-                            sum1 += p1;
-                            sum2 += p2;
-                            sum3 += p3;
-                            pk[c >> 1][(c & 1) * 16 + e / 2] = pack_bf16x2(p0, p1);
-                            pk[c >> 1][(c & 1) * 16 + e / 2 + 1] = pack_bf16x2(p2, p3);
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int c = 2 * h + cc;
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4) {
+                                const uint64_t x01 = f2_fma(f2_pack_u(sr[c][e], sr[c][e + 1]), sl2x2, nmb2);
+                                const uint64_t x23 = f2_fma(f2_pack_u(sr[c][e + 2], sr[c][e + 3]), sl2x2, nmb2);
+                                float a0, a1, a2, a3;
+                                f2_unpack(x01, a0, a1);
+                                f2_unpack(x23, a2, a3);
+                                const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                                const float p2 = ex2_approx(a2), p3 = ex2_approx(a3);
+                                acc0 = f2_add(acc0, f2_pack(p0, p1));
+                                acc1 = f2_add(acc1, f2_pack(p2, p3));
+                                pk[cc * 16 + e / 2] = pack_bf16x2(p0, p1);
+                                pk[cc * 16 + e / 2 + 1] = pack_bf16x2(p2, p3);
+                            }
                         }
+                        tmem_st32(s_tm + 32 * h, pk);
                     }
-                    l += (sum0 + sum1) + (sum2 + sum3);
+                    float s0, s1, s2, s3;
+                    f2_unpack(f2_add(acc0, acc1), s0, s1);
+                    (void)s2;
+                    (void)s3;
+                    l += s0 + s1;
                 }
-                tmem_st32(s_tm + 0, pk[0]);
-                tmem_st32(s_tm + 32, pk[1]);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -426,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t row = (int64_t)(it.b * G.Hq + it.h[t]) * p.S + (int64_t)it.i * p.Sb +
                                     (int64_t)qt * kT + r;
                 const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+                const uint64_t inv2 = f2_pack(inv_l, inv_l);
                 uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -433,15 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(o_tm + c * 32, o);
                     tmem_wait_ld();
                     reg_fence(o);
+                    uint32_t pkd[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 v4;
-                        v4.x = pack_bf16x2(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
-                        v4.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
-                        v4.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv_l, __uint_as_float(o[e + 5]) * inv_l);
-                        v4.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv_l, __uint_as_float(o[e + 7]) * inv_l);
-                        orow[c * 4 + e / 8] = v4;
+                    for (int e = 0; e < 32; e += 2) {
+                        float lo, hi;
+                        f2_unpack(f2_mul(f2_pack_u(o[e], o[e + 1]), inv2), lo, hi);
+                        pkd[e / 2] = pack_bf16x2(lo, hi);
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        orow[c * 4 + e] = make_uint4(pkd[4 * e], pkd[4 * e + 1], pkd[4 * e + 2], pkd[4 * e + 3]);
                 }
                 if (p.lse)
                     p.lse[row] = (l > 0.f) ? (m_used * sl2 + lg2_approx(l)) * 0.69314718055994531f
