@@ -14,10 +14,12 @@
 //    works on items of two query tiles ("slots") that share each K/V tile.
 //  * warp 0, lane 0 -- TMA producer: Q tiles once per item, then K and V
 //    tiles into a ring of smem stages (128B-swizzled, 2 boxes of 64 columns).
-//  * warp 1, lane 0 -- MMA issuer: S_t = Q_t K^T (SS, M=128 N=128 K=16 steps)
-//    into TMEM, and O_t += P_t V (P read from TMEM, V MN-major from smem).
-//    Per key tile the order is PV_0(n-1), S_0(n), PV_1(n-1), S_1(n): while one
-//    softmax warpgroup works, the tensor core runs the other slot's MMAs.
+//  * lane 0 of warps 1 and 3 -- MMA issuers, one per slot: S_t = Q_t K^T (SS,
+//    M=128 N=128 K=16 steps) into TMEM, and O_t += P_t V (P read from TMEM, V
+//    MN-major from smem).  A token passed between them keeps the pipe order
+//    PV_0(n-1) S_0(n) | PV_1(n-1) S_1(n) | ...: while one softmax warpgroup
+//    works, the tensor core runs the other slot's MMAs, and each issuer's
+//    waits overlap the other issuer's MMA issue.
 //  * warp 2 owns the TMEM allocation.
 //  * warps 4-7 / 8-11 -- softmax for slot 0 / 1, one thread per query row
 //    (row r = TMEM lane r): load the S row, mask the diagonal tile, update
@@ -45,8 +47,9 @@ namespace tc {
 
 constexpr int kT = 128;             // query and key tile size
 constexpr int kThreads = 384;       // 12 warps
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // per wait
-constexpr uint64_t kDrainNs = 200000000ull;
+// Bounded waits count SM clock cycles (4e9 cycles is 2 s at 2 GHz, longer at lower clocks).
+constexpr long long kTimeoutCycles = 4000000000ll;
+constexpr long long kDrainCycles = 400000000ll;
 // Register split: 384 threads launched at 168 registers (64512 in total);
 // warpgroup 0 (producer, MMA, TMEM owner) drops to 80, the two softmax
 // warpgroups rise to 208: 128*80 + 256*208 = 63488 <= 64512.
@@ -61,8 +64,8 @@ struct Cfg {
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
     // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
-    // o_full[2], o_empty[2], drain
-    static constexpr int kNumBars = 2 + 2 * kStages + 9;
+    // o_full[2], o_empty[2], drain[2], token[2]
+    static constexpr int kNumBars = 2 + 2 * kStages + 12;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
     static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
@@ -70,7 +73,7 @@ struct Cfg {
     // barrier indices
     static constexpr int bQFull = 0, bQEmpty = 1, bKVFull = 2, bKVEmpty = 2 + kStages,
                          bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
-                         bOEmpty = bOFull + 2, bDrain = bOEmpty + 2;
+                         bOEmpty = bOFull + 2, bDrain = bOEmpty + 2, bToken = bDrain + 2;
 };
 
 struct Params {
@@ -89,13 +92,12 @@ struct Params {
 __device__ __forceinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag,
                                          unsigned int* status) {
     if (mbar_try_wait(b, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    uint32_t it = 0;
-    for (;;) {
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(b, parity)) return true;
-        if ((++it & 31u) == 0) {
+        if ((it & 255u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kTimeoutNs) {
+            if (clock64() - t0 > kTimeoutCycles) {
                 *abort_flag = 1;
                 atomicOr(status, kStatusTimeout);
                 return false;
@@ -105,9 +107,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile i
 }
 // Short bounded wait used only while draining after an abort.
 __device__ __forceinline__ void drain_wait(uint32_t b, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
     while (!mbar_try_wait(b, parity)) {
-        if (globaltimer_ns() - t0 > kDrainNs) return;
+        if (clock64() - t0 > kDrainCycles) return;
     }
 }
 
@@ -130,10 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(bar(C::bQFull), 1);
-        mbar_init(bar(C::bQEmpty), 1);
+        mbar_init(bar(C::bQEmpty), 2);  // one commit per MMA issuer
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(bar(C::bKVFull + s), 1);
-            mbar_init(bar(C::bKVEmpty + s), 1);
+            mbar_init(bar(C::bKVEmpty + s), 2);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(C::bSFull + t), 1);
@@ -141,7 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(C::bOFull + t), 1);
             mbar_init(bar(C::bOEmpty + t), 4);
         }
-        mbar_init(bar(C::bDrain), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(C::bDrain + t), 1);
+            mbar_init(bar(C::bToken + t), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -207,33 +212,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     drain_wait(bar(C::bKVFull + pos % C::kStages), (pos / C::kStages) & 1);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ MMA issuers
+        // Lane 0 of warp 1 issues slot 0's MMAs, lane 0 of warp 3 slot 1's.  A
+        // token (two mbarriers) makes them take turns block by block, so the
+        // tensor pipe still sees PV_0 S_0 | PV_1 S_1 | PV_0 S_0 ... in order,
+        // while each issuer's own waits overlap the other's issue.
         if (lane == 0) {
+            const int t = (warp == 1) ? 0 : 1;
             constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
             constexpr uint32_t idesc_o = make_idesc_bf16(128, D, false, true);
-            auto issue_s = [&](int t, uint32_t stK) {
-                const uint32_t qa = base + C::kQOff + t * C::kTileBytes;
-                const uint32_t ka = base + C::kKVOff + stK * C::kTileBytes;
-                const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
-                const uint64_t dq = make_sdesc(qa, 16, 1024, kLayoutSW128);
-                const uint64_t dk = make_sdesc(ka, 16, 1024, kLayoutSW128);
+            const uint32_t qa = base + C::kQOff + t * C::kTileBytes;
+            const uint32_t s_tm = tmem + (t ? C::kColS1 : C::kColS0);
+            const uint32_t o_tm = tmem + (t ? C::kColO1 : C::kColO0);
+            const uint64_t dq = make_sdesc(qa, 16, 1024, kLayoutSW128);
+            auto issue_s = [&](uint32_t stK) {
+                const uint64_t dk =
+                    make_sdesc(base + C::kKVOff + stK * C::kTileBytes, 16, 1024, kLayoutSW128);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     // start address advances in 16-byte units inside the descriptor
                     const uint32_t off16 = ((kk / 4) * (kT * 128) + (kk % 4) * 32) >> 4;
-                    umma_ss(d, dq + off16, dk + off16, idesc_s, kk > 0);
+                    umma_ss(s_tm, dq + off16, dk + off16, idesc_s, kk > 0);
                 }
             };
-            auto issue_pv = [&](int t, uint32_t stV, bool acc) {
-                const uint32_t va = base + C::kKVOff + stV * C::kTileBytes;
-                const uint32_t pa = tmem + (t ? C::kColS1 : C::kColS0);
-                const uint32_t o = tmem + (t ? C::kColO1 : C::kColO0);
-                const uint64_t dv = make_sdesc(va, kT * 128, 1024, kLayoutSW128);
+            auto issue_pv = [&](uint32_t stV, bool acc) {
+                const uint64_t dv = make_sdesc(base + C::kKVOff + stV * C::kTileBytes, kT * 128,
+                                               1024, kLayoutSW128);
 #pragma unroll
                 for (int kk = 0; kk < kT / 16; ++kk)
-                    umma_ts(o, pa + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                    umma_ts(o_tm, s_tm + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
                             (kk > 0 || acc) ? 1u : 0u);
+            };
+            // block counter: slot 0 issues its block b after slot 1's block b-1,
+            // slot 1 issues block b after slot 0's block b
+            uint32_t bc = 0;
+            auto take_turn = [&]() -> bool {
+                if (t == 0) return bc == 0 || wait_bar(bar(C::bToken + 0), (bc - 1) & 1, abort_flag, p.status);
+                return wait_bar(bar(C::bToken + 1), bc & 1, abort_flag, p.status);
+            };
+            auto pass_turn = [&]() {
+                mbar_arrive(bar(C::bToken + (t == 0 ? 1 : 0)));
+                ++bc;
             };
             uint32_t kv_pos = 0, gt = 0;
             int k = 0;
@@ -241,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (long long item = blockIdx.x; item < G.n_items && ok; item += gridDim.x, ++k) {
                 const Item it = decode_item(G, item);
                 if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status))) break;
-                tc_fence_after();
                 TileWalk w;
                 uint32_t n = 0;
                 for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n) {
@@ -256,54 +275,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1,
                                             abort_flag, p.status)))
                             break;
+                        if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag,
+                                            p.status)))
+                            break;
+                        if (n == 1 && k > 0 &&
+                            !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag,
+                                            p.status)))
+                            break;
                     }
+                    if (!(ok = take_turn())) break;
                     tc_fence_after();
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        if (n > 0) {
-                            if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag,
-                                                p.status)))
-                                break;
-                            if (n == 1 && k > 0 &&
-                                !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag,
-                                                p.status)))
-                                break;
-                            tc_fence_after();
-                            issue_pv(t, stV, n > 1);
-                            if (t == 1) umma_commit(bar(C::bKVEmpty + stV));
-                        }
-                        issue_s(t, stK);
-                        umma_commit(bar(C::bSFull + t));
-                        if (t == 1) umma_commit(bar(C::bKVEmpty + stK));
+                    if (n > 0) {
+                        issue_pv(stV, n > 1);
+                        umma_commit(bar(C::bKVEmpty + stV));
                     }
-                    if (!ok) break;
+                    issue_s(stK);
+                    pass_turn();
+                    umma_commit(bar(C::bSFull + t));
+                    umma_commit(bar(C::bKVEmpty + stK));
                     kv_pos += 2;
                     ++gt;
                 }
                 if (!ok) break;
-                umma_commit(bar(C::bQEmpty));  // every S MMA of this item has been issued
+                umma_commit(bar(C::bQEmpty));  // every S MMA of this slot and item is issued
                 const uint32_t vp = kv_pos - 1, stV = vp % C::kStages;
                 if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1, abort_flag,
                                     p.status)))
                     break;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag, p.status)))
-                        break;
-                    if (n == 1 && k > 0 &&
-                        !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag, p.status)))
-                        break;
-                    tc_fence_after();
-                    issue_pv(t, stV, n > 1);
-                    umma_commit(bar(C::bOFull + t));
-                    if (t == 1) umma_commit(bar(C::bKVEmpty + stV));
-                }
+                if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag, p.status)))
+                    break;
+                if (n == 1 && k > 0 &&
+                    !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag, p.status)))
+                    break;
+                if (!(ok = take_turn())) break;
+                tc_fence_after();
+                issue_pv(stV, n > 1);
+                pass_turn();
+                umma_commit(bar(C::bOFull + t));
+                umma_commit(bar(C::bKVEmpty + stV));
             }
             if (!ok) {
-                umma_commit(bar(C::bDrain));
-                drain_wait(bar(C::bDrain), 0);
+                *abort_flag = 1;
+                umma_commit(bar(C::bDrain + t));
+                drain_wait(bar(C::bDrain + t), 0);
             }
         }
     } else if (warp < 4) {
-        // warps 2-3: TMEM owner / idle
+        // warp 2: TMEM owner
     } else {
         // ------------------------------------------------------------ softmax
         regs_inc<kRegsSoftmax>();
