@@ -63,16 +63,17 @@ struct Cfg {
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
-    // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
+    // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_lo[2], p_hi[2],
     // o_full[2], o_empty[2], drain[2], token[2]
-    static constexpr int kNumBars = 2 + 2 * kStages + 12;
+    static constexpr int kNumBars = 2 + 2 * kStages + 14;
     static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
     static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
     // barrier indices
     static constexpr int bQFull = 0, bQEmpty = 1, bKVFull = 2, bKVEmpty = 2 + kStages,
-                         bSFull = 2 + 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
+                         bSFull = 2 + 2 * kStages, bPLo = bSFull + 2, bPHi = bPLo + 2,
+                         bOFull = bPHi + 2,
                          bOEmpty = bOFull + 2, bDrain = bOEmpty + 2, bToken = bDrain + 2;
 };
 
@@ -139,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(C::bSFull + t), 1);
-            mbar_init(bar(C::bPFull + t), 4);
+            mbar_init(bar(C::bPLo + t), 4);
+            mbar_init(bar(C::bPHi + t), 4);
             mbar_init(bar(C::bOFull + t), 1);
             mbar_init(bar(C::bOEmpty + t), 4);
         }
@@ -236,13 +238,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_ss(s_tm, dq + off16, dk + off16, idesc_s, kk > 0);
                 }
             };
-            auto issue_pv = [&](uint32_t stV, bool acc) {
+            // O += P[:, 64h : 64h+64] V[64h : 64h+64, :]  (keys half h)
+            auto issue_pv_half = [&](uint32_t stV, int h, bool acc) {
                 const uint64_t dv = make_sdesc(base + C::kKVOff + stV * C::kTileBytes, kT * 128,
                                                1024, kLayoutSW128);
 #pragma unroll
-                for (int kk = 0; kk < kT / 16; ++kk)
+                for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
                     umma_ts(o_tm, s_tm + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), idesc_o,
                             (kk > 0 || acc) ? 1u : 0u);
+            };
+            // P of the previous key tile arrives in two halves; the first half's
+            // MMAs run while the softmax still computes the second half.  The
+            // caller has already waited for the first half.
+            auto issue_pv = [&](uint32_t stV, bool acc, uint32_t g) -> bool {
+                issue_pv_half(stV, 0, acc);
+                if (!wait_bar(bar(C::bPHi + t), g & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
+                issue_pv_half(stV, 1, acc);
+                return true;
             };
             // block counter: slot 0 issues its block b after slot 1's block b-1,
             // slot 1 issues block b after slot 0's block b
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1,
                                             abort_flag, p.status)))
                             break;
-                        if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag,
+                        if (!(ok = wait_bar(bar(C::bPLo + t), (gt - 1) & 1, abort_flag,
                                             p.status)))
                             break;
                         if (n == 1 && k > 0 &&
@@ -286,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = take_turn())) break;
                     tc_fence_after();
                     if (n > 0) {
-                        issue_pv(stV, n > 1);
+                        if (!(ok = issue_pv(stV, n > 1, gt - 1))) break;
                         umma_commit(bar(C::bKVEmpty + stV));
                     }
                     issue_s(stK);
@@ -302,14 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1, abort_flag,
                                     p.status)))
                     break;
-                if (!(ok = wait_bar(bar(C::bPFull + t), (gt - 1) & 1, abort_flag, p.status)))
+                if (!(ok = wait_bar(bar(C::bPLo + t), (gt - 1) & 1, abort_flag, p.status)))
                     break;
                 if (n == 1 && k > 0 &&
                     !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag, p.status)))
                     break;
                 if (!(ok = take_turn())) break;
                 tc_fence_after();
-                issue_pv(stV, n > 1);
+                if (!(ok = issue_pv(stV, n > 1, gt - 1))) break;
                 pass_turn();
                 umma_commit(bar(C::bOFull + t));
                 umma_commit(bar(C::bKVEmpty + stV));
@@ -354,6 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e) z[e] = 0u;
                     tmem_st32(s_tm + 0, z);
                     tmem_st32(s_tm + 32, z);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::bPLo + t));
                 } else {
                     uint32_t sr[4][32];
 #pragma unroll
@@ -436,6 +453,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         tmem_st32(s_tm + 32 * h, pk);
+                        if (h == 0) {  // first 64 keys of P are in TMEM: let P.V start on them
+                            tmem_wait_st();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(C::bPLo + t));
+                        }
                     }
                     float s0, s1, s2, s3;
                     f2_unpack(f2_add(acc0, acc1), s0, s1);
@@ -446,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::bPFull + t));
+                if (lane == 0) mbar_arrive(bar(C::bPHi + t));
                 if (LOG && valid && kind != kNone && r == 0) {
                     const int64_t unit =
                         ((int64_t)(it.b * G.Hq + it.h[t]) * G.rg.N + it.i) * G.rg.nt + qt;
