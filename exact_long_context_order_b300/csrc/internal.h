@@ -30,8 +30,10 @@ struct FoldLog {
 
 // Returns 0 on success or an RA_ERR_* code.  status: device pointer to this
 // device's status word.  sm_count: multiprocessors of the current device.
-int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, int sm_count,
-              cudaStream_t stream);
+// work: device counter the kernel takes work items from; zeroed by launch_tc
+// on `stream` before the launch.
+int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, unsigned int* work,
+              int sm_count, cudaStream_t stream);
 bool tc_supported(const FwdProblem& p);
 int launch_simt(const FwdProblem& p, unsigned int* status, cudaStream_t stream);
 int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,

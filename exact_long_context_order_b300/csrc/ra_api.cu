@@ -20,8 +20,15 @@ namespace {
 __device__ unsigned int g_ra_status;
 
 constexpr int kMaxDevices = 64;
+// Work counters of the tensor-core kernel: one small block per device,
+// allocated on first use, holding kWorkSlots counters; each launch takes the
+// next slot (zeroed on its stream), so up to kWorkSlots launches may be in
+// flight on one device at once.
+constexpr int kWorkSlots = 64;
 std::mutex g_mu;
 unsigned int* g_status_ptr[kMaxDevices];
+unsigned int* g_work[kMaxDevices];
+unsigned int g_work_next[kMaxDevices];
 int g_sm_count[kMaxDevices];
 int g_arch_ok[kMaxDevices];  // 0 unknown, 1 sm_103, -1 other
 thread_local char g_cuda_msg[256] = "";
@@ -55,6 +62,23 @@ int device_state(unsigned int** status, int* sm_count) {
     }
     if (status) *status = g_status_ptr[dev];
     if (sm_count) *sm_count = g_sm_count[dev];
+    return RA_OK;
+}
+
+// Next work-counter slot of the current device (allocates the block once).
+int work_slot(unsigned int** slot) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { note_cuda(e); return RA_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_work[dev]) {
+        void* p = nullptr;
+        if ((e = cudaMalloc(&p, kWorkSlots * 64)) != cudaSuccess) { note_cuda(e); return RA_ERR_CUDA; }
+        g_work[dev] = static_cast<unsigned int*>(p);
+    }
+    // 64-byte spacing keeps concurrent launches' counters on separate lines
+    *slot = g_work[dev] + (g_work_next[dev]++ % kWorkSlots) * 16;
     return RA_OK;
 }
 
@@ -104,9 +128,11 @@ int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float*
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool tc_ok = ra::tc_supported(p);
     if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
-    if (kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok))
-        rc = ra::launch_tc(p, nullptr, status, sms, st);
-    else
+    if (kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok)) {
+        unsigned int* work = nullptr;
+        if ((rc = work_slot(&work))) return rc;
+        rc = ra::launch_tc(p, nullptr, status, work, sms, st);
+    } else
         rc = ra::launch_simt(p, status, st);
     if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
     return rc;
@@ -133,7 +159,9 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
     ra::FoldLog fl{log, counts, max_entries};
-    rc = ra::launch_tc(p, &fl, status, sms, static_cast<cudaStream_t>(stream));
+    unsigned int* work = nullptr;
+    if ((rc = work_slot(&work))) return rc;
+    rc = ra::launch_tc(p, &fl, status, work, sms, static_cast<cudaStream_t>(stream));
     if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
     return rc;
 }

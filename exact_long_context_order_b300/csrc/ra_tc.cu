@@ -64,9 +64,9 @@ struct Cfg {
     static constexpr int kKVOff = 2 * kTileBytes;
     static constexpr int kBarOff = kKVOff + kStages * kTileBytes;
     // q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_lo[2], p_hi[2],
-    // o_full[2], o_empty[2], drain[2], token[2]
-    static constexpr int kNumBars = 2 + 2 * kStages + 14;
-    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
+    // o_full[2], o_empty[2], drain[2], token[2], item_full[2], item_empty[2]
+    static constexpr int kNumBars = 2 + 2 * kStages + 18;
+    static constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 16 + 1024;
     static constexpr uint32_t kColS0 = 0, kColS1 = 128;
     static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
@@ -74,7 +74,10 @@ struct Cfg {
     static constexpr int bQFull = 0, bQEmpty = 1, bKVFull = 2, bKVEmpty = 2 + kStages,
                          bSFull = 2 + 2 * kStages, bPLo = bSFull + 2, bPHi = bPLo + 2,
                          bOFull = bPHi + 2,
-                         bOEmpty = bOFull + 2, bDrain = bOEmpty + 2, bToken = bDrain + 2;
+                         bOEmpty = bOFull + 2, bDrain = bOEmpty + 2, bToken = bDrain + 2,
+                         bItemFull = bToken + 2, bItemEmpty = bItemFull + 2;
+    // readers of each published item: two MMA issuers + eight softmax warps
+    static constexpr uint32_t kItemReaders = 10;
 };
 
 struct Params {
@@ -88,6 +91,7 @@ struct Params {
     int32_t* log;
     int32_t* counts;
     int max_entries;
+    unsigned int* work;  // item counter, zero at launch: CTAs take items in order
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag,
@@ -126,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBarOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile long long* item_slot = reinterpret_cast<volatile long long*>(tmem_slot + 4);  // [2]
     auto bar = [&](int idx) -> uint32_t { return base + C::kBarOff + idx * 8; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -148,6 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(C::bDrain + t), 1);
             mbar_init(bar(C::bToken + t), 1);
+            mbar_init(bar(C::bItemFull + t), 1);
+            mbar_init(bar(C::bItemEmpty + t), C::kItemReaders);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -166,20 +173,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Work items are handed out dynamically in their longest-first order: the
+    // producer takes the next index from the global counter one item ahead and
+    // publishes it in a two-entry shared ring; every role reads it from there.
+    // An index >= n_items ends the CTA's loop.
+    auto read_item = [&](int k, bool& ok) -> long long {
+        ok = wait_bar(bar(C::bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status);
+        return ok ? item_slot[k & 1] : G.n_items;
+    };
     if (warp < 4) regs_dec<kRegsOther>();
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            uint32_t kv_pos = 0;
+            uint32_t kv_pos = 0, q_loads = 0;
             int k = 0;
             bool ok = true;
-            for (long long item = blockIdx.x; item < G.n_items; item += gridDim.x, ++k) {
+            auto publish = [&](int kk, long long v) -> bool {
+                if (kk >= 2 && !wait_bar(bar(C::bItemEmpty + (kk & 1)), ((kk >> 1) - 1) & 1,
+                                         abort_flag, p.status))
+                    return false;
+                item_slot[kk & 1] = v;
+                mbar_arrive(bar(C::bItemFull + (kk & 1)));
+                return true;
+            };
+            long long item = (long long)atomicAdd(p.work, 1u);
+            ok = publish(0, item);
+            for (; ok && item < G.n_items; ++k) {
+                const long long next = (long long)atomicAdd(p.work, 1u);
+                if (!(ok = publish(k + 1, next))) break;
                 const Item it = decode_item(G, item);
+                item = next;
                 if (k > 0 && !(ok = wait_bar(bar(C::bQEmpty), (k - 1) & 1, abort_flag, p.status)))
                     break;
                 mbar_arrive_expect_tx(bar(C::bQFull), 2 * C::kTileBytes);
+                ++q_loads;
                 for (int t = 0; t < 2; ++t) {
                     const int row = (int)((int64_t)(it.b * G.Hq + it.h[t]) * p.S +
                                           (int64_t)it.i * p.Sb + (int64_t)it.qt[t] * kT);
@@ -208,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 // let every copy that may still be in flight land before exit
-                if (k > 0 || G.n_items > blockIdx.x) drain_wait(bar(C::bQFull), k & 1);
+                if (q_loads > 0) drain_wait(bar(C::bQFull), (q_loads - 1) & 1);
                 const uint32_t first = kv_pos > (uint32_t)C::kStages ? kv_pos - C::kStages : 0;
                 for (uint32_t pos = first; pos < kv_pos; ++pos)
                     drain_wait(bar(C::bKVFull + pos % C::kStages), (pos / C::kStages) & 1);
@@ -271,7 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t kv_pos = 0, gt = 0;
             int k = 0;
             bool ok = true;
-            for (long long item = blockIdx.x; item < G.n_items && ok; item += gridDim.x, ++k) {
+            for (;; ++k) {
+                const long long item = read_item(k, ok);
+                if (ok) mbar_arrive(bar(C::bItemEmpty + (k & 1)));
+                if (!ok || item >= G.n_items) break;
                 const Item it = decode_item(G, item);
                 if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status))) break;
                 TileWalk w;
@@ -348,7 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t gt = 0;
         int k = 0;
         bool ok = true;
-        for (long long item = blockIdx.x; item < G.n_items && ok; item += gridDim.x, ++k) {
+        for (;; ++k) {
+            const long long item = read_item(k, ok);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::bItemEmpty + (k & 1)));
+            if (item >= G.n_items) break;
             const Item it = decode_item(G, item);
             const int qt = it.qt[t];
             const bool valid = (t == 0) || it.valid1;
@@ -571,7 +608,7 @@ static bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int D) {
 
 template <int D, bool LOG>
 static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* status,
-                       int sm_count, cudaStream_t stream) {
+                       unsigned int* work, int sm_count, cudaStream_t stream) {
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv;
     const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
@@ -590,7 +627,9 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     P.log = flog ? flog->log : nullptr;
     P.counts = flog ? flog->counts : nullptr;
     P.max_entries = flog ? flog->max_entries : 0;
+    P.work = work;
     if (P.G.n_items <= 0) return RA_OK;
+    if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
     auto kern = fwd_kernel<D, LOG>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
@@ -612,14 +651,15 @@ bool tc_supported(const FwdProblem& p) {
     return true;
 }
 
-int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, int sm_count,
-              cudaStream_t stream) {
+int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, unsigned int* work,
+              int sm_count, cudaStream_t stream) {
     if (!tc_supported(p)) return RA_ERR_UNSUPPORTED;
+    if (!work) return RA_ERR_INVALID_ARG;
     if (p.D == 128)
-        return flog ? tc::launch_impl<128, true>(p, flog, status, sm_count, stream)
-                    : tc::launch_impl<128, false>(p, flog, status, sm_count, stream);
-    return flog ? tc::launch_impl<64, true>(p, flog, status, sm_count, stream)
-                : tc::launch_impl<64, false>(p, flog, status, sm_count, stream);
+        return flog ? tc::launch_impl<128, true>(p, flog, status, work, sm_count, stream)
+                    : tc::launch_impl<128, false>(p, flog, status, work, sm_count, stream);
+    return flog ? tc::launch_impl<64, true>(p, flog, status, work, sm_count, stream)
+                : tc::launch_impl<64, false>(p, flog, status, work, sm_count, stream);
 }
 
 }  // namespace ra

@@ -20,9 +20,12 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - All tensor arguments are DEVICE pointers to memory the caller owns; the
- *   library never frees or keeps them.  The library allocates no device
- *   memory for its kernels except one status word per device (a static
- *   __device__ variable created with the module).
+ *   library never frees or keeps them.  Besides one status word per device
+ *   (a static __device__ variable created with the module), the library
+ *   allocates one 4 KiB block per device on the first tensor-core launch on
+ *   that device (cudaMalloc, kept until exit): 64 work-queue counters, one
+ *   per launch in flight, each zeroed on the launch's stream.  Make the first
+ *   such call on a device outside CUDA-graph stream capture.
  * - Layout is "shard-major": q and out are [B, Hq, S, D], k and v are
  *   [B, Hkv, S, D], lse is [B, Hq, S]; all row-major and contiguous.  Shard i
  *   owns rows [i*Sb, (i+1)*Sb) of every (b, h) slice, Sb = S / N.  With
