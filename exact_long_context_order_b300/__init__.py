@@ -35,6 +35,8 @@ _SIGNATURES = {
     "ra_plan": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)], _i32),
     "ra_fold_log": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
                      _f32, _vp, _vp, _i32, _vp], _i32),
+    "ra_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                            _i32, _f32, _vp], _i32),
     "ra_check": ([_vp], _i32),
     "ra_strerror": ([_i32], _c.c_char_p),
     "ra_tile_config": ([_c.POINTER(_i32), _c.POINTER(_i32)], _i32),
@@ -94,6 +96,14 @@ def ra_fold_log(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, 
                 max_entries, stream):
     return lib().ra_fold_log(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, log,
                              counts, max_entries, stream)
+
+
+def ra_forward_noalloc(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, stream):
+    """ra_forward for callers that must not allocate device memory (bf16,
+    tensor-core shapes only; scratch in a static device array shared by all
+    calls, so calls that overlap on the GPU race)."""
+    return lib().ra_forward_noalloc(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
+                                    scale, stream)
 
 
 def ra_check(stream):

@@ -35,6 +35,8 @@ struct FoldLog {
 int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, unsigned int* work,
               int sm_count, cudaStream_t stream);
 bool tc_supported(const FwdProblem& p);
+// Device address of the current device's status word (read by ra_check).
+int device_status_word(unsigned int** status);
 int launch_simt(const FwdProblem& p, unsigned int* status, cudaStream_t stream);
 int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
                  int D, int dtype, cudaStream_t stream);

@@ -111,6 +111,8 @@ ra::FwdProblem make_problem(const void* q, const void* k, const void* v, void* o
 
 }  // namespace
 
+int ra::device_status_word(unsigned int** status) { return device_state(status, nullptr); }
+
 extern "C" {
 
 int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,

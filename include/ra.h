@@ -178,6 +178,34 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
  */
 int ra_check(void* stream);
 
+/*
+ * ra_forward_noalloc: ra_forward for callers that cannot allocate device
+ * memory.  The pages describe nothing like it; it exists because some
+ * programs must not call cudaMalloc while they run attention: a server that
+ * reserved all device memory for its own pool at start-up, a framework whose
+ * caching allocator owns the GPU, or latency-critical code that cannot take
+ * cudaMalloc's device-wide synchronisation or its out-of-memory failure.
+ * ra_forward allocates a 4 KiB scratch block on its first tensor-core call on
+ * a device; this entry point allocates nothing.  Its scratch, the kernel's
+ * work-queue counter, lives in a 256-byte static __device__ array that every
+ * device loading the library holds until the process exits.
+ *   Arguments, layouts and results are those of ra_forward with
+ *   dtype = RA_BF16; only the tensor-core kernel's shapes are accepted
+ *   (D in {64, 128}, S/N a multiple of 128).
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call outside CUDA-graph stream
+ *   capture.  Each call zeroes the counter on `stream` before its kernel.
+ *   All calls share the one array: calls whose kernels may overlap on the GPU
+ *   (different streams without ordering between them) race on it.  Order
+ *   them on one stream or with events.
+ * Errors: as ra_forward; RA_ERR_UNSUPPORTED outside the tensor-core shapes;
+ * RA_ERR_CAPACITY when the scratch the call needs exceeds the array (one
+ * 32-bit counter, so at most 2^31 work items).
+ */
+int ra_forward_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                       int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped,
+                       float scale, void* stream);
+
 /* Human-readable text for a status code (static storage). */
 const char* ra_strerror(int code);
 
