@@ -48,6 +48,10 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default="forward", choices=["forward", "merge", "stripe", "f32"],
+                    help="forward: the ring-attention step (default); merge / stripe: the "
+                         "HBM-bound helpers on the workload's output / query tensors; f32: the "
+                         "fp32 SIMT path on the workload")
     return ap.parse_args()
 
 
@@ -233,6 +237,90 @@ def reference_arm(args, wl):
     return 0
 
 
+
+# ---------------------------------------------------------------- helper kernels
+def aux_arm(args, wl):
+    """Times ra_merge / ra_stripe (HBM-bound) or the fp32 SIMT forward."""
+    import torch
+    import exact_long_context_order_b300 as ra
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    ra.lib()
+    stream = torch.cuda.current_stream()
+    qs, _ = wl.shapes()
+    rows = qs[0] * qs[1] * qs[2]
+    D = qs[3]
+    peaks, peak_src = load_peaks()
+    gen = torch.Generator(device="cuda").manual_seed(wl.seed)
+    if args.op == "merge":
+        oa = torch.randn((rows, D), device="cuda", generator=gen).to(torch.bfloat16)
+        ob = torch.randn((rows, D), device="cuda", generator=gen).to(torch.bfloat16)
+        la = torch.randn((rows,), device="cuda", generator=gen)
+        lb = torch.randn((rows,), device="cuda", generator=gen)
+        bytes_per = rows * (3 * D * 2 + 3 * 4)  # read a, b, lse_a, lse_b; write a, lse_a
+
+        def step():
+            ra.merge(oa, la, ob, lb, stream=stream)
+        name, bound_unit = "ra::aux::merge_kernel<bf16>", "GB/s"
+    elif args.op == "stripe":
+        x = torch.randn(qs, device="cuda", generator=gen).to(torch.bfloat16)
+        y = torch.empty_like(x)
+        bytes_per = 2 * x.numel() * 2
+
+        def step():
+            ra.stripe(x, wl.N, out=y, stream=stream)
+        name, bound_unit = "ra::aux::stripe_kernel<uint4>", "GB/s"
+    else:
+        import ragen
+        # the fp32 path runs the fp32 workload unless another one was asked for
+        toy = ragen.WORKLOADS["toy_f32"] if args.workload == "gqa_128k" else wl
+        qs2, kvs2 = toy.shapes()
+        q = torch.randn(qs2, device="cuda", generator=gen)
+        k = torch.randn(kvs2, device="cuda", generator=gen)
+        v = torch.randn(kvs2, device="cuda", generator=gen)
+        out = torch.empty_like(q)
+        lse = torch.empty(qs2[:3], device="cuda")
+        bytes_per = None
+        flops = toy.flops()
+
+        def step():
+            ra.forward(q, k, v, toy.N, causal=toy.causal, striped=toy.striped, out=out, lse=lse,
+                       stream=stream)
+        name, bound_unit = "ra::simt::fwd_kernel<float>", "GFLOP/s"
+        wl = toy
+    for _ in range(args.warmup):
+        step()
+    ra.check(stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    if bytes_per is not None:
+        value = bytes_per / (ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": value, "peak": peak, "unit": "GB/s",
+                "frac": value / peak, "traffic": None, "kernel": name,
+                "peak_source": f"{peak_src} hbm_gbs"}
+        metric = f"{args.op} HBM throughput (GB/s) on {wl.name} tensors"
+    else:
+        value = flops / (ms * 1e-3) / 1e9
+        roof = {"bound": "alu", "achieved": value, "peak": None, "unit": "GFLOP/s", "frac": None,
+                "traffic": None, "kernel": name}
+        metric = f"fp32 SIMT forward GFLOP/s on {wl.name}"
+    line = {"metric": metric, "value": value, "unit": bound_unit, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.op != "f32" else "f32", "data": "synthetic",
+            "config": dict(wl.describe(), op=args.op), "gpu_launches": args.steps,
+            "roofline": roof}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
 # ---------------------------------------------------------------- our arm
 def main():
     args = parse()
@@ -240,6 +328,8 @@ def main():
     wl = ragen.WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, wl)
+    if args.op != "forward":
+        return aux_arm(args, wl)
 
     import torch
     import torch.distributed as dist

@@ -7,7 +7,9 @@
 //  * stripe -- bit-exact row permutation between token order and the striped
 //              shard-major order, token t <-> row (t mod N)*Sb + t div N
 //              (glossary page, Striped Attention).
-// Both are one warp per row, 16-byte vector accesses where the row allows.
+// Rows of 2..32 16-byte vectors use the row-group kernels (several rows per
+// warp, every lane moving 16 bytes, loads batched ahead of stores); other
+// shapes fall back to one warp per row.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -121,6 +123,90 @@ __global__ void __launch_bounds__(kBlock) stripe_kernel(const V* __restrict__ sr
     }
 }
 
+// Row-group variants: a row of VPR 16-byte vectors (VPR a power of two <= 32)
+// is handled by VPR consecutive lanes, so a warp covers 32/VPR rows at once
+// and every lane moves 16 bytes; UNROLL batches are loaded before any store
+// to keep enough bytes in flight for HBM.
+template <typename T, int VPR, int UNROLL>
+__global__ void __launch_bounds__(kBlock) merge_rows_kernel(T* __restrict__ oa, float* __restrict__ la,
+                                                           const T* __restrict__ ob,
+                                                           const float* __restrict__ lb,
+                                                           int64_t rows) {
+    constexpr int RPW = 32 / VPR;  // rows per warp per batch
+    const int lane = threadIdx.x & 31, sub = lane / VPR, v = lane % VPR;
+    const int64_t warp_id = ((int64_t)blockIdx.x * kBlock + threadIdx.x) / 32;
+    const int64_t n_warps = (int64_t)gridDim.x * (kBlock / 32);
+    uint4* va = reinterpret_cast<uint4*>(oa);
+    const uint4* vb = reinterpret_cast<const uint4*>(ob);
+    for (int64_t r0 = warp_id * RPW * UNROLL; r0 < rows; r0 += n_warps * RPW * UNROLL) {
+        uint4 xa[UNROLL], xb[UNROLL];
+        float ca[UNROLL], cb[UNROLL], ls[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t row = r0 + u * RPW + sub;
+            if (row < rows) {
+                xa[u] = va[row * VPR + v];
+                xb[u] = __ldg(vb + row * VPR + v);
+                const float a = la[row], b = __ldg(lb + row);
+                const float mx = fmaxf(a, b);
+                ca[u] = cb[u] = 0.f;
+                ls[u] = -INFINITY;
+                if (mx != -INFINITY) {
+                    const float wa = expf(a - mx), wb = expf(b - mx), tot = wa + wb;
+                    ls[u] = mx + logf(tot);
+                    ca[u] = wa / tot;
+                    cb[u] = wb / tot;
+                }
+            }
+        }
+        __syncwarp();  // every lane has read la[] before lane 0 of a row rewrites it
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t row = r0 + u * RPW + sub;
+            if (row < rows) {
+                Vec<T>::fma2(xa[u], xb[u], ca[u], cb[u]);
+                va[row * VPR + v] = xa[u];
+                if (v == 0) la[row] = ls[u];  // every lane of this row read la[row] above
+            }
+        }
+    }
+}
+
+template <int VPR, int UNROLL>
+__global__ void __launch_bounds__(kBlock) stripe_rows_kernel(const uint4* __restrict__ src,
+                                                            uint4* __restrict__ dst, int64_t BH,
+                                                            int64_t S, int64_t N, int inverse) {
+    constexpr int RPW = 32 / VPR;
+    const int lane = threadIdx.x & 31, sub = lane / VPR, v = lane % VPR;
+    const int64_t Sb = S / N, total = BH * S;
+    const int64_t warp_id = ((int64_t)blockIdx.x * kBlock + threadIdx.x) / 32;
+    const int64_t n_warps = (int64_t)gridDim.x * (kBlock / 32);
+    for (int64_t r0 = warp_id * RPW * UNROLL; r0 < total; r0 += n_warps * RPW * UNROLL) {
+        uint4 x[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t wr = r0 + u * RPW + sub;
+            if (wr < total) {
+                const int64_t bh = wr / S, p = wr % S;
+                int64_t sp;
+                if (!inverse) {
+                    const int64_t i = p / Sb, r = p % Sb;
+                    sp = r * N + i;
+                } else {
+                    const int64_t i = p % N, r = p / N;
+                    sp = i * Sb + r;
+                }
+                x[u] = __ldg(src + (bh * S + sp) * VPR + v);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t wr = r0 + u * RPW + sub;
+            if (wr < total) dst[wr * VPR + v] = x[u];
+        }
+    }
+}
+
 static unsigned grid_for(int64_t rows) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -135,7 +221,14 @@ int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_
                  int D, int dtype, cudaStream_t stream) {
     if (rows == 0) return RA_OK;
     const unsigned grid = aux::grid_for(rows);
-    if (dtype == RA_BF16) {
+    if (dtype == RA_BF16 && (D == 64 || D == 128 || D == 256)) {
+        auto* a = static_cast<__nv_bfloat16*>(out_a);
+        auto* b = static_cast<const __nv_bfloat16*>(out_b);
+        const unsigned g = aux::grid_for(rows / 8 + 1);
+        if (D == 64) aux::merge_rows_kernel<__nv_bfloat16, 8, 4><<<g, aux::kBlock, 0, stream>>>(a, lse_a, b, lse_b, rows);
+        else if (D == 128) aux::merge_rows_kernel<__nv_bfloat16, 16, 4><<<g, aux::kBlock, 0, stream>>>(a, lse_a, b, lse_b, rows);
+        else aux::merge_rows_kernel<__nv_bfloat16, 32, 4><<<g, aux::kBlock, 0, stream>>>(a, lse_a, b, lse_b, rows);
+    } else if (dtype == RA_BF16) {
         auto* a = static_cast<__nv_bfloat16*>(out_a);
         auto* b = static_cast<const __nv_bfloat16*>(out_b);
         if (D % 8 == 0)
@@ -158,7 +251,19 @@ int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int6
     const int64_t rows = BH * S;
     if (rows == 0) return RA_OK;
     const unsigned grid = aux::grid_for(rows);
-    if (row_bytes % 16 == 0)
+    const int64_t vpr = row_bytes / 16;
+    if (row_bytes % 16 == 0 && (vpr == 2 || vpr == 4 || vpr == 8 || vpr == 16 || vpr == 32)) {
+        const unsigned g = aux::grid_for(rows / 8 + 1);
+        auto* sp = static_cast<const uint4*>(src);
+        auto* dp = static_cast<uint4*>(dst);
+        switch (vpr) {
+            case 2: aux::stripe_rows_kernel<2, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
+            case 4: aux::stripe_rows_kernel<4, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
+            case 8: aux::stripe_rows_kernel<8, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
+            case 16: aux::stripe_rows_kernel<16, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
+            default: aux::stripe_rows_kernel<32, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
+        }
+    } else if (row_bytes % 16 == 0)
         aux::stripe_kernel<uint4><<<grid, aux::kBlock, 0, stream>>>(
             static_cast<const uint4*>(src), static_cast<uint4*>(dst), BH, S, N, row_bytes / 16, inverse);
     else
