@@ -62,6 +62,26 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """Largest timed duration over all ranks (no-op without a process group).
+
+    Replicas run independently; this reduction and the barriers around the
+    timed region are the only cross-rank communication of the bench."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(world: int, work_per_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job rate: the work of all replicas over the slowest rank's time
+    (work units per second)."""
+    return world * work_per_step * steps / (max_ms * 1e-3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -399,13 +419,9 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     per_launch_ms = [a.elapsed_time(b) for a, b in ev]
     launch_avg_ms = float(np.mean(per_launch_ms))
-    t_max = total_ms
-    if world > 1:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-    value = world * flops * args.steps / (t_max * 1e-3) / 1e12
-    tok_s = world * tokens * args.steps / (t_max * 1e-3)
+    t_max = max_over_ranks(total_ms, device="cuda")
+    value = aggregate_rate(world, flops, args.steps, t_max) / 1e12
+    tok_s = aggregate_rate(world, tokens, args.steps, t_max)
 
     # ------------------------------------------------ end to end: host buffers through the C ABI
     e2e = None
@@ -444,12 +460,8 @@ def main():
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            tt = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": world * flops * args.steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = max_over_ranks(a.elapsed_time(b), device="cuda")
+        e2e = {"value": aggregate_rate(world, flops, args.steps, e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms / args.steps}
         # the e2e outputs must equal the device-resident run (same inputs)
