@@ -37,6 +37,8 @@ _SIGNATURES = {
                      _f32, _vp, _vp, _i32, _vp], _i32),
     "ra_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
                             _i32, _f32, _vp], _i32),
+    "ra_watchdog_selftest": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
+                              _i32, _f32, _i64, _vp], _i32),
     "ra_check": ([_vp], _i32),
     "ra_strerror": ([_i32], _c.c_char_p),
     "ra_tile_config": ([_c.POINTER(_i32), _c.POINTER(_i32)], _i32),
@@ -104,6 +106,12 @@ def ra_forward_noalloc(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, 
     calls, so calls that overlap on the GPU race)."""
     return lib().ra_forward_noalloc(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
                                     scale, stream)
+
+
+def ra_watchdog_selftest(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale,
+                         timeout_cycles, stream):
+    return lib().ra_watchdog_selftest(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
+                                      scale, timeout_cycles, stream)
 
 
 def ra_check(stream):

@@ -31,9 +31,13 @@ struct FoldLog {
 // Returns 0 on success or an RA_ERR_* code.  status: device pointer to this
 // device's status word.  sm_count: multiprocessors of the current device.
 // work: device counter the kernel takes work items from; zeroed by launch_tc
-// on `stream` before the launch.
+// on `stream` before the launch.  timeout_cycles (<= 0: the default of 4e9
+// SM cycles) bounds every wait of the kernel; withhold_first_k = 1 is the
+// failure-detection self test (each CTA's first K-tile copy is never issued,
+// so its waits run out and the kernel reports kStatusTimeout).
 int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, unsigned int* work,
-              int sm_count, cudaStream_t stream);
+              int sm_count, cudaStream_t stream, long long timeout_cycles = 0,
+              int withhold_first_k = 0);
 bool tc_supported(const FwdProblem& p);
 // Device address of the current device's status word (read by ra_check).
 int device_status_word(unsigned int** status);

@@ -168,6 +168,26 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
     return rc;
 }
 
+int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out, float* lse,
+                         int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped,
+                         float scale, int64_t timeout_cycles, void* stream) {
+    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16);
+    if (rc) return rc;
+    if (timeout_cycles < 100000 || timeout_cycles > 4000000000ll) return RA_ERR_INVALID_ARG;
+    const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
+                                          scale, RA_BF16);
+    if (!ra::tc_supported(p)) return RA_ERR_UNSUPPORTED;
+    unsigned int* status = nullptr;
+    int sms = 0;
+    if ((rc = device_state(&status, &sms))) return rc;
+    unsigned int* work = nullptr;
+    if ((rc = work_slot(&work))) return rc;
+    rc = ra::launch_tc(p, nullptr, status, work, sms, static_cast<cudaStream_t>(stream),
+                       timeout_cycles, 1);
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
 int ra_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
              int D, int dtype, void* stream) {
     if (rows < 0 || D <= 0 || D > 1024) return RA_ERR_INVALID_ARG;

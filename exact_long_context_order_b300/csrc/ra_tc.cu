@@ -92,17 +92,18 @@ struct Params {
     int32_t* counts;
     int max_entries;
     unsigned int* work;  // item counter, zero at launch: CTAs take items in order
+    long long timeout_cycles;  // self test only: limit of every bounded wait
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int* status) {
+                                         unsigned int* status, long long limit) {
     if (mbar_try_wait(b, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(b, parity)) return true;
         if ((it & 255u) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kTimeoutCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 atomicOr(status, kStatusTimeout);
                 return false;
@@ -118,7 +119,7 @@ __device__ __forceinline__ void drain_wait(uint32_t b, uint32_t parity) {
     }
 }
 
-template <int D, bool LOG>
+template <int D, bool LOG, bool SELFTEST>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -135,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const ItemGeom& G = p.G;
+    // limit of every bounded wait (the failure-detection self test uses a short one)
+    const long long wlim = SELFTEST ? p.timeout_cycles : kTimeoutCycles;
 
     if (tid == 0) {
         mbar_init(bar(C::bQFull), 1);
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // publishes it in a two-entry shared ring; every role reads it from there.
     // An index >= n_items ends the CTA's loop.
     auto read_item = [&](int k, bool& ok) -> long long {
-        ok = wait_bar(bar(C::bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status);
+        ok = wait_bar(bar(C::bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, wlim);
         return ok ? item_slot[k & 1] : G.n_items;
     };
     if (warp < 4) regs_dec<kRegsOther>();
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             auto publish = [&](int kk, long long v) -> bool {
                 if (kk >= 2 && !wait_bar(bar(C::bItemEmpty + (kk & 1)), ((kk >> 1) - 1) & 1,
-                                         abort_flag, p.status))
+                                         abort_flag, p.status, wlim))
                     return false;
                 item_slot[kk & 1] = v;
                 mbar_arrive(bar(C::bItemFull + (kk & 1)));
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = publish(k + 1, next))) break;
                 const Item it = decode_item(G, item);
                 item = next;
-                if (k > 0 && !(ok = wait_bar(bar(C::bQEmpty), (k - 1) & 1, abort_flag, p.status)))
+                if (k > 0 && !(ok = wait_bar(bar(C::bQEmpty), (k - 1) & 1, abort_flag, p.status, wlim)))
                     break;
                 mbar_arrive_expect_tx(bar(C::bQFull), 2 * C::kTileBytes);
                 ++q_loads;
@@ -221,9 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (w.start(G.rg, it); !w.done(G.rg) && ok; w.next(G.rg, it)) {
                     const int row = (int)(kvrow0 + (int64_t)w.j * p.Sb + (int64_t)w.kt * kT);
                     for (int kv = 0; kv < 2; ++kv) {
+                        if (SELFTEST && kv_pos == 0) {  // self test: nothing ever signals stage 0
+                            ++kv_pos;
+                            continue;
+                        }
                         const uint32_t st = kv_pos % C::kStages, use = kv_pos / C::kStages;
                         if (use > 0 && !(ok = wait_bar(bar(C::bKVEmpty + st), (use - 1) & 1,
-                                                       abort_flag, p.status)))
+                                                       abort_flag, p.status, wlim)))
                             break;
                         mbar_arrive_expect_tx(bar(C::bKVFull + st), C::kTileBytes);
                         const CUtensorMap* tm = kv ? &tm_v : &tm_k;
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // caller has already waited for the first half.
             auto issue_pv = [&](uint32_t stV, bool acc, uint32_t g) -> bool {
                 issue_pv_half(stV, 0, acc);
-                if (!wait_bar(bar(C::bPHi + t), g & 1, abort_flag, p.status)) return false;
+                if (!wait_bar(bar(C::bPHi + t), g & 1, abort_flag, p.status, wlim)) return false;
                 tc_fence_after();
                 issue_pv_half(stV, 1, acc);
                 return true;
@@ -290,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // slot 1 issues block b after slot 0's block b
             uint32_t bc = 0;
             auto take_turn = [&]() -> bool {
-                if (t == 0) return bc == 0 || wait_bar(bar(C::bToken + 0), (bc - 1) & 1, abort_flag, p.status);
-                return wait_bar(bar(C::bToken + 1), bc & 1, abort_flag, p.status);
+                if (t == 0) return bc == 0 || wait_bar(bar(C::bToken + 0), (bc - 1) & 1, abort_flag, p.status, wlim);
+                return wait_bar(bar(C::bToken + 1), bc & 1, abort_flag, p.status, wlim);
             };
             auto pass_turn = [&]() {
                 mbar_arrive(bar(C::bToken + (t == 0 ? 1 : 0)));
@@ -305,27 +312,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) mbar_arrive(bar(C::bItemEmpty + (k & 1)));
                 if (!ok || item >= G.n_items) break;
                 const Item it = decode_item(G, item);
-                if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status))) break;
+                if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status, wlim))) break;
                 TileWalk w;
                 uint32_t n = 0;
                 for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n) {
                     const uint32_t stK = kv_pos % C::kStages;
                     if (!(ok = wait_bar(bar(C::bKVFull + stK), (kv_pos / C::kStages) & 1,
-                                        abort_flag, p.status)))
+                                        abort_flag, p.status, wlim)))
                         break;
                     uint32_t stV = 0;
                     if (n > 0) {
                         const uint32_t vp = kv_pos - 1;
                         stV = vp % C::kStages;
                         if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1,
-                                            abort_flag, p.status)))
+                                            abort_flag, p.status, wlim)))
                             break;
                         if (!(ok = wait_bar(bar(C::bPLo + t), (gt - 1) & 1, abort_flag,
-                                            p.status)))
+                                            p.status, wlim)))
                             break;
                         if (n == 1 && k > 0 &&
                             !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag,
-                                            p.status)))
+                                            p.status, wlim)))
                             break;
                     }
                     if (!(ok = take_turn())) break;
@@ -345,12 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(bar(C::bQEmpty));  // every S MMA of this slot and item is issued
                 const uint32_t vp = kv_pos - 1, stV = vp % C::kStages;
                 if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1, abort_flag,
-                                    p.status)))
+                                    p.status, wlim)))
                     break;
-                if (!(ok = wait_bar(bar(C::bPLo + t), (gt - 1) & 1, abort_flag, p.status)))
+                if (!(ok = wait_bar(bar(C::bPLo + t), (gt - 1) & 1, abort_flag, p.status, wlim)))
                     break;
                 if (n == 1 && k > 0 &&
-                    !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag, p.status)))
+                    !(ok = wait_bar(bar(C::bOEmpty + t), (k - 1) & 1, abort_flag, p.status, wlim)))
                     break;
                 if (!(ok = take_turn())) break;
                 tc_fence_after();
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t n = 0;
             for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n, ++gt) {
                 const int kind = fold_kind(G.rg, it.i, w.j, qt, w.kt);
-                ok = wait_bar(bar(C::bSFull + t), gt & 1, abort_flag, p.status);
+                ok = wait_bar(bar(C::bSFull + t), gt & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 if (kind == kNone) {
@@ -524,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
-            ok = wait_bar(bar(C::bOFull + t), k & 1, abort_flag, p.status);
+            ok = wait_bar(bar(C::bOFull + t), k & 1, abort_flag, p.status, wlim);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             if (valid) {
@@ -608,7 +615,8 @@ static bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int D) {
 
 template <int D, bool LOG>
 static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* status,
-                       unsigned int* work, int sm_count, cudaStream_t stream) {
+                       unsigned int* work, int sm_count, cudaStream_t stream,
+                       long long timeout_cycles, int withhold_first_k) {
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv;
     const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
@@ -628,9 +636,10 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     P.counts = flog ? flog->counts : nullptr;
     P.max_entries = flog ? flog->max_entries : 0;
     P.work = work;
+    P.timeout_cycles = timeout_cycles > 0 ? timeout_cycles : kTimeoutCycles;
     if (P.G.n_items <= 0) return RA_OK;
     if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
-    auto kern = fwd_kernel<D, LOG>;
+    auto kern = withhold_first_k ? fwd_kernel<D, false, true> : fwd_kernel<D, LOG, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return RA_ERR_CUDA;
@@ -652,14 +661,18 @@ bool tc_supported(const FwdProblem& p) {
 }
 
 int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, unsigned int* work,
-              int sm_count, cudaStream_t stream) {
+              int sm_count, cudaStream_t stream, long long timeout_cycles, int withhold_first_k) {
     if (!tc_supported(p)) return RA_ERR_UNSUPPORTED;
     if (!work) return RA_ERR_INVALID_ARG;
     if (p.D == 128)
-        return flog ? tc::launch_impl<128, true>(p, flog, status, work, sm_count, stream)
-                    : tc::launch_impl<128, false>(p, flog, status, work, sm_count, stream);
-    return flog ? tc::launch_impl<64, true>(p, flog, status, work, sm_count, stream)
-                : tc::launch_impl<64, false>(p, flog, status, work, sm_count, stream);
+        return flog ? tc::launch_impl<128, true>(p, flog, status, work, sm_count, stream,
+                                                 timeout_cycles, withhold_first_k)
+                    : tc::launch_impl<128, false>(p, flog, status, work, sm_count, stream,
+                                                  timeout_cycles, withhold_first_k);
+    return flog ? tc::launch_impl<64, true>(p, flog, status, work, sm_count, stream,
+                                            timeout_cycles, withhold_first_k)
+                : tc::launch_impl<64, false>(p, flog, status, work, sm_count, stream,
+                                             timeout_cycles, withhold_first_k);
 }
 
 }  // namespace ra

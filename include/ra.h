@@ -171,6 +171,23 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
                 int32_t* log, int32_t* counts, int max_entries, void* stream);
 
 /*
+ * ra_watchdog_selftest: failure-detection self test of the tensor-core
+ * kernel.  It launches the kernel on the caller's problem (same arguments as
+ * ra_forward, bf16, tensor-core shapes) with every wait bounded by
+ * timeout_cycles SM clock cycles (1e5 .. 4e9) and with each CTA's first K-tile
+ * copy never issued, so the waits that depend on it run out.  The kernel then
+ * records RA_ERR_TIMEOUT in the device status word, lets its copies and MMAs
+ * in flight finish, frees its tensor memory and returns; nothing faults or
+ * hangs and the CUDA context stays usable.  out and lse are left undefined.
+ * Returns RA_OK once the launch is enqueued; ra_check(stream) then reports
+ * RA_ERR_TIMEOUT.  (Normal launches bound every wait at 4e9 cycles.)
+ * Errors: as ra_forward; RA_ERR_INVALID_ARG for timeout_cycles out of range.
+ */
+int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out, float* lse,
+                         int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped,
+                         float scale, int64_t timeout_cycles, void* stream);
+
+/*
  * ra_check: synchronise `stream`, then read and clear this device's status
  * word.  Returns RA_OK, RA_ERR_TIMEOUT, RA_ERR_BOUNDS or RA_ERR_CUDA (the
  * synchronisation itself failed; the CUDA error string is kept for

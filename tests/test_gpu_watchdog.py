@@ -1,0 +1,57 @@
+"""Failure detection on the GPU without a fault: the tensor-core kernel's
+bounded waits.  ra_watchdog_selftest withholds each CTA's first K-tile copy,
+so the waits that need it run out after a short limit; the kernel must
+report RA_ERR_TIMEOUT through ra_check, return promptly, and leave the
+context usable -- a normal forward right after it must still match the
+oracle."""
+import time
+
+import numpy as np
+import pytest
+
+from helpers import assert_close, from_device, inputs, reference, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ra(cuda_ok):
+    import exact_long_context_order_b300 as m
+    from exact_long_context_order_b300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+def test_withheld_copy_times_out_and_context_stays_usable(ra):
+    import torch
+    B, Hq, Hkv, S, N, D = 1, 2, 1, 512, 2, 128
+    q, k, v = inputs(31, B, Hq, Hkv, S, D, "bf16")
+    tq, tk, tv = (to_device(x, "bf16") for x in (q, k, v))
+    out = torch.empty_like(tq)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    stream = ra._stream_handle(None)
+    assert ra.ra_check(stream) == ra.RA_OK  # clean start
+
+    t0 = time.time()
+    rc = ra.ra_watchdog_selftest(ra._ptr(tq), ra._ptr(tk), ra._ptr(tv), ra._ptr(out),
+                                 ra._ptr(lse), B, Hq, Hkv, S, D, N, 1, 1, 0.0, 20_000_000, stream)
+    assert rc == ra.RA_OK, ra.ra_strerror(rc)
+    assert ra.ra_check(stream) == ra.RA_ERR_TIMEOUT
+    assert time.time() - t0 < 30.0
+    assert ra.ra_check(stream) == ra.RA_OK  # the status word was cleared
+
+    # the context still works: a normal forward is correct
+    out2, lse2 = ra.forward(tq, tk, tv, N, causal=True, striped=True)
+    ra.check()
+    ro, rl = reference(q, k, v, N, True, True, "bf16")
+    assert_close(from_device(out2), from_device(lse2), ro, rl, "bf16", "after the self test")
+
+
+def test_selftest_argument_checks(ra):
+    import ctypes
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: rejected on the host
+    assert ra.ra_watchdog_selftest(p, p, p, p, None, 1, 1, 1, 256, 128, 2, 1, 0, 0.0, 10,
+                                   None) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_watchdog_selftest(p, p, p, p, None, 1, 1, 1, 256, 96, 2, 1, 0, 0.0,
+                                   1_000_000, None) == ra.RA_ERR_UNSUPPORTED
