@@ -22,6 +22,7 @@ RA_ERR_CUDA, RA_ERR_TIMEOUT, RA_ERR_BOUNDS, RA_ERR_CAPACITY = 4, 5, 6, 7
 RA_BF16, RA_F32 = 0, 1
 RA_KERNEL_AUTO, RA_KERNEL_TC, RA_KERNEL_SIMT = 0, 1, 2
 RA_FOLD_FULL, RA_FOLD_INCL, RA_FOLD_STRICT = 0, 1, 2
+RA_LAYOUT_CONTIGUOUS, RA_LAYOUT_STRIPED, RA_LAYOUT_ZIGZAG = 0, 1, 2
 
 _c = ctypes
 _vp, _i32, _i64, _f32 = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_float
@@ -32,6 +33,7 @@ _SIGNATURES = {
                        _f32, _i32, _i32, _vp], _i32),
     "ra_merge": ([_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp], _i32),
     "ra_stripe": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _vp], _i32),
+    "ra_relayout": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _i32, _vp], _i32),
     "ra_plan": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)], _i32),
     "ra_fold_log": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
                      _f32, _vp, _vp, _i32, _vp], _i32),
@@ -88,6 +90,10 @@ def ra_merge(out_a, lse_a, out_b, lse_b, rows, D, dtype, stream):
 
 def ra_stripe(src, dst, BH, S, N, row_bytes, inverse, stream):
     return lib().ra_stripe(src, dst, BH, S, N, row_bytes, inverse, stream)
+
+
+def ra_relayout(src, dst, BH, S, N, row_bytes, layout, inverse, stream):
+    return lib().ra_relayout(src, dst, BH, S, N, row_bytes, layout, inverse, stream)
 
 
 def ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items):
@@ -156,7 +162,8 @@ def forward(q, k, v, N: int, causal: bool = False, striped: bool = False, scale=
     """Ring attention over shard-major torch CUDA tensors.
 
     q [B, Hq, S, D], k and v [B, Hkv, S, D], all bf16 or all float32,
-    contiguous, on the current device.  Returns (out, lse): out like q, lse
+    contiguous, on the current device.  ``striped`` is the layout: False/0
+    contiguous, True/1 striped, 2 zigzag.  Returns (out, lse): out like q, lse
     [B, Hq, S] float32 (None when want_lse is False and lse is None).
     """
     import torch
@@ -230,6 +237,20 @@ def stripe(x, N: int, inverse: bool = False, out=None, stream=None):
         out = torch.empty_like(x)
     rc = ra_stripe(_ptr(x), _ptr(out), BH, S, N, row_bytes, int(inverse), _stream_handle(stream))
     _check(rc, "ra_stripe")
+    return out
+
+
+def relayout(x, N: int, layout: int, inverse: bool = False, out=None, stream=None):
+    """Token order <-> shard-major layout (RA_LAYOUT_*) along dim -2 of [..., S, D]."""
+    import torch
+    S = x.shape[-2]
+    row_bytes = x.shape[-1] * x.element_size()
+    BH = x.numel() // (S * x.shape[-1])
+    if out is None:
+        out = torch.empty_like(x)
+    rc = ra_relayout(_ptr(x), _ptr(out), BH, S, N, row_bytes, int(layout), int(inverse),
+                     _stream_handle(stream))
+    _check(rc, "ra_relayout")
     return out
 
 

@@ -17,7 +17,7 @@ struct FwdProblem {
     float* lse;
     int B, Hq, Hkv;
     int64_t S;
-    int D, N, causal, striped;
+    int D, N, causal, striped;  // striped: layout 0 contiguous, 1 striped, 2 zigzag
     float scale;  // resolved (> 0)
     int dtype;    // RA_BF16 / RA_F32
 };
@@ -44,7 +44,8 @@ int device_status_word(unsigned int** status);
 int launch_simt(const FwdProblem& p, unsigned int* status, cudaStream_t stream);
 int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
                  int D, int dtype, cudaStream_t stream);
+// layout: 1 striped, 2 zigzag (0 contiguous is the identity)
 int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
-                  int inverse, cudaStream_t stream);
+                  int layout, int inverse, cudaStream_t stream);
 
 }  // namespace ra

@@ -85,10 +85,12 @@ int work_slot(unsigned int** slot) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int validate_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B,
-                     int Hq, int Hkv, int64_t S, int D, int N, int dtype) {
+                     int Hq, int Hkv, int64_t S, int D, int N, int dtype, int layout) {
     if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
     if (S % N != 0 || Hq % Hkv != 0) return RA_ERR_INVALID_ARG;
+    if (layout < RA_LAYOUT_CONTIGUOUS || layout > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
+    if (layout == RA_LAYOUT_ZIGZAG && (S / N) % 2) return RA_ERR_INVALID_ARG;
     if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_INVALID_ARG;
     if (D > 256) return RA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_ALIGN;
@@ -103,7 +105,7 @@ ra::FwdProblem make_problem(const void* q, const void* k, const void* v, void* o
     p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.N = N;
     p.causal = causal ? 1 : 0;
-    p.striped = striped ? 1 : 0;
+    p.striped = striped;
     p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
     p.dtype = dtype;
     return p;
@@ -118,7 +120,7 @@ extern "C" {
 int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                   int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
                   int dtype, int kernel, void* stream) {
-    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, dtype);
+    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, dtype, striped);
     if (rc) return rc;
     if (kernel != RA_KERNEL_AUTO && kernel != RA_KERNEL_TC && kernel != RA_KERNEL_SIMT)
         return RA_ERR_INVALID_ARG;
@@ -150,7 +152,7 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
 int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
                 int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
                 int32_t* log, int32_t* counts, int max_entries, void* stream) {
-    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16);
+    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16, striped);
     if (rc) return rc;
     if (!log || !counts || !aligned16(log) || ((uintptr_t)counts & 3u)) return RA_ERR_INVALID_ARG;
     const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
@@ -171,7 +173,7 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
 int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out, float* lse,
                          int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped,
                          float scale, int64_t timeout_cycles, void* stream) {
-    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16);
+    int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16, striped);
     if (rc) return rc;
     if (timeout_cycles < 100000 || timeout_cycles > 4000000000ll) return RA_ERR_INVALID_ARG;
     const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
@@ -203,10 +205,12 @@ int ra_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, i
     return rc;
 }
 
-int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
-              int inverse, void* stream) {
+int ra_relayout(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
+                int layout, int inverse, void* stream) {
     if (BH < 0 || S < 0 || N <= 0 || row_bytes <= 0 || row_bytes % 4) return RA_ERR_INVALID_ARG;
     if (S % N) return RA_ERR_INVALID_ARG;
+    if (layout < RA_LAYOUT_CONTIGUOUS || layout > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
+    if (layout == RA_LAYOUT_ZIGZAG && (S / N) % 2) return RA_ERR_INVALID_ARG;
     if (BH == 0 || S == 0) return RA_OK;
     if (!src || !dst) return RA_ERR_INVALID_ARG;
     if (!aligned16(src) || !aligned16(dst)) return RA_ERR_ALIGN;
@@ -216,20 +220,27 @@ int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t 
     if (s < d + bytes && d < s + bytes) return RA_ERR_INVALID_ARG;  // overlap
     int rc = device_state(nullptr, nullptr);
     if (rc) return rc;
-    rc = ra::launch_stripe(src, dst, BH, S, N, row_bytes, inverse ? 1 : 0,
+    rc = ra::launch_stripe(src, dst, BH, S, N, row_bytes, layout, inverse ? 1 : 0,
                            static_cast<cudaStream_t>(stream));
     if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
     return rc;
 }
 
+int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
+              int inverse, void* stream) {
+    return ra_relayout(src, dst, BH, S, N, row_bytes, RA_LAYOUT_STRIPED, inverse, stream);
+}
+
 int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, int32_t* items,
             int64_t cap, int64_t* n_items) {
     if (!n_items || S <= 0 || N <= 0 || tile < 2 || S % N) return RA_ERR_INVALID_ARG;
+    if (striped < RA_LAYOUT_CONTIGUOUS || striped > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
     const int64_t Sb = S / N;
     if (Sb % tile) return RA_ERR_INVALID_ARG;
+    if (striped == RA_LAYOUT_ZIGZAG && (Sb / tile) % 2) return RA_ERR_INVALID_ARG;
     const int64_t nt = Sb / tile;
     if (nt > 0x7fffffff || i < 0 || i >= N || qt < 0 || qt >= nt) return RA_ERR_INVALID_ARG;
-    ra::RingGeom g{N, (int)nt, causal ? 1 : 0, striped ? 1 : 0};
+    ra::RingGeom g{N, (int)nt, causal ? 1 : 0, striped};
     int64_t n = 0;
     for (int s = 0; s < N; ++s) {
         const int j = ((i - s) % N + N) % N;

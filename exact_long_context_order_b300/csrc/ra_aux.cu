@@ -4,9 +4,12 @@
 //              rescale-and-add that the online softmax performs when a new
 //              block arrives (aiunderstanding.org, "Approfondimento
 //              tecnico"; glossary page, running-max remark).
-//  * stripe -- bit-exact row permutation between token order and the striped
-//              shard-major order, token t <-> row (t mod N)*Sb + t div N
-//              (glossary page, Striped Attention).
+//  * relayout -- bit-exact row permutation between token order and a
+//              shard-major layout: striped, token t <-> row (t mod N)*Sb +
+//              t div N (glossary page, Striped Attention), or zigzag, shard i
+//              holding chunks i and 2N-1-i of 2N chunks (the Zulu
+//              aiunderstanding.org page names the variant; this layout is the
+//              build's reading of it).
 // Rows of 2..32 16-byte vectors use the row-group kernels (several rows per
 // warp, every lane moving 16 bytes, loads batched ahead of stores); other
 // shapes fall back to one warp per row.
@@ -98,10 +101,35 @@ __global__ void __launch_bounds__(kBlock) merge_kernel(T* __restrict__ oa, float
     }
 }
 
+// Shard-major row of token t (layout 1 striped, 2 zigzag, else contiguous).
+__device__ __forceinline__ int64_t row_of_token(int64_t t, int64_t Sb, int64_t N, int layout) {
+    if (layout == 1) return (t % N) * Sb + t / N;
+    if (layout == 2) {
+        const int64_t h = Sb / 2, c = t / h, o = t % h;
+        return c < N ? c * Sb + o : (2 * N - 1 - c) * Sb + h + o;
+    }
+    return t;
+}
+// Token held by shard-major row p.
+__device__ __forceinline__ int64_t token_of_row(int64_t p, int64_t Sb, int64_t N, int layout) {
+    const int64_t i = p / Sb, r = p % Sb;
+    if (layout == 1) return r * N + i;
+    if (layout == 2) {
+        const int64_t h = Sb / 2;
+        return r < h ? i * h + r : (2 * N - 1 - i) * h + (r - h);
+    }
+    return p;
+}
+// Source row (within a slice) of destination row p.
+__device__ __forceinline__ int64_t src_row(int64_t p, int64_t Sb, int64_t N, int layout,
+                                           int inverse) {
+    return inverse ? row_of_token(p, Sb, N, layout) : token_of_row(p, Sb, N, layout);
+}
+
 template <typename V>
 __global__ void __launch_bounds__(kBlock) stripe_kernel(const V* __restrict__ src, V* __restrict__ dst,
                                                         int64_t BH, int64_t S, int64_t N,
-                                                        int64_t row_vecs, int inverse) {
+                                                        int64_t row_vecs, int layout, int inverse) {
     const int lane = threadIdx.x & 31;
     const int64_t Sb = S / N;
     const int64_t total = BH * S;
@@ -109,14 +137,7 @@ __global__ void __launch_bounds__(kBlock) stripe_kernel(const V* __restrict__ sr
     for (int64_t wr = (int64_t)blockIdx.x * (kBlock / 32) + threadIdx.x / 32; wr < total;
          wr += warps) {
         const int64_t bh = wr / S, p = wr % S;  // p: destination row within the slice
-        int64_t sp;
-        if (!inverse) {  // dst row p = i*Sb + r holds token r*N + i
-            const int64_t i = p / Sb, r = p % Sb;
-            sp = r * N + i;
-        } else {  // dst row p = token t = r*N + i comes from row i*Sb + r
-            const int64_t i = p % N, r = p / N;
-            sp = i * Sb + r;
-        }
+        const int64_t sp = src_row(p, Sb, N, layout, inverse);
         const V* s = src + (bh * S + sp) * row_vecs;
         V* d = dst + (bh * S + p) * row_vecs;
         for (int64_t e = lane; e < row_vecs; e += 32) d[e] = s[e];
@@ -175,7 +196,8 @@ __global__ void __launch_bounds__(kBlock) merge_rows_kernel(T* __restrict__ oa, 
 template <int VPR, int UNROLL>
 __global__ void __launch_bounds__(kBlock) stripe_rows_kernel(const uint4* __restrict__ src,
                                                             uint4* __restrict__ dst, int64_t BH,
-                                                            int64_t S, int64_t N, int inverse) {
+                                                            int64_t S, int64_t N, int layout,
+                                                            int inverse) {
     constexpr int RPW = 32 / VPR;
     const int lane = threadIdx.x & 31, sub = lane / VPR, v = lane % VPR;
     const int64_t Sb = S / N, total = BH * S;
@@ -188,14 +210,7 @@ __global__ void __launch_bounds__(kBlock) stripe_rows_kernel(const uint4* __rest
             const int64_t wr = r0 + u * RPW + sub;
             if (wr < total) {
                 const int64_t bh = wr / S, p = wr % S;
-                int64_t sp;
-                if (!inverse) {
-                    const int64_t i = p / Sb, r = p % Sb;
-                    sp = r * N + i;
-                } else {
-                    const int64_t i = p % N, r = p / N;
-                    sp = i * Sb + r;
-                }
+                const int64_t sp = src_row(p, Sb, N, layout, inverse);
                 x[u] = __ldg(src + (bh * S + sp) * VPR + v);
             }
         }
@@ -247,7 +262,7 @@ int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_
 }
 
 int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
-                  int inverse, cudaStream_t stream) {
+                  int layout, int inverse, cudaStream_t stream) {
     const int64_t rows = BH * S;
     if (rows == 0) return RA_OK;
     const unsigned grid = aux::grid_for(rows);
@@ -257,18 +272,18 @@ int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int6
         auto* sp = static_cast<const uint4*>(src);
         auto* dp = static_cast<uint4*>(dst);
         switch (vpr) {
-            case 2: aux::stripe_rows_kernel<2, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
-            case 4: aux::stripe_rows_kernel<4, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
-            case 8: aux::stripe_rows_kernel<8, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
-            case 16: aux::stripe_rows_kernel<16, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
-            default: aux::stripe_rows_kernel<32, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, inverse); break;
+            case 2: aux::stripe_rows_kernel<2, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, layout, inverse); break;
+            case 4: aux::stripe_rows_kernel<4, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, layout, inverse); break;
+            case 8: aux::stripe_rows_kernel<8, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, layout, inverse); break;
+            case 16: aux::stripe_rows_kernel<16, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, layout, inverse); break;
+            default: aux::stripe_rows_kernel<32, 4><<<g, aux::kBlock, 0, stream>>>(sp, dp, BH, S, N, layout, inverse); break;
         }
     } else if (row_bytes % 16 == 0)
         aux::stripe_kernel<uint4><<<grid, aux::kBlock, 0, stream>>>(
-            static_cast<const uint4*>(src), static_cast<uint4*>(dst), BH, S, N, row_bytes / 16, inverse);
+            static_cast<const uint4*>(src), static_cast<uint4*>(dst), BH, S, N, row_bytes / 16, layout, inverse);
     else
         aux::stripe_kernel<uint32_t><<<grid, aux::kBlock, 0, stream>>>(
-            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), BH, S, N, row_bytes / 4, inverse);
+            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), BH, S, N, row_bytes / 4, layout, inverse);
     return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 

@@ -54,6 +54,7 @@ extern "C" int ra_forward_noalloc(const void* q, const void* k, const void* v, v
     if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
     if (S % N != 0 || Hq % Hkv != 0) return RA_ERR_INVALID_ARG;
+    if (striped < RA_LAYOUT_CONTIGUOUS || striped > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
                           reinterpret_cast<uintptr_t>(lse);
@@ -63,7 +64,7 @@ extern "C" int ra_forward_noalloc(const void* q, const void* k, const void* v, v
     p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse;
     p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.N = N;
     p.causal = causal ? 1 : 0;
-    p.striped = striped ? 1 : 0;
+    p.striped = striped;
     p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
     p.dtype = RA_BF16;
     if (!ra::tc_supported(p)) return RA_ERR_UNSUPPORTED;

@@ -8,7 +8,8 @@
 // s = 0..N-1, key by key in ascending local order, and keeps a running max m,
 // normaliser l and numerator acc[D]; out = acc / l, lse = m + ln l.
 // Visibility comes from token positions (contiguous: row p is token p;
-// striped: row r of shard j is token r*N + j), so masking needs no tiles.
+// striped: row r of shard j is token r*N + j; zigzag: shard j holds chunk j,
+// then chunk 2N-1-j, of 2N chunks of Sb/2 tokens), so masking needs no tiles.
 // Key/value rows are staged through shared memory in chunks shared by the
 // 128 query rows of a block; chunks past the block's last visible key stop
 // the walk of that shard (keys of a shard are in ascending position).
@@ -27,10 +28,20 @@ namespace simt {
 constexpr int kRows = 128;
 
 struct Params {
-    int B, Hq, Hkv, g, N, D, causal, striped;
+    int B, Hq, Hkv, g, N, D, causal, striped;  // striped: layout 0/1/2
     int64_t S, Sb;
     float scale;
 };
+
+// token position of local row r of shard i
+__device__ __forceinline__ int64_t token_pos(const Params& p, int64_t i, int64_t r) {
+    if (p.striped == 1) return r * p.N + i;
+    if (p.striped == 2) {
+        const int64_t h = p.Sb / 2;
+        return r < h ? i * h + r : (2 * (int64_t)p.N - 1 - i) * h + (r - h);
+    }
+    return i * p.Sb + r;
+}
 
 __device__ __forceinline__ float load_f(const float* p) { return *p; }
 __device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -52,8 +63,8 @@ __global__ void __launch_bounds__(kRows) fwd_kernel(const T* __restrict__ q, con
     const bool active = r < p.Sb;
     const int64_t r_last = (r0 + kRows - 1 < p.Sb) ? r0 + kRows - 1 : p.Sb - 1;
     const int64_t N = p.N;
-    const int64_t qpos = p.striped ? r * N + i : i * p.Sb + r;
-    const int64_t qpos_last = p.striped ? r_last * N + i : i * p.Sb + r_last;
+    const int64_t qpos = token_pos(p, i, r);
+    const int64_t qpos_last = token_pos(p, i, r_last);
     const int D = p.D;
 
     float qr[DMAX], acc[DMAX];
@@ -70,7 +81,7 @@ __global__ void __launch_bounds__(kRows) fwd_kernel(const T* __restrict__ q, con
     for (int s = 0; s < p.N; ++s) {
         const int j = (int)((i - s + N) % N);
         for (int64_t c0 = 0; c0 < p.Sb; c0 += KC) {
-            const int64_t kpos0 = p.striped ? c0 * N + j : j * p.Sb + c0;
+            const int64_t kpos0 = token_pos(p, j, c0);
             if (p.causal && kpos0 > qpos_last) break;
             const int nk = (int)((p.Sb - c0 < KC) ? p.Sb - c0 : KC);
             __syncthreads();
@@ -89,7 +100,7 @@ __global__ void __launch_bounds__(kRows) fwd_kernel(const T* __restrict__ q, con
             if (!active) continue;
             for (int kr = 0; kr < nk; ++kr) {
                 const int64_t c = c0 + kr;
-                const int64_t kpos = p.striped ? c * N + j : j * p.Sb + c;
+                const int64_t kpos = token_pos(p, j, c);
                 if (p.causal && kpos > qpos) continue;
                 float sc = 0.f;
 #pragma unroll

@@ -655,6 +655,7 @@ bool tc_supported(const FwdProblem& p) {
     if (p.S % p.N) return false;
     const int64_t Sb = p.S / p.N;
     if (Sb % tc::kT) return false;
+    if (p.striped == kZigzag && (Sb / tc::kT) % 2) return false;  // chunk = whole tiles
     if ((int64_t)p.B * p.Hq * p.S >= (1ll << 31) || (int64_t)p.B * p.Hkv * p.S >= (1ll << 31))
         return false;
     return true;

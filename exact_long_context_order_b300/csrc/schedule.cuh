@@ -14,6 +14,14 @@
 //                         every j, kt < qt FULL and kt == qt INCL if j <= i,
 //                         STRICT (local key row < local query row) if j > i
 // since token r*N + i sees token c*N + j iff c < r, or c == r and j <= i.
+//   causal, zigzag        (2N chunks of Sb/2 tokens; shard i holds chunk i,
+//                         then chunk 2N-1-i; h = nt/2 tiles per chunk): a
+//                         query tile in the first half sees the first half of
+//                         shards j < i and its own chunk up to the diagonal;
+//                         one in the second half sees all of shards j > i,
+//                         the first half of shards j < i, and its own shard up
+//                         to the diagonal (INCL).  Live tiles are always a
+//                         prefix [0, nk) of shard j.
 #pragma once
 #include <cstdint>
 
@@ -24,12 +32,13 @@
 namespace ra {
 
 enum FoldKind : int { kFull = 0, kIncl = 1, kStrict = 2, kNone = 3 };
+enum Layout : int { kContiguous = 0, kStriped = 1, kZigzag = 2 };
 
 struct RingGeom {
     int N;        // virtual devices (shards)
     int nt;       // tiles per shard (Sb / tile)
     int causal;
-    int striped;
+    int striped;  // layout: kContiguous, kStriped or kZigzag
 };
 
 // Live key tiles of shard j for query tile qt of shard i: kt in [0, *nk); the
@@ -38,13 +47,19 @@ RA_HD void shard_span(const RingGeom& g, int i, int j, int qt, int* nk, int* dia
     if (!g.causal) {
         *nk = g.nt;
         *diag_kind = kNone;
-    } else if (!g.striped) {
+    } else if (g.striped == kContiguous) {
         if (j < i) { *nk = g.nt; *diag_kind = kNone; }
         else if (j == i) { *nk = qt + 1; *diag_kind = kIncl; }
         else { *nk = 0; *diag_kind = kNone; }
-    } else {
+    } else if (g.striped == kStriped) {
         *nk = qt + 1;
         *diag_kind = (j <= i) ? kIncl : kStrict;
+    } else {  // zigzag
+        const int h = g.nt / 2;
+        *diag_kind = kNone;
+        if (j == i) { *nk = qt + 1; *diag_kind = kIncl; }
+        else if (qt < h) *nk = (j < i) ? h : 0;
+        else *nk = (j > i) ? g.nt : h;
     }
 }
 
@@ -76,7 +91,7 @@ RA_HD ItemGeom make_item_geom(int B, int Hq, int Hkv, int N, int nt, int causal,
     G.rg.N = N; G.rg.nt = nt; G.rg.causal = causal; G.rg.striped = striped;
     G.B = B; G.Hq = Hq; G.Hkv = Hkv; G.g = Hq / Hkv;
     G.pair_heads = (G.g % 2 == 0) ? 1 : 0;
-    const bool contig_causal = causal && !striped;
+    const bool contig_causal = causal && striped == kContiguous;
     if (G.pair_heads) {
         int hp = G.g / 2;
         G.L = contig_causal ? N * nt : nt;
@@ -104,7 +119,7 @@ RA_HD Item decode_item(const ItemGeom& G, long long item) {
     it.b = (int)(grp / G.Hkv);
     it.kvh = (int)(grp % G.Hkv);
     const int N = G.rg.N, nt = G.rg.nt;
-    const bool contig_causal = G.rg.causal && !G.rg.striped;
+    const bool contig_causal = G.rg.causal && G.rg.striped == kContiguous;
     if (G.pair_heads) {
         int hp_count = G.g / 2, hp, qt;
         if (contig_causal) {

@@ -28,10 +28,17 @@
  *   such call on a device outside CUDA-graph stream capture.
  * - Layout is "shard-major": q and out are [B, Hq, S, D], k and v are
  *   [B, Hkv, S, D], lse is [B, Hq, S]; all row-major and contiguous.  Shard i
- *   owns rows [i*Sb, (i+1)*Sb) of every (b, h) slice, Sb = S / N.  With
- *   striped = 0 row p holds token p (contiguous sharding).  With striped = 1
- *   row r of shard i holds token r*N + i (token t lives on shard t mod N).
- *   ra_stripe converts between token order and the striped shard-major order.
+ *   owns rows [i*Sb, (i+1)*Sb) of every (b, h) slice, Sb = S / N.  The
+ *   argument `striped` selects which tokens a shard holds (RA_LAYOUT_*):
+ *     0 contiguous: row p holds token p;
+ *     1 striped:    row r of shard i holds token r*N + i (token t on shard
+ *                   t mod N; the glossary page's Striped Attention);
+ *     2 zigzag:     the sequence is cut into 2N chunks of Sb/2 tokens and
+ *                   shard i holds chunk i followed by chunk 2N-1-i (a
+ *                   variant the Zulu aiunderstanding.org page only names;
+ *                   this is the library's reading).  Needs Sb even.
+ *   ra_relayout (ra_stripe for the striped layout) converts between token
+ *   order and a shard-major layout.
  * - Query head h reads key/value head h / (Hq / Hkv) (grouped-query
  *   attention; Hq must be a multiple of Hkv).
  * - causal = 1 masks every key whose token position is after the query's
@@ -69,10 +76,13 @@ enum {
 
 enum { RA_BF16 = 0, RA_F32 = 1 };
 
+enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1, RA_LAYOUT_ZIGZAG = 2 };
+
 /* Kernel selection for ra_forward_ex. */
 enum {
     RA_KERNEL_AUTO = 0, /* tensor-core kernel when the shape allows it, else SIMT */
-    RA_KERNEL_TC = 1,   /* tcgen05 tensor-core kernel (bf16, D in {64,128}, Sb % 128 == 0) */
+    RA_KERNEL_TC = 1,   /* tcgen05 tensor-core kernel (bf16, D in {64,128}, Sb % 128 == 0,
+                           Sb % 256 == 0 for zigzag) */
     RA_KERNEL_SIMT = 2  /* fp32 SIMT kernel (any D <= 256, any Sb); f32 or bf16 */
 };
 
@@ -136,6 +146,21 @@ int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t 
               int inverse, void* stream);
 
 /*
+ * ra_relayout: permute rows between token order and a shard-major layout.
+ *   src, dst: [BH, S, row_bytes] byte arrays (device; must not overlap).
+ *   layout: RA_LAYOUT_* (contiguous is a plain copy).
+ *   inverse = 0: dst row p = src row (token held by shard-major row p)
+ *                (token order -> shard-major)
+ *   inverse = 1: dst row t = src row (shard-major row holding token t)
+ *                (shard-major -> token order)
+ * for every (bh) slice.  row_bytes > 0 and a multiple of 4.  Bit-exact copy.
+ * Errors: RA_ERR_INVALID_ARG (also: unknown layout, zigzag with odd S/N),
+ * RA_ERR_ALIGN (pointers not 16-byte aligned), RA_ERR_CUDA.
+ */
+int ra_relayout(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
+                int layout, int inverse, void* stream);
+
+/*
  * ra_plan (host only, no GPU): the fold list of one query tile.
  * For query shard i and query tile qt (rows [qt*tile, (qt+1)*tile) of the
  * shard), writes n_items entries of 4 int32 each, (s, j, kt, kind), in fold
@@ -145,7 +170,8 @@ int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t 
  * key row <= local query row) or RA_FOLD_STRICT (local key row < local query
  * row).  This is the exact order the tensor-core kernel folds the tile in.
  *   items: int32[cap][4] or NULL (then only *n_items is set).
- *   Requires tile >= 2 and Sb % tile == 0.
+ *   striped is the layout (RA_LAYOUT_*).  Requires tile >= 2 and
+ *   Sb % tile == 0 (Sb % (2*tile) == 0 for zigzag).
  * Errors: RA_ERR_INVALID_ARG, RA_ERR_CAPACITY (cap too small; *n_items is
  * still set).
  */

@@ -31,28 +31,45 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------- layouts
-def positions(S: int, N: int, striped: bool) -> np.ndarray:
+CONTIGUOUS, STRIPED, ZIGZAG = 0, 1, 2
+
+
+def positions(S: int, N: int, striped) -> np.ndarray:
     """Token position held by each shard-major row (length S, int64).
 
-    Contiguous sharding (aiunderstanding.org, "Immersione profonda": each
-    device owns a contiguous block of tokens): row p holds token p.
-    Striped (glossary page, Striped Attention: tokens spread evenly over the
-    devices, read as token t -> device t mod N, local row t div N): row
-    i*Sb + r holds token r*N + i.
+    Layouts (``striped`` is False/0, True/1 or 2):
+      0 contiguous (aiunderstanding.org, "Immersione profonda": each device
+        owns a contiguous block of tokens): row p holds token p;
+      1 striped (glossary page, Striped Attention: tokens spread evenly over
+        the devices, read as token t -> device t mod N, local row t div N):
+        row i*Sb + r holds token r*N + i;
+      2 zigzag (aiunderstanding.org page in Zulu, "Ikusasa": named as another
+        causal load-balancing variant, not defined there; read as: cut the
+        sequence into 2N chunks of Sb/2 tokens, device i holds chunk i then
+        chunk 2N-1-i): row i*Sb + r holds token i*Sb/2 + r for r < Sb/2 and
+        (2N-1-i)*Sb/2 + (r - Sb/2) otherwise.
     """
     if S % N:
         raise ValueError("S must be a multiple of N")
     Sb = S // N
     p = np.arange(S, dtype=np.int64)
-    if not striped:
+    layout = int(striped)
+    if layout == CONTIGUOUS:
         return p
     i, r = p // Sb, p % Sb
-    return r * N + i
+    if layout == STRIPED:
+        return r * N + i
+    if layout == ZIGZAG:
+        if Sb % 2:
+            raise ValueError("zigzag needs an even shard size")
+        h = Sb // 2
+        return np.where(r < h, i * h + r, (2 * N - 1 - i) * h + (r - h))
+    raise ValueError(f"unknown layout {striped}")
 
 
-def stripe_perm(S: int, N: int) -> np.ndarray:
-    """perm[p] = token held by shard-major row p under the striped layout."""
-    return positions(S, N, True)
+def stripe_perm(S: int, N: int, layout=1) -> np.ndarray:
+    """perm[p] = token held by shard-major row p (striped layout by default)."""
+    return positions(S, N, layout)
 
 
 def to_shard_major(x_tok: np.ndarray, N: int, striped: bool) -> np.ndarray:

@@ -26,7 +26,7 @@ class Workload:
     N: int
     D: int
     causal: bool
-    striped: bool
+    striped: int  # layout: 0 contiguous, 1 striped, 2 zigzag
 
     @property
     def seed(self) -> int:
@@ -53,7 +53,8 @@ class Workload:
         return {
             "workload": self.name, "dtype": self.dtype, "B": self.B, "Hq": self.Hq,
             "Hkv": self.Hkv, "S": self.S, "N": self.N, "Sb": self.Sb, "D": self.D,
-            "causal": self.causal, "layout": "striped" if self.striped else "contiguous",
+            "causal": self.causal,
+            "layout": ("contiguous", "striped", "zigzag")[int(self.striped)],
         }
 
 
@@ -65,6 +66,9 @@ WORKLOADS = {
                                   2, 32, 32, 32768, 8, 128, True, False),
     "causal_32k_striped": Workload(2, "bf16_causal_B2_H32_S32768_N8_D128_striped", "bf16",
                                    2, 32, 32, 32768, 8, 128, True, True),
+    # the same shape under the zigzag layout (2N chunks, device i holds chunks i and 2N-1-i)
+    "causal_32k_zigzag": Workload(2, "bf16_causal_B2_H32_S32768_N8_D128_zigzag", "bf16",
+                                  2, 32, 32, 32768, 8, 128, True, 2),
     "gqa_128k": Workload(3, "bf16_causal_gqa_B1_Hq32_Hkv8_S131072_N16_D128_striped", "bf16",
                          1, 32, 8, 131072, 16, 128, True, True),
     # profiling case: same kernel shape as gqa_128k, inputs larger than L2 but under 1 GB

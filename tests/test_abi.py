@@ -61,6 +61,13 @@ def test_host_validation_rejects_before_any_device_work(lib):
     assert call(Hq=3, Hkv=2) == ra.RA_ERR_INVALID_ARG    # Hq % Hkv
     assert call(B=0) == ra.RA_ERR_INVALID_ARG
     assert call(D=512) == ra.RA_ERR_UNSUPPORTED
+    p2 = ctypes.c_void_p(16 * 1024)
+    assert ra.ra_forward(p2, p2, p2, p2, None, 1, 1, 1, 6, 8, 2, 1, 2, 0.0, ra.RA_BF16,
+                         None) == ra.RA_ERR_INVALID_ARG   # zigzag needs an even S/N
+    assert ra.ra_forward(p2, p2, p2, p2, None, 1, 1, 1, 8, 8, 2, 1, 3, 0.0, ra.RA_BF16,
+                         None) == ra.RA_ERR_INVALID_ARG   # unknown layout
+    assert ra.ra_relayout(p2, ctypes.c_void_p(1 << 30), 1, 6, 2, 16, 2, 0,
+                          None) == ra.RA_ERR_INVALID_ARG
     assert call(q=ctypes.c_void_p(16 * 1024 + 2)) == ra.RA_ERR_ALIGN
     assert ra.ra_forward_ex(p, p, p, p, None, 1, 1, 1, 256, 128, 2, 0, 0, 0.0, ra.RA_BF16, 7,
                             None) == ra.RA_ERR_INVALID_ARG
@@ -88,8 +95,9 @@ def test_plan_errors(lib):
     assert n.value == 2
 
 
-@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])
-@pytest.mark.parametrize("S,N,T", [(512, 4, 32), (768, 3, 64), (384, 1, 128), (1024, 8, 16),
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True),
+                                            (True, 2)])
+@pytest.mark.parametrize("S,N,T", [(512, 4, 32), (768, 3, 64), (256, 1, 128), (1024, 8, 16),
                                    (96, 6, 2)])
 def test_plan_equals_bruteforce_schedule(lib, causal, striped, S, N, T):
     """Bit-exact: the library's closed-form fold list == oracle brute force."""

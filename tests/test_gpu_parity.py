@@ -81,6 +81,9 @@ TC_GRID = [
     (1, 4, 4, 1024, 4, 64, True, True),
     (1, 2, 1, 1536, 3, 64, False, False),
     (1, 4, 2, 2048, 4, 128, False, False),
+    (1, 4, 2, 2048, 4, 128, True, 2),      # zigzag, GQA head pairing
+    (2, 2, 2, 1536, 3, 128, True, 2),      # zigzag, MHA tile pairing, 2 tiles per chunk
+    (1, 2, 1, 1024, 2, 64, True, 2),
 ]
 
 
@@ -105,7 +108,7 @@ def test_tc_custom_scale_and_no_lse(ra):
     assert torch.isfinite(out.float()).all()
 
 
-@pytest.mark.parametrize("causal,striped", [(True, False), (True, True), (False, False)])
+@pytest.mark.parametrize("causal,striped", [(True, False), (True, True), (False, False), (True, 2)])
 def test_simt_bf16_matches_oracle(ra, causal, striped):
     B, Hq, Hkv, S, N, D = 1, 2, 1, 640, 5, 96  # outside the tensor-core envelope
     q, k, v = inputs(77, B, Hq, Hkv, S, D, "bf16")
@@ -121,6 +124,8 @@ def test_simt_bf16_matches_oracle(ra, causal, striped):
     (2, 2, 768, 2, True, False),
     (3, 1, 768, 2, True, True),
     (2, 1, 512, 2, False, False),
+    (2, 1, 1024, 2, True, 2),
+    (2, 2, 1536, 3, True, 2),
 ])
 def test_fold_log_is_the_bruteforce_schedule(ra, Hq, Hkv, S, N, causal, striped):
     """Bit-exact: the order in which the kernel folded every query tile equals
@@ -149,16 +154,21 @@ def test_fold_log_is_the_bruteforce_schedule(ra, Hq, Hkv, S, N, causal, striped)
     assert_close(from_device(out), from_device(lse), ro, rl, "bf16", "logging variant")
 
 
-@pytest.mark.parametrize("S,N,D,dt", [(4096, 8, 128, "bf16"), (96, 3, 16, "f32"),
-                                      (130, 5, 6, "bf16")])
-def test_stripe_permutation_bitexact(ra, S, N, D, dt):
+@pytest.mark.parametrize("S,N,D,dt,layout", [(4096, 8, 128, "bf16", 1), (96, 3, 16, "f32", 1),
+                                             (130, 5, 6, "bf16", 1), (4096, 8, 128, "bf16", 2),
+                                             (120, 3, 6, "bf16", 2), (64, 4, 16, "f32", 2)])
+def test_stripe_permutation_bitexact(ra, S, N, D, dt, layout):
     import torch
     x = np.asarray(inputs(9, 2, 3, 1, S, D, dt)[0])
     tx = to_device(x, dt)
-    sm = ra.stripe(tx, N)
-    back = ra.stripe(sm, N, inverse=True)
+    if layout == 1:
+        sm = ra.stripe(tx, N)
+        back = ra.stripe(sm, N, inverse=True)
+    else:
+        sm = ra.relayout(tx, N, layout)
+        back = ra.relayout(sm, N, layout, inverse=True)
     torch.cuda.synchronize()
-    perm = oracle.stripe_perm(S, N)
+    perm = oracle.stripe_perm(S, N, layout)
     got = sm.cpu().view(torch.int16 if dt == "bf16" else torch.int32).numpy()
     want = x.view(np.int16 if dt == "bf16" else np.int32)[..., perm, :]
     assert np.array_equal(got, want)
@@ -244,7 +254,8 @@ def test_noncausal_8k_every_row(ra):
 
 
 @pytest.mark.parametrize("name,n_rows", [("causal_32k_contig", 768), ("causal_32k_striped", 768),
-                                         ("gqa_128k", 768), ("long_1m", 384)])
+                                         ("causal_32k_zigzag", 768), ("gqa_128k", 768),
+                                         ("long_1m", 384)])
 def test_full_size_sampled_rows(ra, name, n_rows):
     import torch
     wl = WORKLOADS[name]

@@ -59,7 +59,7 @@ def test_full_matches_brute_force(causal, Hq, Hkv):
         np.testing.assert_allclose(lse[0, h], lb, rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("striped", [False, True])
+@pytest.mark.parametrize("striped", [False, True, 2])
 @pytest.mark.parametrize("causal", [False, True])
 def test_ring_matches_brute_force(causal, striped):
     S, D, N = 16, 4, 4
@@ -74,7 +74,7 @@ def test_ring_matches_brute_force(causal, striped):
         np.testing.assert_allclose(lse[0, h], lb, atol=1e-12, rtol=0)
 
 
-@pytest.mark.parametrize("striped", [False, True])
+@pytest.mark.parametrize("striped", [False, True, 2])
 @pytest.mark.parametrize("causal", [False, True])
 def test_zero_query_closed_form(causal, striped):
     """Q = 0 makes every visible key equally likely: O is the mean of the
@@ -135,14 +135,14 @@ def test_library_sdpa_crosscheck(causal):
     ref = torch.nn.functional.scaled_dot_product_attention(
         torch.from_numpy(q), tk, tv, is_causal=causal).numpy()
     np.testing.assert_allclose(o, ref, atol=1e-12, rtol=0)
-    for striped in (False, True):
+    for striped in (False, True, 2):
         qs, ks, vs = (oracle.to_shard_major(x, 5, striped) for x in (q, k, v))
         o_sm, _ = oracle.ring_attention(qs, ks, vs, 5, causal, striped)
         np.testing.assert_allclose(oracle.to_token_order(o_sm, 5, striped), ref, atol=1e-12)
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 8])
-@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True), (True, 2)])
 def test_ring_equals_full(N, causal, striped):
     """The pages' central claim: the ring-order blockwise fold equals full attention."""
     S, D = 48, 8
@@ -168,15 +168,31 @@ def test_permutation_equivariance_noncausal():
     np.testing.assert_allclose(lse2, lse[..., pq], atol=1e-12)
 
 
-def test_striped_equals_contiguous_after_unpermuting():
+@pytest.mark.parametrize("layout", [1, 2])
+def test_striped_and_zigzag_equal_contiguous_after_unpermuting(layout):
     S, D, N = 64, 8, 8
     q, k, v = rnd((1, 2, S, D), 23), rnd((1, 1, S, D), 24), rnd((1, 1, S, D), 25)
     o_c, lse_c = oracle.ring_attention(q, k, v, N, True, False)  # token order == contiguous
-    qs, ks, vs = (oracle.to_shard_major(x, N, True) for x in (q, k, v))
-    o_s, lse_s = oracle.ring_attention(qs, ks, vs, N, True, True)
-    np.testing.assert_allclose(oracle.to_token_order(o_s, N, True), o_c, atol=1e-12)
-    np.testing.assert_allclose(oracle.to_token_order(lse_s[..., None], N, True)[..., 0], lse_c,
+    qs, ks, vs = (oracle.to_shard_major(x, N, layout) for x in (q, k, v))
+    o_s, lse_s = oracle.ring_attention(qs, ks, vs, N, True, layout)
+    np.testing.assert_allclose(oracle.to_token_order(o_s, N, layout), o_c, atol=1e-12)
+    np.testing.assert_allclose(oracle.to_token_order(lse_s[..., None], N, layout)[..., 0], lse_c,
                                atol=1e-12)
+
+
+def test_zigzag_positions_example():
+    """2N chunks of Sb/2 tokens; device i holds chunk i then chunk 2N-1-i."""
+    # N=4, S=16: chunks of 2 tokens; device 0 holds chunks 0 and 7, device 3 chunks 3 and 4
+    assert oracle.positions(16, 4, 2).tolist() == [0, 1, 14, 15, 2, 3, 12, 13,
+                                                   4, 5, 10, 11, 6, 7, 8, 9]
+    assert oracle.positions(4, 1, 2).tolist() == [0, 1, 2, 3]
+    # every device owns the same number of visible causal pairs (the point of the layout)
+    S, N = 64, 4
+    pos = oracle.positions(S, N, 2).reshape(N, -1)
+    work = [sum(int(t) + 1 for t in dev) for dev in pos]
+    assert len(set(work)) == 1
+    with pytest.raises(ValueError):
+        oracle.positions(12, 4, 2)  # odd shard size
 
 
 def test_stripe_permutation_examples():
@@ -249,7 +265,8 @@ def _covered_pairs(S, N, causal, striped, T, sched):
     return cover, want
 
 
-@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True),
+                                            (True, 2)])
 def test_schedule_covers_each_visible_pair_once(causal, striped):
     S, N, T = 256, 4, 16
     sched = oracle.fold_schedule(S, N, causal, striped, T, T)
@@ -271,6 +288,9 @@ def test_schedule_tile_counts_closed_form():
     assert len(oracle.fold_schedule(S, N, True, False, T, T)) == n * (n + 1) // 2
     assert len(oracle.fold_schedule(S, N, True, True, T, T)) == N * N * m * (m + 1) // 2
     assert len(oracle.fold_schedule(S, N, False, False, T, T)) == n * n
+    # zigzag: chunk pairs are full or diagonal, never strict -> the contiguous count
+    zz = oracle.fold_schedule(S, N, True, 2, T, T)
+    assert len(zz) == n * (n + 1) // 2 and all(e[5] != STRICT for e in zz)
     # the 32K-token, 8-device layouts at 128-token tiles, from one query shard per
     # kind of pair to keep it fast: shard 3 (contiguous) sees 3 full blocks + diagonal
     S, N, T = 32768, 8, 128
