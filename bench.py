@@ -48,7 +48,8 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", default="forward", choices=["forward", "merge", "stripe", "f32"],
+    ap.add_argument("--op", default="forward",
+                    choices=["forward", "merge", "stripe", "f32", "ulysses"],
                     help="forward: the ring-attention step (default); merge / stripe: the "
                          "HBM-bound helpers on the workload's output / query tensors; f32: the "
                          "fp32 SIMT path on the workload")
@@ -282,6 +283,15 @@ def aux_arm(args, wl):
         def step():
             ra.merge(oa, la, ob, lb, stream=stream)
         name, bound_unit = "ra::aux::merge_kernel<bf16>", "GB/s"
+    elif args.op == "ulysses":
+        B, H, S, D = qs
+        x = torch.randn((wl.N, B, H, S // wl.N, D), device="cuda", generator=gen).to(torch.bfloat16)
+        y = torch.empty((wl.N, B, H // wl.N, S, D), dtype=torch.bfloat16, device="cuda")
+        bytes_per = 2 * x.numel() * 2
+
+        def step():
+            ra.ulysses_exchange(x, wl.N, out=y, stream=stream)
+        name, bound_unit = "ra::aux::ulysses_chunks_kernel<uint4>", "GB/s"
     elif args.op == "stripe":
         x = torch.randn(qs, device="cuda", generator=gen).to(torch.bfloat16)
         y = torch.empty_like(x)

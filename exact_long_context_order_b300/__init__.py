@@ -34,6 +34,7 @@ _SIGNATURES = {
     "ra_merge": ([_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp], _i32),
     "ra_stripe": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _vp], _i32),
     "ra_relayout": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _i32, _vp], _i32),
+    "ra_ulysses_exchange": ([_vp, _vp, _i32, _i32, _i64, _i32, _i64, _i32, _vp], _i32),
     "ra_plan": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)], _i32),
     "ra_fold_log": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
                      _f32, _vp, _vp, _i32, _vp], _i32),
@@ -94,6 +95,10 @@ def ra_stripe(src, dst, BH, S, N, row_bytes, inverse, stream):
 
 def ra_relayout(src, dst, BH, S, N, row_bytes, layout, inverse, stream):
     return lib().ra_relayout(src, dst, BH, S, N, row_bytes, layout, inverse, stream)
+
+
+def ra_ulysses_exchange(src, dst, B, H, S, N, row_bytes, inverse, stream):
+    return lib().ra_ulysses_exchange(src, dst, B, H, S, N, row_bytes, inverse, stream)
 
 
 def ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items):
@@ -251,6 +256,25 @@ def relayout(x, N: int, layout: int, inverse: bool = False, out=None, stream=Non
     rc = ra_relayout(_ptr(x), _ptr(out), BH, S, N, row_bytes, int(layout), int(inverse),
                      _stream_handle(stream))
     _check(rc, "ra_relayout")
+    return out
+
+
+def ulysses_exchange(x, N: int, inverse: bool = False, out=None, stream=None):
+    """Sequence-sharded [N, B, H, S/N, D] <-> head-sharded [N, B, H/N, S, D]."""
+    import torch
+    if not inverse:
+        n, B, H, Sb, D = x.shape
+        shape = (N, B, H // N, N * Sb, D)
+        S = N * Sb
+    else:
+        n, B, Hl, S, D = x.shape
+        shape = (N, B, Hl * N, S // N, D)
+        H = Hl * N
+    if out is None:
+        out = torch.empty(shape, dtype=x.dtype, device=x.device)
+    rc = ra_ulysses_exchange(_ptr(x), _ptr(out), B, H, S, N, D * x.element_size(), int(inverse),
+                             _stream_handle(stream))
+    _check(rc, "ra_ulysses_exchange")
     return out
 
 

@@ -48,4 +48,7 @@ int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_
 int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
                   int layout, int inverse, cudaStream_t stream);
 
+int launch_ulysses(const void* src, void* dst, int64_t B, int64_t H, int64_t S, int N,
+                   int64_t row_bytes, int inverse, cudaStream_t stream);
+
 }  // namespace ra

@@ -231,6 +231,25 @@ int ra_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t 
     return ra_relayout(src, dst, BH, S, N, row_bytes, RA_LAYOUT_STRIPED, inverse, stream);
 }
 
+int ra_ulysses_exchange(const void* src, void* dst, int B, int H, int64_t S, int N,
+                        int64_t row_bytes, int inverse, void* stream) {
+    if (B < 0 || H < 0 || S < 0 || N <= 0 || row_bytes <= 0 || row_bytes % 4) return RA_ERR_INVALID_ARG;
+    if (S % N || H % N) return RA_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || S == 0) return RA_OK;
+    if (!src || !dst) return RA_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return RA_ERR_ALIGN;
+    const char* s = static_cast<const char*>(src);
+    char* d = static_cast<char*>(dst);
+    const int64_t bytes = (int64_t)B * H * S * row_bytes;
+    if (s < d + bytes && d < s + bytes) return RA_ERR_INVALID_ARG;  // overlap
+    int rc = device_state(nullptr, nullptr);
+    if (rc) return rc;
+    rc = ra::launch_ulysses(src, dst, B, H, S, N, row_bytes, inverse ? 1 : 0,
+                            static_cast<cudaStream_t>(stream));
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
 int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, int32_t* items,
             int64_t cap, int64_t* n_items) {
     if (!n_items || S <= 0 || N <= 0 || tile < 2 || S % N) return RA_ERR_INVALID_ARG;

@@ -10,6 +10,9 @@
 //              holding chunks i and 2N-1-i of 2N chunks (the Zulu
 //              aiunderstanding.org page names the variant; this layout is the
 //              build's reading of it).
+//  * ulysses -- the all-to-all of DeepSpeed Ulysses (glossary page, comparison
+//              with other kinds of parallelism) as a permutation between N
+//              device-contiguous buffers: sequence-sharded <-> head-sharded.
 // Rows of 2..32 16-byte vectors use the row-group kernels (several rows per
 // warp, every lane moving 16 bytes, loads batched ahead of stores); other
 // shapes fall back to one warp per row.
@@ -222,6 +225,43 @@ __global__ void __launch_bounds__(kBlock) stripe_rows_kernel(const uint4* __rest
     }
 }
 
+// Ulysses head/sequence exchange between N device-contiguous buffers:
+// forward, sequence-sharded [N][B][H][Sb] -> head-sharded [N][B][H/N][S]:
+//   dst[d][b][hl][t] = src[t / Sb][b][d*H/N + hl][t % Sb]; inverse maps back.
+// The exchange moves whole chunks of Sb consecutive rows: destination chunk c
+// (grid y) is decoded once per thread, then its Sb*row_bytes bytes are copied
+// as 16-byte vectors (or 4-byte words when rows are not 16-byte multiples).
+template <typename V>
+__global__ void __launch_bounds__(kBlock) ulysses_chunks_kernel(const V* __restrict__ src,
+                                                               V* __restrict__ dst, int64_t B,
+                                                               int64_t H, int64_t S, int64_t N,
+                                                               int64_t chunk_elems, int inverse) {
+    const int64_t c = blockIdx.y;  // destination chunk
+    const int64_t Hl = H / N;
+    int64_t src_chunk_row;         // first source row of the chunk
+    if (!inverse) {                // c = ((d*B + b)*Hl + hl)*N + i
+        const int64_t i = c % N, hl = (c / N) % Hl, b = (c / (N * Hl)) % B, d = c / (N * Hl * B);
+        src_chunk_row = ((i * B + b) * H + d * Hl + hl) * (S / N);
+    } else {                       // c = (i*B + b)*H + h
+        const int64_t h = c % H, b = (c / H) % B, i = c / (H * B);
+        src_chunk_row = ((h / Hl * B + b) * Hl + h % Hl) * S + i * (S / N);
+    }
+    const int64_t row_elems = chunk_elems / (S / N);
+    const V* s = src + src_chunk_row * row_elems;
+    V* d = dst + c * chunk_elems;
+    constexpr int U = 4;
+    for (int64_t e = ((int64_t)blockIdx.x * kBlock + threadIdx.x) * U; e < chunk_elems;
+         e += (int64_t)gridDim.x * kBlock * U) {
+        V x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (e + u < chunk_elems) x[u] = __ldg(s + e + u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (e + u < chunk_elems) d[e + u] = x[u];
+    }
+}
+
 static unsigned grid_for(int64_t rows) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -231,6 +271,31 @@ static unsigned grid_for(int64_t rows) {
 }
 
 }  // namespace aux
+
+int launch_ulysses(const void* src, void* dst, int64_t B, int64_t H, int64_t S, int N,
+                   int64_t row_bytes, int inverse, cudaStream_t stream) {
+    const int64_t chunks = B * H * N;
+    if (chunks == 0 || S == 0) return RA_OK;
+    if (chunks > 65535) {  // one grid row per chunk
+        return RA_ERR_UNSUPPORTED;
+    }
+    const int64_t chunk_bytes = (S / N) * row_bytes;
+    const bool vec = (row_bytes % 16 == 0);
+    const int64_t chunk_elems = chunk_bytes / (vec ? 16 : 4);
+    int64_t gx = (chunk_elems + aux::kBlock * 4 - 1) / (aux::kBlock * 4);
+    if (gx > 64) gx = 64;
+    if (gx < 1) gx = 1;
+    dim3 grid((unsigned)gx, (unsigned)chunks);
+    if (vec)
+        aux::ulysses_chunks_kernel<uint4><<<grid, aux::kBlock, 0, stream>>>(
+            static_cast<const uint4*>(src), static_cast<uint4*>(dst), B, H, S, N, chunk_elems,
+            inverse);
+    else
+        aux::ulysses_chunks_kernel<uint32_t><<<grid, aux::kBlock, 0, stream>>>(
+            static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), B, H, S, N,
+            chunk_elems, inverse);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
 
 int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
                  int D, int dtype, cudaStream_t stream) {

@@ -161,6 +161,29 @@ int ra_relayout(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_
                 int layout, int inverse, void* stream);
 
 /*
+ * ra_ulysses_exchange: the head/sequence all-to-all of DeepSpeed Ulysses,
+ * the alternative context-parallel scheme the glossary page contrasts with
+ * ring attention ("Atencao em anel vs. outros tipos de paralelismo": every
+ * device receives all tokens of a subset of the heads), as a permutation
+ * between N device-contiguous buffers on one GPU.
+ *   inverse = 0: src sequence-sharded [N][B][H][S/N][row_bytes] (device i
+ *                holds tokens [i*S/N, (i+1)*S/N) of every head) ->
+ *                dst head-sharded [N][B][H/N][S][row_bytes] (device d holds
+ *                heads [d*H/N, (d+1)*H/N), all tokens in order):
+ *                dst[d][b][hl][t] = src[t/(S/N)][b][d*H/N + hl][t%(S/N)]
+ *   inverse = 1: the reverse permutation.
+ * Device d's head-sharded buffer is an ra_forward input ([B, H/N, S, D],
+ * contiguous layout, one ring device), so exchange -> attention -> inverse
+ * exchange is Ulysses attention.  Requires S % N == 0 and H % N == 0;
+ * row_bytes > 0 and a multiple of 4; src and dst must not overlap.
+ * Bit-exact copy.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_ALIGN, RA_ERR_CUDA, RA_ERR_UNSUPPORTED
+ * (more than 65535 chunks, B*H*N).
+ */
+int ra_ulysses_exchange(const void* src, void* dst, int B, int H, int64_t S, int N,
+                        int64_t row_bytes, int inverse, void* stream);
+
+/*
  * ra_plan (host only, no GPU): the fold list of one query tile.
  * For query shard i and query tile qt (rows [qt*tile, (qt+1)*tile) of the
  * shard), writes n_items entries of 4 int32 each, (s, j, kt, kind), in fold

@@ -40,4 +40,5 @@ from .attention import (  # noqa: F401
     merge,
     fold_schedule,
     toy_ring_no_max,
+    ulysses_exchange,
 )

@@ -275,6 +275,43 @@ def fold_schedule(S: int, N: int, causal: bool, striped: bool, Tq: int, Tk: int,
     return out
 
 
+# ------------------------------------------------- head/sequence exchange
+def ulysses_exchange(x, N: int, inverse: bool = False):
+    """The all-to-all of DeepSpeed Ulysses as a permutation between N
+    device-contiguous buffers (glossary page, "Atencao em anel vs. outros
+    tipos de paralelismo": the exchange gives each device every token of a
+    subset of the attention heads).
+
+    Forward: x is sequence-sharded [N, B, H, S/N, ...] (device i holds tokens
+    [i*S/N, (i+1)*S/N) of every head); the result is head-sharded
+    [N, B, H/N, S, ...] (device d holds heads [d*H/N, (d+1)*H/N), every token
+    in order):  out[d, b, hl, t] = x[t // (S/N), b, d*H/N + hl, t % (S/N)].
+    inverse=True maps back.  H must be a multiple of N.
+    """
+    x = np.asarray(x)
+    if not inverse:
+        n, B, H, Sb = x.shape[:4]
+        if n != N or H % N:
+            raise ValueError("bad shapes")
+        Hl, S = H // N, N * Sb
+        out = np.empty((N, B, Hl, S) + x.shape[4:], dtype=x.dtype)
+        for d in range(N):
+            for hl in range(Hl):
+                for t in range(S):
+                    out[d, :, hl, t] = x[t // Sb, :, d * Hl + hl, t % Sb]
+        return out
+    n, B, Hl, S = x.shape[:4]
+    if n != N or S % N:
+        raise ValueError("bad shapes")
+    Sb, H = S // N, N * Hl
+    out = np.empty((N, B, H, Sb) + x.shape[4:], dtype=x.dtype)
+    for i in range(N):
+        for h in range(H):
+            for r in range(Sb):
+                out[i, :, h, r] = x[h // Hl, :, h % Hl, i * Sb + r]
+    return out
+
+
 # ----------------------------------------------------- the pages' toy
 def toy_ring_no_max(q, k, v, n_devices: int):
     """The glossary page's four-device simulation, as its text describes it.

@@ -230,6 +230,42 @@ def test_merge_of_kernel_partials_is_full_attention(ra):
     assert_close(from_device(oa), from_device(la), ro, rl, "bf16", "merged halves")
 
 
+# ------------------------------------------------------------------ Ulysses exchange
+@pytest.mark.parametrize("N,B,H,S,D,dt", [(4, 2, 8, 512, 128, "bf16"), (2, 1, 4, 96, 16, "f32"),
+                                          (3, 1, 6, 30, 6, "bf16")])
+def test_ulysses_exchange_bitexact(ra, N, B, H, S, D, dt):
+    import torch
+    x = np.asarray(inputs(13, N * B, H, 1, S // N, D, dt)[0]).reshape(N, B, H, S // N, D)
+    tx = to_device(x, dt)
+    y = ra.ulysses_exchange(tx, N)
+    back = ra.ulysses_exchange(y, N, inverse=True)
+    torch.cuda.synchronize()
+    view = torch.int16 if dt == "bf16" else torch.int32
+    want = oracle.ulysses_exchange(x.view(np.int16 if dt == "bf16" else np.int32), N)
+    assert np.array_equal(y.cpu().view(view).numpy(), want)
+    assert torch.equal(back, tx)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_ulysses_attention_equals_full_attention(ra, causal):
+    """Sequence-sharded inputs -> exchange -> ra_forward per device over its
+    heads -> inverse exchange == full attention."""
+    import torch
+    N, B, H, S, D = 4, 1, 8, 2048, 128
+    q, k, v = inputs(57, B, H, H, S, D, "bf16")
+    seq = [to_device(np.ascontiguousarray(
+        x.reshape(B, H, N, S // N, D).transpose(2, 0, 1, 3, 4)), "bf16") for x in (q, k, v)]
+    hs = [ra.ulysses_exchange(x, N) for x in seq]
+    outs = torch.empty_like(hs[0])
+    for d in range(N):
+        o_d, _ = ra.forward(hs[0][d], hs[1][d], hs[2][d], 1, causal=causal, out=outs[d])
+    back = ra.ulysses_exchange(outs, N, inverse=True)
+    ra.check()
+    o = from_device(back).transpose(1, 2, 0, 3, 4).reshape(B, H, S, D)
+    ro, rl = reference(q, k, v, 1, causal, False, "bf16")
+    assert_close(o, None, ro, rl, "bf16", "ulysses")
+
+
 # ------------------------------------------------------------------ named workloads
 def _device_inputs(wl):
     """Generate a workload's q, k, v straight into pinned host memory, copy to

@@ -305,3 +305,44 @@ def test_schedule_tile_counts_closed_form():
     # and the per-(b, h) totals of the 32K layouts follow from the formulas above
     assert 8 * m * (m + 1) // 2 + 28 * m * m == 32896
     assert N * N * m * (m + 1) // 2 == 33792
+
+
+# ----------------------------------------------------------------- Ulysses exchange
+def test_ulysses_exchange_moves_every_row_to_its_definition():
+    """Rows carry their own (device, b, head, local row) coordinates; after the
+    exchange each must sit at the head-sharded index the definition gives."""
+    N, B, H, Sb = 4, 2, 8, 3
+    x = np.zeros((N, B, H, Sb, 4), dtype=np.int64)
+    for i in range(N):
+        for b in range(B):
+            for h in range(H):
+                for r in range(Sb):
+                    x[i, b, h, r] = (i, b, h, r)
+    y = oracle.ulysses_exchange(x, N)
+    assert y.shape == (N, B, H // N, N * Sb, 4)
+    seen = set()
+    for d in range(N):
+        for b in range(B):
+            for hl in range(H // N):
+                for t in range(N * Sb):
+                    i, bb, h, r = y[d, b, hl, t]
+                    assert (bb, h, i * Sb + r) == (b, d * (H // N) + hl, t)
+                    seen.add((i, bb, h, r))
+    assert len(seen) == N * B * H * Sb  # a permutation: every row exactly once
+    np.testing.assert_array_equal(oracle.ulysses_exchange(y, N, inverse=True), x)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ulysses_pipeline_equals_full_attention(causal):
+    """Exchange, full attention per device over its heads, exchange back ==
+    full attention (the other context-parallel scheme reaches the same result)."""
+    N, B, H, S, D = 2, 1, 4, 16, 8
+    q, k, v = rnd((B, H, S, D), 40), rnd((B, H, S, D), 41), rnd((B, H, S, D), 42)
+    seq = [x.reshape(B, H, N, S // N, D).transpose(2, 0, 1, 3, 4) for x in (q, k, v)]
+    hs = [oracle.ulysses_exchange(x, N) for x in seq]
+    outs = np.stack([oracle.full_attention(hs[0][d], hs[1][d], hs[2][d], causal)[0]
+                     for d in range(N)])
+    back = oracle.ulysses_exchange(outs, N, inverse=True)  # [N, B, H, Sb, D]
+    o = back.transpose(1, 2, 0, 3, 4).reshape(B, H, S, D)
+    o_f, _ = oracle.full_attention(q, k, v, causal)
+    np.testing.assert_allclose(o, o_f, atol=1e-12)
