@@ -206,7 +206,7 @@ def fold_log(q, k, v, N: int, causal: bool, striped: bool, scale=None, stream=No
     import torch
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
-    nt = S // N // 128
+    nt = (S // N + 127) // 128  # a shard's last tile may be partial
     tiles = B * Hq * N * nt
     max_entries = N * nt
     out = torch.empty_like(q)

@@ -158,7 +158,7 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
     const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
                                           scale, RA_BF16);
     if (!ra::tc_supported(p)) return RA_ERR_UNSUPPORTED;
-    if ((int64_t)max_entries < (int64_t)N * (S / N / 128)) return RA_ERR_CAPACITY;
+    if ((int64_t)max_entries < (int64_t)N * ((S / N + 127) / 128)) return RA_ERR_CAPACITY;
     unsigned int* status = nullptr;
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
@@ -255,9 +255,10 @@ int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, 
     if (!n_items || S <= 0 || N <= 0 || tile < 2 || S % N) return RA_ERR_INVALID_ARG;
     if (striped < RA_LAYOUT_CONTIGUOUS || striped > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
     const int64_t Sb = S / N;
-    if (Sb % tile) return RA_ERR_INVALID_ARG;
-    if (striped == RA_LAYOUT_ZIGZAG && (Sb / tile) % 2) return RA_ERR_INVALID_ARG;
-    const int64_t nt = Sb / tile;
+    // the last tile of a shard may be partial, except under zigzag, whose
+    // chunks must be whole tiles
+    if (striped == RA_LAYOUT_ZIGZAG && Sb % (2 * tile)) return RA_ERR_INVALID_ARG;
+    const int64_t nt = (Sb + tile - 1) / tile;
     if (nt > 0x7fffffff || i < 0 || i >= N || qt < 0 || qt >= nt) return RA_ERR_INVALID_ARG;
     ra::RingGeom g{N, (int)nt, causal ? 1 : 0, striped};
     int64_t n = 0;

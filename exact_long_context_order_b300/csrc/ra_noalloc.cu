@@ -72,7 +72,8 @@ extern "C" int ra_forward_noalloc(const void* q, const void* k, const void* v, v
     // The scratch this call needs must fit the static array: one 32-bit work
     // counter, and the work-item count must fit that counter.
     const int64_t need_bytes = 4;
-    const int64_t items_bound = (int64_t)B * Hq * (S / 128);  // >= work items of the kernel
+    const int64_t Sb = S / N;
+    const int64_t items_bound = (int64_t)B * Hq * N * ((Sb + 127) / 128);  // >= work items
     if (need_bytes > kNoAllocScratchBytes || items_bound >= (int64_t)1 << 31)
         return RA_ERR_CAPACITY;
 

@@ -84,6 +84,7 @@ struct Params {
     ItemGeom G;
     int64_t S;
     int Sb;
+    int rem;  // rows of each shard's last tile (128 unless Sb % 128 != 0)
     float sl2;  // scale * log2(e)
     __nv_bfloat16* out;
     float* lse;
@@ -422,8 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 4; ++c) reg_fence(sr[c]);
-                    if (kind != kFull) {
-                        const int lim = (kind == kIncl) ? r : r - 1;  // visible iff col <= lim
+                    // visible iff col <= lim: the diagonal masks, and on a shard's
+                    // last (partial) key tile the columns past the shard's end
+                    int lim = (kind == kIncl) ? r : (kind == kStrict) ? r - 1 : kT - 1;
+                    if (w.kt == G.rg.nt - 1 && p.rem - 1 < lim) lim = p.rem - 1;
+                    if (lim < kT - 1) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -537,6 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid) {
                 const int64_t row = (int64_t)(it.b * G.Hq + it.h[t]) * p.S + (int64_t)it.i * p.Sb +
                                     (int64_t)qt * kT + r;
+                // a shard's last tile may hold fewer than 128 real rows
+                const bool row_ok = qt < G.rg.nt - 1 || r < p.rem;
                 const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
                 const uint64_t inv2 = f2_pack(inv_l, inv_l);
                 uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
@@ -553,11 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         f2_unpack(f2_mul(f2_pack_u(o[e], o[e + 1]), inv2), lo, hi);
                         pkd[e / 2] = pack_bf16x2(lo, hi);
                     }
+                    if (row_ok) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        orow[c * 4 + e] = make_uint4(pkd[4 * e], pkd[4 * e + 1], pkd[4 * e + 2], pkd[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e)
+                            orow[c * 4 + e] = make_uint4(pkd[4 * e], pkd[4 * e + 1], pkd[4 * e + 2],
+                                                         pkd[4 * e + 3]);
+                    }
                 }
-                if (p.lse)
+                if (p.lse && row_ok)
                     p.lse[row] = (l > 0.f) ? (m_used * sl2 + lg2_approx(l)) * 0.69314718055994531f
                                            : -INFINITY;
                 if (LOG && r == 0) {
@@ -625,9 +634,11 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
         return RA_ERR_CUDA;
     Params P;
     const int Sb = (int)(pr.S / pr.N);
-    P.G = make_item_geom(pr.B, pr.Hq, pr.Hkv, pr.N, Sb / kT, pr.causal, pr.striped);
+    const int nt = (Sb + kT - 1) / kT;
+    P.G = make_item_geom(pr.B, pr.Hq, pr.Hkv, pr.N, nt, pr.causal, pr.striped);
     P.S = pr.S;
     P.Sb = Sb;
+    P.rem = Sb - (nt - 1) * kT;
     P.sl2 = (float)((double)pr.scale * 1.4426950408889634);
     P.out = static_cast<__nv_bfloat16*>(pr.out);
     P.lse = pr.lse;
@@ -654,8 +665,10 @@ bool tc_supported(const FwdProblem& p) {
     if (p.dtype != RA_BF16 || (p.D != 64 && p.D != 128)) return false;
     if (p.S % p.N) return false;
     const int64_t Sb = p.S / p.N;
-    if (Sb % tc::kT) return false;
-    if (p.striped == kZigzag && (Sb / tc::kT) % 2) return false;  // chunk = whole tiles
+    // a ragged last tile per shard is supported for contiguous and striped
+    // shards; zigzag chunks must be whole tiles
+    if (p.striped == kZigzag && Sb % (2 * tc::kT)) return false;
+    if (Sb > (1ll << 30)) return false;
     if ((int64_t)p.B * p.Hq * p.S >= (1ll << 31) || (int64_t)p.B * p.Hkv * p.S >= (1ll << 31))
         return false;
     return true;

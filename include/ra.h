@@ -81,8 +81,8 @@ enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_STRIPED = 1, RA_LAYOUT_ZIGZAG = 2 };
 /* Kernel selection for ra_forward_ex. */
 enum {
     RA_KERNEL_AUTO = 0, /* tensor-core kernel when the shape allows it, else SIMT */
-    RA_KERNEL_TC = 1,   /* tcgen05 tensor-core kernel (bf16, D in {64,128}, Sb % 128 == 0,
-                           Sb % 256 == 0 for zigzag) */
+    RA_KERNEL_TC = 1,   /* tcgen05 tensor-core kernel (bf16, D in {64,128}; any Sb for
+                           contiguous/striped shards, Sb % 256 == 0 for zigzag) */
     RA_KERNEL_SIMT = 2  /* fp32 SIMT kernel (any D <= 256, any Sb); f32 or bf16 */
 };
 
@@ -193,8 +193,9 @@ int ra_ulysses_exchange(const void* src, void* dst, int B, int H, int64_t S, int
  * key row <= local query row) or RA_FOLD_STRICT (local key row < local query
  * row).  This is the exact order the tensor-core kernel folds the tile in.
  *   items: int32[cap][4] or NULL (then only *n_items is set).
- *   striped is the layout (RA_LAYOUT_*).  Requires tile >= 2 and
- *   Sb % tile == 0 (Sb % (2*tile) == 0 for zigzag).
+ *   striped is the layout (RA_LAYOUT_*).  Requires tile >= 2; a shard's last
+ *   tile may be partial (ceil(Sb/tile) tiles), except under zigzag, which
+ *   needs Sb % (2*tile) == 0.
  * Errors: RA_ERR_INVALID_ARG, RA_ERR_CAPACITY (cap too small; *n_items is
  * still set).
  */
@@ -257,7 +258,7 @@ int ra_check(void* stream);
  * device loading the library holds until the process exits.
  *   Arguments, layouts and results are those of ra_forward with
  *   dtype = RA_BF16; only the tensor-core kernel's shapes are accepted
- *   (D in {64, 128}, S/N a multiple of 128).
+ *   (D in {64, 128}; S/N a multiple of 256 for zigzag).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call outside CUDA-graph stream
  *   capture.  Each call zeroes the counter on `stream` before its kernel.

@@ -71,6 +71,10 @@ WORKLOADS = {
                                   2, 32, 32, 32768, 8, 128, True, 2),
     "gqa_128k": Workload(3, "bf16_causal_gqa_B1_Hq32_Hkv8_S131072_N16_D128_striped", "bf16",
                          1, 32, 8, 131072, 16, 128, True, True),
+    # the 128K GQA shape with ragged shards (8000 tokens each: the last tile of
+    # every shard holds 64 rows)
+    "gqa_128k_ragged": Workload(6, "bf16_causal_gqa_B1_Hq32_Hkv8_S128000_N16_D128_striped", "bf16",
+                                1, 32, 8, 128000, 16, 128, True, 1),
     # profiling case: same kernel shape as gqa_128k, inputs larger than L2 but under 1 GB
     "prof_64k": Workload(5, "bf16_causal_gqa_B1_Hq16_Hkv4_S65536_N8_D128_striped", "bf16",
                          1, 16, 4, 65536, 8, 128, True, True),

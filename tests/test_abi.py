@@ -85,7 +85,7 @@ def test_host_validation_rejects_before_any_device_work(lib):
 def test_plan_errors(lib):
     n = ctypes.c_int64()
     assert ra.ra_plan(256, 2, 1, 0, 128, 0, 0, None, 0, None) == ra.RA_ERR_INVALID_ARG
-    assert ra.ra_plan(256, 2, 1, 0, 100, 0, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(256, 2, 1, 2, 96, 0, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
     assert ra.ra_plan(256, 2, 1, 0, 128, 2, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
     assert ra.ra_plan(256, 2, 1, 0, 128, 0, 1, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
     assert ra.ra_plan(256, 2, 1, 0, 128, 1, 0, None, 0, ctypes.byref(n)) == ra.RA_OK
@@ -105,7 +105,24 @@ def test_plan_equals_bruteforce_schedule(lib, causal, striped, S, N, T):
     by_tile = {}
     for (i, qt, s, j, kt, kind) in ref:
         by_tile.setdefault((i, qt), []).append((s, j, kt, kind))
-    nt = S // N // T
+    nt = -(-(S // N) // T)
+    for i in range(N):
+        for qt in range(nt):
+            assert ra.plan(S, N, causal, striped, i, qt, tile=T) == by_tile.get((i, qt), []), \
+                (i, qt)
+
+
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])
+@pytest.mark.parametrize("S,N,T", [(600, 3, 64), (130, 1, 16), (7 * 44, 7, 8)])
+def test_plan_with_a_partial_last_tile(lib, causal, striped, S, N, T):
+    """Shards whose size is not a multiple of the tile: ceil(Sb/T) tiles, the
+    last partial; the planner still equals the brute-force schedule."""
+    ref = oracle.fold_schedule(S, N, causal, striped, T, T)
+    by_tile = {}
+    for (i, qt, s, j, kt, kind) in ref:
+        by_tile.setdefault((i, qt), []).append((s, j, kt, kind))
+    nt = -(-(S // N) // T)
+    assert (S // N) % T
     for i in range(N):
         for qt in range(nt):
             assert ra.plan(S, N, causal, striped, i, qt, tile=T) == by_tile.get((i, qt), []), \

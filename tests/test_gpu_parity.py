@@ -84,6 +84,12 @@ TC_GRID = [
     (1, 4, 2, 2048, 4, 128, True, 2),      # zigzag, GQA head pairing
     (2, 2, 2, 1536, 3, 128, True, 2),      # zigzag, MHA tile pairing, 2 tiles per chunk
     (1, 2, 1, 1024, 2, 64, True, 2),
+    # ragged: the last tile of every shard is partial
+    (1, 2, 1, 600, 3, 128, True, False),     # Sb = 200
+    (1, 4, 2, 1200, 4, 128, True, True),     # Sb = 300, striped
+    (2, 2, 2, 1000, 2, 128, True, False),    # Sb = 500, MHA tile pairing
+    (1, 2, 2, 520, 2, 64, False, False),     # Sb = 260, non-causal, D = 64
+    (1, 2, 1, 130, 1, 128, True, True),      # Sb = 130, one ring device
 ]
 
 
@@ -126,6 +132,8 @@ def test_simt_bf16_matches_oracle(ra, causal, striped):
     (2, 1, 512, 2, False, False),
     (2, 1, 1024, 2, True, 2),
     (2, 2, 1536, 3, True, 2),
+    (2, 1, 600, 3, True, True),   # ragged shards
+    (2, 2, 1000, 2, True, False),
 ])
 def test_fold_log_is_the_bruteforce_schedule(ra, Hq, Hkv, S, N, causal, striped):
     """Bit-exact: the order in which the kernel folded every query tile equals
@@ -141,7 +149,7 @@ def test_fold_log_is_the_bruteforce_schedule(ra, Hq, Hkv, S, N, causal, striped)
     by_tile = {}
     for (i, qt, s, j, kt, kind) in ref:
         by_tile.setdefault((i, qt), []).append((s, j, kt, kind))
-    nt = S // N // 128
+    nt = -(-(S // N) // 128)
     for b in range(B):
         for h in range(Hq):
             for i in range(N):

@@ -49,9 +49,16 @@ def test_withheld_copy_times_out_and_context_stays_usable(ra):
 
 
 def test_selftest_argument_checks(ra):
-    import ctypes
-    p = ctypes.c_void_p(1 << 20)  # never dereferenced: rejected on the host
-    assert ra.ra_watchdog_selftest(p, p, p, p, None, 1, 1, 1, 256, 128, 2, 1, 0, 0.0, 10,
-                                   None) == ra.RA_ERR_INVALID_ARG
-    assert ra.ra_watchdog_selftest(p, p, p, p, None, 1, 1, 1, 256, 96, 2, 1, 0, 0.0,
-                                   1_000_000, None) == ra.RA_ERR_UNSUPPORTED
+    """Refused on the host; the buffers are real and large enough anyway."""
+    import torch
+    q = torch.zeros((1, 1, 256, 128), dtype=torch.bfloat16, device="cuda")
+    k, v, o = torch.zeros_like(q), torch.zeros_like(q), torch.zeros_like(q)
+    P = [ra._ptr(x) for x in (q, k, v, o)]
+    assert ra.ra_watchdog_selftest(*P, None, 1, 1, 1, 256, 128, 2, 1, 0, 0.0, 10,
+                                   None) == ra.RA_ERR_INVALID_ARG    # limit below 1e5 cycles
+    q96 = torch.zeros((1, 1, 256, 96), dtype=torch.bfloat16, device="cuda")
+    P96 = [ra._ptr(x) for x in (q96, torch.zeros_like(q96), torch.zeros_like(q96),
+                                torch.zeros_like(q96))]
+    assert ra.ra_watchdog_selftest(*P96, None, 1, 1, 1, 256, 96, 2, 1, 0, 0.0, 1_000_000,
+                                   None) == ra.RA_ERR_UNSUPPORTED   # D = 96
+    torch.cuda.synchronize()

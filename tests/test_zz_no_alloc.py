@@ -58,11 +58,21 @@ def test_noalloc_matches_forward_on_two_calls(ra):
 
 
 def test_noalloc_rejects_shapes_outside_the_tensor_core_kernel(ra):
-    import ctypes
-    p = ctypes.c_void_p(1 << 20)  # never dereferenced: the host rejects the call first
-    assert ra.ra_forward_noalloc(p, p, p, p, None, 1, 1, 1, 256, 96, 2, 1, 0, 0.0,
-                                 None) == ra.RA_ERR_UNSUPPORTED
-    assert ra.ra_forward_noalloc(p, p, p, p, None, 1, 1, 1, 200, 128, 2, 1, 0, 0.0,
-                                 None) == ra.RA_ERR_UNSUPPORTED
-    assert ra.ra_forward_noalloc(None, p, p, p, None, 1, 1, 1, 256, 128, 2, 1, 0, 0.0,
-                                 None) == ra.RA_ERR_INVALID_ARG
+    """Calls that must be refused on the host.  Every pointer is a real device
+    buffer large enough for the problem, so a call that were accepted by
+    mistake would still read and write valid memory."""
+    import torch
+
+    def bufs(B, H, S, D):
+        q = torch.zeros((B, H, S, D), dtype=torch.bfloat16, device="cuda")
+        return q, torch.zeros_like(q), torch.zeros_like(q), torch.zeros_like(q)
+
+    q, k, v, o = bufs(1, 1, 256, 96)          # D = 96: no tensor-core kernel
+    assert ra.ra_forward_noalloc(ra._ptr(q), ra._ptr(k), ra._ptr(v), ra._ptr(o), None,
+                                 1, 1, 1, 256, 96, 2, 1, 0, 0.0, None) == ra.RA_ERR_UNSUPPORTED
+    q, k, v, o = bufs(1, 1, 768, 128)         # zigzag with S/N = 384: chunks are not whole tiles
+    assert ra.ra_forward_noalloc(ra._ptr(q), ra._ptr(k), ra._ptr(v), ra._ptr(o), None,
+                                 1, 1, 1, 768, 128, 2, 1, 2, 0.0, None) == ra.RA_ERR_UNSUPPORTED
+    assert ra.ra_forward_noalloc(None, ra._ptr(k), ra._ptr(v), ra._ptr(o), None,
+                                 1, 1, 1, 768, 128, 2, 1, 0, 0.0, None) == ra.RA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
