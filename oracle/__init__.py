@@ -23,6 +23,10 @@ Sources (the pages these functions follow):
     mathematically identical to full attention.
   * "Ring Attention la gi?" (thienlv.com), section "Uu Diem": compatible with
     GQA.
+  * Training as the use (Italian aiunderstanding.org page, "Implementazione
+    nel mondo reale"; glossary page, training throughput and
+    context_parallel): the gradients are the chain rule of the plain
+    definition; the ring-order backward is this oracle's reading.
 
 Pin status: every function here is pinned by a CPU test against something
 other than itself (brute force, closed forms, a library routine, the pages'
@@ -41,4 +45,6 @@ from .attention import (  # noqa: F401
     fold_schedule,
     toy_ring_no_max,
     ulysses_exchange,
+    attention_backward,
+    ring_attention_backward,
 )

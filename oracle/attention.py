@@ -229,6 +229,119 @@ def merge(o_a, lse_a, o_b, lse_b):
     return o, lse
 
 
+# ------------------------------------------------------------- gradients
+def attention_backward(q, k, v, dout, causal: bool, scale=None, chunk: int = 512):
+    """Gradients of the plain definition with respect to q, k and v, float64.
+
+    The pages use the method to train long-context models (the Italian
+    aiunderstanding.org page, "Implementazione nel mondo reale": training an
+    LLM on 1M-token sequences; the glossary page: end-to-end training
+    throughput, and PyTorch's context_parallel replacing scaled dot-product
+    attention in training).  They do not write the backward out, so this is
+    the chain rule applied to O = softmax(scale Q K^T) V, row by row, with
+    dO = dL/dO given.  For query row t and its visible keys u:
+        P_tu  = softmax_u(scale q_t . k_u)
+        dV_u  = sum_t P_tu dO_t
+        dP_tu = dO_t . v_u
+        dS_tu = P_tu (dP_tu - sum_u' P_tu' dP_tu')      (softmax Jacobian)
+        dQ_t  = scale sum_u dS_tu k_u
+        dK_u  = scale sum_t dS_tu q_t
+    With grouped-query attention a key/value head's gradient is the sum over
+    the query heads that read it.  Token-order tensors; query rows are taken
+    in chunks of ``chunk`` only to bound memory.  Returns dq, dk, dv.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    dout = np.asarray(dout, np.float64)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    sc = _scale(D, scale)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    pos = np.arange(S, dtype=np.int64)
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, h // g], v[b, h // g]
+            for r0 in range(0, S, chunk):
+                r1 = min(S, r0 + chunk)
+                s = (q[b, h, r0:r1] @ kh.T) * sc
+                if causal:
+                    s = np.where(pos[None, :] <= pos[r0:r1, None], s, -np.inf)
+                m = s.max(axis=1, keepdims=True)
+                m = np.where(np.isfinite(m), m, 0.0)
+                e = np.exp(s - m)
+                den = e.sum(axis=1, keepdims=True)
+                P = e / np.where(den > 0, den, 1.0)
+                dP = dout[b, h, r0:r1] @ vh.T
+                dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                dv[b, h // g] += P.T @ dout[b, h, r0:r1]
+                dq[b, h, r0:r1] = sc * (dS @ kh)
+                dk[b, h // g] += sc * (dS.T @ q[b, h, r0:r1])
+    return dq, dk, dv
+
+
+def ring_attention_backward(q, k, v, dout, N: int, causal: bool, striped, scale=None):
+    """Backward of ``ring_attention`` folded in ring order, float64.
+
+    Reading (the pages name training as the use but leave the backward
+    open): the same ring as the forward, with each key/value block carrying
+    its gradient accumulators dK_j, dV_j as it travels, while dQ_i stays on
+    device i.  Before the ring each device has the forward's lse_i and O_i
+    and forms delta_t = dO_t . O_t, which equals sum_u P_tu dP_tu.  At step
+    s = 0..N-1 device i holds block j = (i - s) mod N and, for the visible
+    pairs of Q_i and K_j (other pairs have P = 0; a block with none is
+    skipped):
+        P     = exp(scale Q_i K_j^T - lse_i)
+        dV_j += P^T dO_i
+        dP    = dO_i V_j^T
+        dS    = P * (dP - delta_i)
+        dQ_i += scale dS K_j
+        dK_j += scale dS^T Q_i
+    Shard-major tensors in, shard-major gradients out.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    dout = np.asarray(dout, np.float64)
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    Sb = S // N
+    sc = _scale(D, scale)
+    pos = positions(S, N, striped)
+    o, lse = ring_attention(q, k, v, N, causal, striped, scale)
+    delta = (dout * o).sum(axis=-1)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            Q, dO = q[b, h], dout[b, h]
+            K, V = k[b, h // g], v[b, h // g]
+            dK, dV = dk[b, h // g], dv[b, h // g]
+            for s in range(N):
+                for i in range(N):
+                    j = (i - s) % N
+                    qi = slice(i * Sb, (i + 1) * Sb)
+                    kj = slice(j * Sb, (j + 1) * Sb)
+                    vis = (pos[kj][None, :] <= pos[qi][:, None]) if causal else \
+                        np.ones((Sb, Sb), dtype=bool)
+                    if not vis.any():
+                        continue
+                    with np.errstate(invalid="ignore"):
+                        P = np.where(vis, np.exp((Q[qi] @ K[kj].T) * sc - lse[b, h, qi][:, None]),
+                                     0.0)
+                    dV[kj] += P.T @ dO[qi]
+                    dP = dO[qi] @ V[kj].T
+                    dS = P * (dP - delta[b, h, qi][:, None])
+                    dq[b, h, qi] += sc * (dS @ K[kj])
+                    dK[kj] += sc * (dS.T @ Q[qi])
+    return dq, dk, dv
+
+
 # ------------------------------------------------------------- schedule
 def fold_schedule(S: int, N: int, causal: bool, striped: bool, Tq: int, Tk: int,
                   i_list=None, qt_list=None):

@@ -1,0 +1,140 @@
+"""Pins for the oracle's gradients, each against something other than itself.
+
+* central finite differences of the forward definition (itself pinned by
+  brute force in test_oracle.py) on tiny inputs;
+* a library routine: torch's scaled_dot_product_attention on CPU in float64,
+  differentiated by autograd;
+* closed forms: with every value row equal, O is that row whatever the
+  scores, so dQ = dK = 0; with Q = 0 the weights are uniform over the visible
+  keys, so dV_u is a plain average of dO over the rows that see u, and dK = 0;
+* invariants: adding a constant to a row's scores changes nothing, so the
+  key gradients sum to zero over keys; every row's weights sum to one, so the
+  value gradients sum to the sum of dO;
+* the ring-order backward equals the plain gradients for every layout.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def loss(q, k, v, dout, causal, scale=None):
+    o, _ = oracle.full_attention(q, k, v, causal, scale)
+    return float((o * dout).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (4, 2), (3, 1)])
+def test_gradients_match_finite_differences(causal, Hq, Hkv):
+    B, S, D = 1, 7, 3
+    q, k, v = rnd((B, Hq, S, D), 11), rnd((B, Hkv, S, D), 12), rnd((B, Hkv, S, D), 13)
+    dout = rnd((B, Hq, S, D), 14)
+    scale = 0.7
+    dq, dk, dv = oracle.attention_backward(q, k, v, dout, causal, scale, chunk=3)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": q, "k": k, "v": v}
+            args[name] = xp
+            lp = loss(args["q"], args["k"], args["v"], dout, causal, scale)
+            args[name] = xm
+            lm = loss(args["q"], args["k"], args["v"], dout, causal, scale)
+            fd[idx] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(g, fd, rtol=0, atol=2e-8, err_msg=name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hq,Hkv", [(2, 2), (4, 1)])
+def test_gradients_match_torch_autograd(causal, Hq, Hkv):
+    torch = pytest.importorskip("torch")
+    B, S, D = 2, 40, 16
+    q, k, v = rnd((B, Hq, S, D), 21), rnd((B, Hkv, S, D), 22), rnd((B, Hkv, S, D), 23)
+    dout = rnd((B, Hq, S, D), 24)
+    dq, dk, dv = oracle.attention_backward(q, k, v, dout, causal, chunk=16)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    g = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(g, dim=1), tv.repeat_interleave(g, dim=1), is_causal=causal)
+    o.backward(torch.tensor(dout, dtype=torch.float64))
+    for mine, lib in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        np.testing.assert_allclose(mine, lib.numpy(), rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_equal_value_rows_give_zero_query_and_key_gradients(causal):
+    B, Hq, Hkv, S, D = 1, 2, 1, 24, 8
+    q, k = rnd((B, Hq, S, D), 31), rnd((B, Hkv, S, D), 32)
+    v = np.broadcast_to(rnd((1, 1, 1, D), 33), (B, Hkv, S, D)).copy()
+    dout = rnd((B, Hq, S, D), 34)
+    dq, dk, dv = oracle.attention_backward(q, k, v, dout, causal)
+    assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
+    assert np.abs(dv).max() > 0.1
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_query_closed_form(causal):
+    """Q = 0: row t weighs its n_t visible keys equally (n_t = t + 1 causal,
+    S otherwise), so dV_u = sum over rows t that see u of dO_t / n_t; the
+    key gradient is scale * dS^T Q = 0."""
+    B, Hq, Hkv, S, D = 1, 3, 1, 20, 4
+    q = np.zeros((B, Hq, S, D))
+    k, v = rnd((B, Hkv, S, D), 41), rnd((B, Hkv, S, D), 42)
+    dout = rnd((B, Hq, S, D), 43)
+    _, dk, dv = oracle.attention_backward(q, k, v, dout, causal)
+    want = np.zeros((S, D))
+    for h in range(Hq):
+        for u in range(S):
+            for t in range(S):
+                if causal and t < u:
+                    continue
+                want[u] += dout[0, h, t] / ((t + 1) if causal else S)
+    np.testing.assert_allclose(dv[0, 0], want, rtol=0, atol=1e-12)
+    assert np.abs(dk).max() < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradient_sums_over_keys(causal):
+    B, Hq, Hkv, S, D = 2, 4, 2, 33, 6
+    q, k, v = rnd((B, Hq, S, D), 51), rnd((B, Hkv, S, D), 52), rnd((B, Hkv, S, D), 53)
+    dout = rnd((B, Hq, S, D), 54)
+    _, dk, dv = oracle.attention_backward(q, k, v, dout, causal, chunk=10)
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, rtol=0, atol=1e-11)
+    want = dout.reshape(B, Hkv, Hq // Hkv, S, D).sum(axis=(2, 3))
+    np.testing.assert_allclose(dv.sum(axis=2), want, rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+@pytest.mark.parametrize("causal,layout", [(False, 0), (True, 0), (True, 1), (True, 2)])
+def test_ring_backward_equals_plain(N, causal, layout):
+    B, Hq, Hkv, S, D = 1, 4, 2, 48, 8
+    q, k, v = rnd((B, Hq, S, D), 61), rnd((B, Hkv, S, D), 62), rnd((B, Hkv, S, D), 63)
+    dout = rnd((B, Hq, S, D), 64)
+    ref = oracle.attention_backward(q, k, v, dout, causal, chunk=20)
+    sm = [oracle.to_shard_major(x, N, layout) for x in (q, k, v, dout)]
+    got = oracle.ring_attention_backward(*sm, N, causal, layout)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(oracle.to_token_order(g, N, layout), r, rtol=0, atol=1e-11)
+
+
+def test_ring_backward_scale_argument():
+    """Scaling q by r and the scale by 1/r leaves every score unchanged; by
+    the chain rule dQ then scales by 1/r while dK and dV are unchanged."""
+    B, Hq, Hkv, S, D, N = 1, 2, 1, 16, 4, 4
+    q, k, v = rnd((B, Hq, S, D), 71), rnd((B, Hkv, S, D), 72), rnd((B, Hkv, S, D), 73)
+    dout = rnd((B, Hq, S, D), 74)
+    r = 0.3 / (1 / math.sqrt(D))
+    a = oracle.ring_attention_backward(q, k, v, dout, N, True, 1, scale=0.3)
+    b = oracle.ring_attention_backward(q * r, k, v, dout, N, True, 1)  # default 1/sqrt(D)
+    np.testing.assert_allclose(a[0], b[0] * r, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(a[2], b[2], rtol=0, atol=1e-12)
