@@ -3,7 +3,7 @@ on one B300, as a C-ABI shared library with a thin ctypes binding.
 
 The functions named ``ra_*`` mirror ``include/ra.h`` one to one: plain
 integers and pointers in, an RA_* status out; they only marshal arguments.
-``forward``, ``merge``, ``stripe`` and ``plan`` are conveniences over them
+``forward``, ``backward``, ``merge``, ``stripe`` and ``plan`` are conveniences over them
 for torch CUDA tensors (PyTorch is used only for device memory and streams);
 every step of the computation runs in the library's CUDA kernels.
 
@@ -36,12 +36,19 @@ _SIGNATURES = {
     "ra_relayout": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _i32, _vp], _i32),
     "ra_ulysses_exchange": ([_vp, _vp, _i32, _i32, _i64, _i32, _i64, _i32, _vp], _i32),
     "ra_plan": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)], _i32),
+    "ra_plan_backward": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)],
+                         _i32),
     "ra_fold_log": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
                      _f32, _vp, _vp, _i32, _vp], _i32),
     "ra_forward_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
                             _i32, _f32, _vp], _i32),
     "ra_watchdog_selftest": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32,
                               _i32, _f32, _i64, _vp], _i32),
+    "ra_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+                     _i64, _i32, _i32, _i32, _i32, _f32, _i32, _vp], _i32),
+    "ra_backward_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32,
+                        _i32, _i64, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
+    "ra_backward_workspace": ([_i32, _i32, _i64, _i32, _c.POINTER(_i64)], _i32),
     "ra_check": ([_vp], _i32),
     "ra_strerror": ([_i32], _c.c_char_p),
     "ra_tile_config": ([_c.POINTER(_i32), _c.POINTER(_i32)], _i32),
@@ -105,6 +112,10 @@ def ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items):
     return lib().ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items)
 
 
+def ra_plan_backward(S, N, causal, striped, tile, j, kt, items, cap, n_items):
+    return lib().ra_plan_backward(S, N, causal, striped, tile, j, kt, items, cap, n_items)
+
+
 def ra_fold_log(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, log, counts,
                 max_entries, stream):
     return lib().ra_fold_log(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, log,
@@ -123,6 +134,25 @@ def ra_watchdog_selftest(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped
                          timeout_cycles, stream):
     return lib().ra_watchdog_selftest(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
                                       scale, timeout_cycles, stream)
+
+
+def ra_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv, S,
+                D, N, causal, striped, scale, dtype, stream):
+    return lib().ra_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B,
+                             Hq, Hkv, S, D, N, causal, striped, scale, dtype, stream)
+
+
+def ra_backward_ex(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, Hq, Hkv,
+                   S, D, N, causal, striped, scale, dtype, kernel, stream):
+    return lib().ra_backward_ex(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes,
+                                B, Hq, Hkv, S, D, N, causal, striped, scale, dtype, kernel, stream)
+
+
+def ra_backward_workspace(B, Hq, S, D):
+    """Returns (status, bytes)."""
+    n = _i64()
+    rc = lib().ra_backward_workspace(B, Hq, S, D, ctypes.byref(n))
+    return rc, n.value
 
 
 def ra_check(stream):
@@ -194,6 +224,43 @@ def forward(q, k, v, N: int, causal: bool = False, striped: bool = False, scale=
                        _stream_handle(stream))
     _check(rc, "ra_forward")
     return out, lse
+
+
+def backward(q, k, v, out, lse, dout, N: int, causal: bool = False, striped: bool = False,
+             scale=None, kernel: str = "auto", workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of ``forward`` over shard-major torch CUDA tensors.
+
+    q, k, v, out and lse are the forward's inputs and outputs, dout = dL/dout
+    (like out).  The workspace (a uint8 CUDA tensor of at least
+    ra_backward_workspace bytes) is allocated here when not given.
+    """
+    import torch
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    dtype = {torch.bfloat16: RA_BF16, torch.float32: RA_F32}.get(q.dtype)
+    if dtype is None:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    for t in (k, v):
+        if t.dtype != q.dtype or t.shape != (B, Hkv, S, D) or not t.is_contiguous():
+            raise ValueError("k and v must be contiguous [B, Hkv, S, D] of q's dtype")
+    for t in (q, out, dout):
+        if t.dtype != q.dtype or t.shape != (B, Hq, S, D) or not t.is_contiguous():
+            raise ValueError("q, out and dout must be contiguous [B, Hq, S, D] of one dtype")
+    if lse is None or lse.dtype != torch.float32 or lse.shape != (B, Hq, S):
+        raise ValueError("lse must be the forward's float32 [B, Hq, S]")
+    rc, need = ra_backward_workspace(B, Hq, S, D)
+    _check(rc, "ra_backward_workspace")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    rc = ra_backward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
+                        _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, Hq, Hkv, S, D,
+                        N, int(causal), int(striped), float(scale or 0.0), dtype,
+                        _KERNELS[kernel], _stream_handle(stream))
+    _check(rc, "ra_backward")
+    return dq, dk, dv
 
 
 def fold_log(q, k, v, N: int, causal: bool, striped: bool, scale=None, stream=None):
@@ -286,6 +353,17 @@ def plan(S: int, N: int, causal: bool, striped: bool, i: int, qt: int, tile: int
     buf = (ctypes.c_int32 * (4 * max(1, n.value)))()
     _check(ra_plan(S, N, int(causal), int(striped), tile, i, qt, buf, n.value, ctypes.byref(n)),
            "ra_plan")
+    return [tuple(buf[4 * e:4 * e + 4]) for e in range(n.value)]
+
+
+def plan_backward(S: int, N: int, causal: bool, striped, j: int, kt: int, tile: int = 128):
+    """The dk/dv visiting order of key tile kt of shard j as [(s, i, qt, kind)]."""
+    n = _i64()
+    _check(ra_plan_backward(S, N, int(causal), int(striped), tile, j, kt, None, 0,
+                            ctypes.byref(n)), "ra_plan_backward")
+    buf = (_i32 * (4 * max(n.value, 1)))()
+    _check(ra_plan_backward(S, N, int(causal), int(striped), tile, j, kt, buf, n.value,
+                            ctypes.byref(n)), "ra_plan_backward")
     return [tuple(buf[4 * e:4 * e + 4]) for e in range(n.value)]
 
 

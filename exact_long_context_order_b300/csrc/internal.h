@@ -48,6 +48,35 @@ int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_
 int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
                   int layout, int inverse, cudaStream_t stream);
 
+// Backward problem: the forward's tensors plus dout, the gradients and the
+// per-row terms delta (float32 [B*Hq*S], in the caller's workspace).
+struct BwdProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* out;
+    const float* lse;
+    const void* dout;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* delta;
+    int B, Hq, Hkv;
+    int64_t S;
+    int D, N, causal, striped;
+    float scale;
+    int dtype;
+};
+
+int launch_bwd_delta(const BwdProblem& p, cudaStream_t stream);
+int launch_bwd_simt(const BwdProblem& p, cudaStream_t stream);
+int launch_bwd_dkdv_simt(const BwdProblem& p, cudaStream_t stream);
+bool tc_bwd_supported(const BwdProblem& p);
+// Tensor-core backward (delta already computed): the dq kernel, then the
+// dk/dv kernel, each zeroing the work counter on `stream` before it starts.
+int launch_bwd_tc(const BwdProblem& p, unsigned int* status, unsigned int* work, int sm_count,
+                  cudaStream_t stream);
+
 int launch_ulysses(const void* src, void* dst, int64_t B, int64_t H, int64_t S, int N,
                    int64_t row_bytes, int inverse, cudaStream_t stream);
 

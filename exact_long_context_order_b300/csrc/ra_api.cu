@@ -84,8 +84,9 @@ int work_slot(unsigned int** slot) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int validate_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B,
-                     int Hq, int Hkv, int64_t S, int D, int N, int dtype, int layout) {
+int validate_forward(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, int B, int Hq, int Hkv, int64_t S, int D, int N, int dtype,
+                     int layout) {
     if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
     if (S % N != 0 || Hq % Hkv != 0) return RA_ERR_INVALID_ARG;
@@ -109,6 +110,15 @@ ra::FwdProblem make_problem(const void* q, const void* k, const void* v, void* o
     p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
     p.dtype = dtype;
     return p;
+}
+
+// Workspace of ra_backward: delta, float32 per query row, padded to 256
+// bytes.  -1 when the size overflows.
+int64_t backward_workspace_bytes(int B, int Hq, int64_t S, int D) {
+    (void)D;
+    const double est = 4.0 * B * Hq * (double)S + 256;
+    if (est > 4.0e18) return -1;
+    return ((4 * (int64_t)B * Hq * S) + 255) / 256 * 256;
 }
 
 }  // namespace
@@ -147,6 +157,68 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
                void* stream) {
     return ra_forward_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale, dtype,
                          RA_KERNEL_AUTO, stream);
+}
+
+int ra_backward_workspace(int B, int Hq, int64_t S, int D, int64_t* bytes) {
+    if (!bytes || B <= 0 || Hq <= 0 || S <= 0 || D <= 0) return RA_ERR_INVALID_ARG;
+    const int64_t wb = backward_workspace_bytes(B, Hq, S, D);
+    if (wb < 0) return RA_ERR_INVALID_ARG;
+    *bytes = wb;
+    return RA_OK;
+}
+
+int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
+                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                   void* workspace, int64_t workspace_bytes, int B, int Hq, int Hkv, int64_t S,
+                   int D, int N, int causal, int striped, float scale, int dtype, int kernel,
+                   void* stream) {
+    int rc = validate_forward(q, k, v, out, nullptr, B, Hq, Hkv, S, D, N, dtype, striped);
+    if (rc) return rc;
+    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
+    if (kernel != RA_KERNEL_AUTO && kernel != RA_KERNEL_TC && kernel != RA_KERNEL_SIMT)
+        return RA_ERR_INVALID_ARG;
+    if (D > 128) return RA_ERR_UNSUPPORTED;
+    if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv) || !aligned16(workspace))
+        return RA_ERR_ALIGN;
+    const int64_t need = backward_workspace_bytes(B, Hq, S, D);
+    if (need < 0) return RA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return RA_ERR_CAPACITY;
+    unsigned int* status = nullptr;
+    int sms = 0;
+    if ((rc = device_state(&status, &sms))) return rc;
+    ra::BwdProblem p;
+    p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse; p.dout = dout;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.delta = static_cast<float*>(workspace);
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.N = N;
+    p.causal = causal ? 1 : 0;
+    p.striped = striped;
+    p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
+    p.dtype = dtype;
+    const bool tc_ok = ra::tc_bwd_supported(p);
+    if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = ra::launch_bwd_delta(p, st))) {
+        if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+        return rc;
+    }
+    if (kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok)) {
+        unsigned int* work = nullptr;
+        if ((rc = work_slot(&work))) return rc;
+        rc = ra::launch_bwd_tc(p, status, work, sms, st);
+    } else
+        rc = ra::launch_bwd_simt(p, st);
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
+int ra_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                int64_t workspace_bytes, int B, int Hq, int Hkv, int64_t S, int D, int N,
+                int causal, int striped, float scale, int dtype, void* stream) {
+    return ra_backward_ex(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, Hq,
+                          Hkv, S, D, N, causal, striped, scale, dtype, RA_KERNEL_AUTO, stream);
 }
 
 int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
@@ -276,6 +348,31 @@ int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, 
             }
             ++n;
         }
+    }
+    *n_items = n;
+    return (items && n > cap) ? RA_ERR_CAPACITY : RA_OK;
+}
+
+int ra_plan_backward(int64_t S, int N, int causal, int striped, int tile, int j, int kt,
+                     int32_t* items, int64_t cap, int64_t* n_items) {
+    if (!n_items || S <= 0 || N <= 0 || tile < 2 || S % N) return RA_ERR_INVALID_ARG;
+    if (striped < RA_LAYOUT_CONTIGUOUS || striped > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
+    const int64_t Sb = S / N;
+    if (striped == RA_LAYOUT_ZIGZAG && Sb % (2 * tile)) return RA_ERR_INVALID_ARG;
+    const int64_t nt = (Sb + tile - 1) / tile;
+    if (nt > 0x7fffffff || j < 0 || j >= N || kt < 0 || kt >= nt) return RA_ERR_INVALID_ARG;
+    ra::RingGeom g{N, (int)nt, causal ? 1 : 0, striped};
+    int64_t n = 0;
+    ra::KeyWalk w;
+    for (w.start(g, j, kt, 1); !w.done(g); w.next(g, j, kt, 1)) {
+        if (items && n < cap) {
+            int32_t* e = items + n * 4;
+            e[0] = w.s;
+            e[1] = w.i;
+            e[2] = w.qt;
+            e[3] = ra::fold_kind(g, w.i, j, w.qt, kt);
+        }
+        ++n;
     }
     *n_items = n;
     return (items && n > cap) ? RA_ERR_CAPACITY : RA_OK;

@@ -41,6 +41,8 @@
 #include "ptx.cuh"
 #include "ra.h"
 #include "schedule.cuh"
+#include "tmap.h"
+#include "waits.cuh"
 
 namespace ra {
 namespace tc {
@@ -95,30 +97,6 @@ struct Params {
     unsigned int* work;  // item counter, zero at launch: CTAs take items in order
     long long timeout_cycles;  // self test only: limit of every bounded wait
 };
-
-__device__ __forceinline__ bool wait_bar(uint32_t b, uint32_t parity, volatile int* abort_flag,
-                                         unsigned int* status, long long limit) {
-    if (mbar_try_wait(b, parity)) return true;
-    const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(b, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > limit) {
-                *abort_flag = 1;
-                atomicOr(status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-// Short bounded wait used only while draining after an abort.
-__device__ __forceinline__ void drain_wait(uint32_t b, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(b, parity)) {
-        if (clock64() - t0 > kDrainCycles) return;
-    }
-}
 
 template <int D, bool LOG, bool SELFTEST>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -245,10 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 // let every copy that may still be in flight land before exit
-                if (q_loads > 0) drain_wait(bar(C::bQFull), (q_loads - 1) & 1);
+                if (q_loads > 0) drain_wait(bar(C::bQFull), (q_loads - 1) & 1, kDrainCycles);
                 const uint32_t first = kv_pos > (uint32_t)C::kStages ? kv_pos - C::kStages : 0;
                 for (uint32_t pos = first; pos < kv_pos; ++pos)
-                    drain_wait(bar(C::bKVFull + pos % C::kStages), (pos / C::kStages) & 1);
+                    drain_wait(bar(C::bKVFull + pos % C::kStages), (pos / C::kStages) & 1, kDrainCycles);
             }
         }
     } else if (warp == 1 || warp == 3) {
@@ -370,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {
                 *abort_flag = 1;
                 umma_commit(bar(C::bDrain + t));
-                drain_wait(bar(C::bDrain + t), 0);
+                drain_wait(bar(C::bDrain + t), 0, kDrainCycles);
             }
         }
     } else if (warp < 4) {
@@ -590,38 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn get_encode() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void* f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
-// rows x D bf16 row-major, box of 128 rows x 64 columns, 128-byte swizzle
-static bool encode_rows(CUtensorMap* m, const void* ptr, int64_t rows, int D) {
-    EncodeTiledFn enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)kT};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, bool LOG>
 static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* status,
                        unsigned int* work, int sm_count, cudaStream_t stream,
@@ -629,8 +575,8 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv;
     const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
-    if (!encode_rows(&mq, pr.q, q_rows, D) || !encode_rows(&mk, pr.k, kv_rows, D) ||
-        !encode_rows(&mv, pr.v, kv_rows, D))
+    if (!encode_rows_bf16(&mq, pr.q, q_rows, D) || !encode_rows_bf16(&mk, pr.k, kv_rows, D) ||
+        !encode_rows_bf16(&mv, pr.v, kv_rows, D))
         return RA_ERR_CUDA;
     Params P;
     const int Sb = (int)(pr.S / pr.N);

@@ -1,0 +1,917 @@
+// Tensor-core (tcgen05) ring-attention backward for sm_103a: bf16 in, fp32
+// accumulate, head dimension 128.
+//
+// The gradients are the chain rule of the forward; the pages give training as
+// the method's use (the Italian aiunderstanding.org page, "Implementazione nel
+// mondo reale": 1M-token LLM training; the glossary page: end-to-end training
+// throughput) without writing the backward out.  With P = exp(scale q.k - lse)
+// and delta = dO.O per query row:
+//   dS = P (dO.v - delta),  dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+// The work is split between two persistent kernels so that neither needs
+// atomics and the results do not depend on scheduling:
+//  * dq_kernel: one 128-row query tile per work item, folding the key/value
+//    tiles of the forward's fold list in ring order (dQ of shard i stays on
+//    device i, like the forward's output).  Per key tile: S = Q K^T and
+//    dP = dO V^T (SS MMAs into TMEM); the softmax warps form dS in registers
+//    and write it (bf16) over S; dQ += dS K (A from TMEM, K read MN-major).
+//  * dkv_kernel: one 128-row key tile per work item.  Its dK and dV
+//    accumulators travel with the block: it visits the query shards
+//    i = (j + s) mod N, s = 0..N-1, and in each the query tiles that see it,
+//    for every query head of its GQA group.  Per query tile: S^T = K Q^T and
+//    dP^T = V dO^T; P^T and dS^T (bf16) are written over them; dV += P^T dO
+//    and dK += dS^T Q (A from TMEM, dO and Q read MN-major).
+// Both kernels recompute S and dP, so a tile pair costs 7 tile GEMMs where a
+// single kernel reducing dQ across key tiles would cost 5.
+//
+// Both use one CTA per SM (384 threads): warp 0 lane 0 issues TMA copies,
+// warp 1 lane 0 issues MMAs, warp 2 owns TMEM, warp 3 (dkv only) stages the
+// per-row lse and delta of each query tile, and warps 4-11 are two
+// warpgroups that split the 128 columns of each score tile.  Every mbarrier
+// wait is bounded; on time-out a kernel records kStatusTimeout, drains its
+// in-flight copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "ra.h"
+#include "schedule.cuh"
+#include "tmap.h"
+#include "waits.cuh"
+
+namespace ra {
+namespace tcb {
+
+constexpr int kT = 128;                    // query and key tile rows
+constexpr int kD = 128;                    // head dimension
+constexpr int kBoxBytes = kT * 128;        // 128 rows x 64 bf16 columns (128-byte swizzle)
+constexpr int kTileBytes = kT * kD * 2;    // two boxes
+constexpr int kThreads = 384;
+constexpr long long kTimeoutCycles = 4000000000ll;
+constexpr long long kDrainCycles = 400000000ll;
+// 384 threads launched at 168 registers; warps 0-3 drop to 80, the two
+// softmax warpgroups rise to 208: 128*80 + 256*208 = 63488 <= 64512.
+constexpr uint32_t kRegsOther = 80, kRegsSoftmax = 208;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// D (+)= A B^T for two K-major 128 x 128 bf16 tiles in smem (8 K-steps of 16).
+__device__ __forceinline__ void mma_nt(uint32_t d_tm, uint32_t a_smem, uint32_t b_smem,
+                                       bool acc) {
+    constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
+    const uint64_t da = make_sdesc(a_smem, 16, 1024, kLayoutSW128);
+    const uint64_t db = make_sdesc(b_smem, 16, 1024, kLayoutSW128);
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off16 = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+        umma_ss(d_tm, da + off16, db + off16, idesc, (acc || kk > 0) ? 1u : 0u);
+    }
+}
+
+// D (+)= A B: A is 128 x 128 bf16 in TMEM (two values per column), B a
+// row-major 128 x 128 tile in smem read MN-major (8 K-steps of 16 rows).
+__device__ __forceinline__ void mma_tn(uint32_t d_tm, uint32_t a_tm, uint32_t b_smem, bool acc) {
+    constexpr uint32_t idesc = make_idesc_bf16(128, kD, false, true);
+    const uint64_t db = make_sdesc(b_smem, kBoxBytes, 1024, kLayoutSW128);
+#pragma unroll
+    for (int kk = 0; kk < kT / 16; ++kk)
+        umma_ts(d_tm, a_tm + kk * 8, db + (uint64_t)((kk * 2048) >> 4), idesc,
+                (acc || kk > 0) ? 1u : 0u);
+}
+
+struct Params {
+    TileGeom G;
+    int64_t S;
+    int Sb;
+    int rem;      // rows of each shard's last tile
+    float sl2;    // scale * log2(e)
+    float scale;
+    const float* lse;
+    const float* delta;
+    __nv_bfloat16* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    unsigned int* status;
+    unsigned int* work;
+};
+
+// ============================================================== dq kernel
+namespace dqk {
+// K tiles are read by S(n) and, a tile later, by dQ(n): three stages keep the
+// next load in flight; V tiles are read only by dP(n): two stages.
+constexpr int kKStages = 3, kVStages = 2;
+constexpr int kQOff = 0, kDOOff = kTileBytes, kKOff = 2 * kTileBytes;
+constexpr int kVOff = kKOff + kKStages * kTileBytes;
+constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+enum {
+    bQFull = 0, bQEmpty, bKFull, bKEmpty = bKFull + kKStages, bVFull = bKEmpty + kKStages,
+    bVEmpty = bVFull + kVStages, bSdpFull = bVEmpty + kVStages, bSRead, bDsFull,
+    bDqFull = bDsFull + 2, bDqEmpty, bDrain, bItemFull, bItemEmpty = bItemFull + 2,
+    kNumBars = bItemEmpty + 2
+};
+constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 32 + 1024;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColDP = 256, kColDQ = 384;
+constexpr uint32_t kItemReaders = 9;  // the MMA issuer and eight softmax warps
+}  // namespace dqk
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const Params p) {
+    using namespace dqk;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kBarOff + kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile long long* item_slot = reinterpret_cast<volatile long long*>(tmem_slot + 2);  // [2]
+    auto bar = [&](int idx) -> uint32_t { return base + kBarOff + idx * 8; };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const TileGeom& G = p.G;
+    const int nt = G.rg.nt;
+
+    if (tid == 0) {
+        mbar_init(bar(bQFull), 1);
+        mbar_init(bar(bQEmpty), 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(bar(bKFull + s), 1);
+            mbar_init(bar(bKEmpty + s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(bar(bVFull + s), 1);
+            mbar_init(bar(bVEmpty + s), 1);
+        }
+        mbar_init(bar(bSdpFull), 1);
+        mbar_init(bar(bSRead), 8);
+        mbar_init(bar(bDsFull + 0), 8);
+        mbar_init(bar(bDsFull + 1), 8);
+        mbar_init(bar(bDqFull), 1);
+        mbar_init(bar(bDqEmpty), 8);
+        mbar_init(bar(bDrain), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(bItemFull + t), 1);
+            mbar_init(bar(bItemEmpty + t), kItemReaders);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto read_item = [&](int k, bool& ok) -> long long {
+        ok = wait_bar(bar(bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, kTimeoutCycles);
+        return ok ? item_slot[k & 1] : G.n_items;
+    };
+    auto walk_item = [&](const QTile& t) {
+        Item it;
+        it.b = t.b; it.kvh = t.kvh; it.i = t.i;
+        it.h[0] = it.h[1] = t.h;
+        it.qt[0] = it.qt[1] = t.qt;
+        it.valid1 = 0;
+        return it;
+    };
+
+    if (warp < 4) regs_dec<kRegsOther>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_q = policy_evict_first();
+            const uint64_t pol_kv = policy_evict_last();
+            uint32_t tiles = 0, q_loads = 0;  // key tiles loaded (K and V ring positions)
+            int k = 0;
+            bool ok = true;
+            auto publish = [&](int kk, long long v) -> bool {
+                if (kk >= 2 && !wait_bar(bar(bItemEmpty + (kk & 1)), ((kk >> 1) - 1) & 1,
+                                         abort_flag, p.status, kTimeoutCycles))
+                    return false;
+                item_slot[kk & 1] = v;
+                mbar_arrive(bar(bItemFull + (kk & 1)));
+                return true;
+            };
+            long long item = (long long)atomicAdd(p.work, 1u);
+            ok = publish(0, item);
+            for (; ok && item < G.n_items; ++k) {
+                const long long next = (long long)atomicAdd(p.work, 1u);
+                if (!(ok = publish(k + 1, next))) break;
+                const QTile t = decode_qtile(G, item);
+                const Item it = walk_item(t);
+                item = next;
+                if (k > 0 && !(ok = wait_bar(bar(bQEmpty), (k - 1) & 1, abort_flag, p.status,
+                                             kTimeoutCycles)))
+                    break;
+                mbar_arrive_expect_tx(bar(bQFull), 2 * kTileBytes);
+                ++q_loads;
+                const int qrow = (int)((int64_t)(t.b * G.Hq + t.h) * p.S + (int64_t)t.i * p.Sb +
+                                       (int64_t)t.qt * kT);
+                for (int bx = 0; bx < 2; ++bx) {
+                    tma_load_2d(base + kQOff + bx * kBoxBytes, &tm_q, bx * 64, qrow, bar(bQFull),
+                                pol_q);
+                    tma_load_2d(base + kDOOff + bx * kBoxBytes, &tm_do, bx * 64, qrow,
+                                bar(bQFull), pol_q);
+                }
+                const int64_t kvrow0 = (int64_t)(t.b * G.Hkv + t.kvh) * p.S;
+                TileWalk w;
+                for (w.start(G.rg, it); !w.done(G.rg) && ok; w.next(G.rg, it), ++tiles) {
+                    const int row = (int)(kvrow0 + (int64_t)w.j * p.Sb + (int64_t)w.kt * kT);
+                    const uint32_t sk = tiles % kKStages, uk = tiles / kKStages;
+                    if (uk > 0 && !(ok = wait_bar(bar(bKEmpty + sk), (uk - 1) & 1, abort_flag,
+                                                  p.status, kTimeoutCycles)))
+                        break;
+                    mbar_arrive_expect_tx(bar(bKFull + sk), kTileBytes);
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_2d(base + kKOff + sk * kTileBytes + bx * kBoxBytes, &tm_k,
+                                    bx * 64, row, bar(bKFull + sk), pol_kv);
+                    const uint32_t sv = tiles % kVStages, uv = tiles / kVStages;
+                    if (uv > 0 && !(ok = wait_bar(bar(bVEmpty + sv), (uv - 1) & 1, abort_flag,
+                                                  p.status, kTimeoutCycles))) {
+                        ++tiles;  // K of this tile is in flight
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(bVFull + sv), kTileBytes);
+                    for (int bx = 0; bx < 2; ++bx)
+                        tma_load_2d(base + kVOff + sv * kTileBytes + bx * kBoxBytes, &tm_v,
+                                    bx * 64, row, bar(bVFull + sv), pol_kv);
+                }
+            }
+            if (!ok) {
+                // let every copy that may still be in flight land before exit
+                if (q_loads > 0) drain_wait(bar(bQFull), (q_loads - 1) & 1, kDrainCycles);
+                for (uint32_t pos = tiles > (uint32_t)kKStages ? tiles - kKStages : 0; pos < tiles;
+                     ++pos)
+                    drain_wait(bar(bKFull + pos % kKStages), (pos / kKStages) & 1, kDrainCycles);
+                for (uint32_t pos = tiles > (uint32_t)kVStages ? tiles - kVStages : 0; pos < tiles;
+                     ++pos)
+                    drain_wait(bar(bVFull + pos % kVStages), (pos / kVStages) & 1, kDrainCycles);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // Per key tile n: S(n) into S[n&1], dP(n) into DP, then dQ += dS(n-1) K(n-1)
+        // once the softmax has written dS(n-1) over S[(n-1)&1].
+        if (lane == 0) {
+            uint32_t g = 0;  // key tiles issued so far (ring positions of K and V)
+            int k = 0;
+            bool ok = true;
+            auto sbuf = [&](uint32_t gg) { return tmem + ((gg & 1) ? kColS1 : kColS0); };
+            auto issue_dq = [&](uint32_t n, int kk) -> bool {
+                // dq of tile g-1: needs its dS and, for the item's first, a drained DQ
+                if (!wait_bar(bar(bDsFull + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag,
+                              p.status, kTimeoutCycles))
+                    return false;
+                if (n == 1 && kk > 0 &&
+                    !wait_bar(bar(bDqEmpty), (kk - 1) & 1, abort_flag, p.status, kTimeoutCycles))
+                    return false;
+                tc_fence_after();
+                const uint32_t sk = (g - 1) % kKStages;
+                mma_tn(tmem + kColDQ, sbuf(g - 1), base + kKOff + sk * kTileBytes, n > 1);
+                umma_commit(bar(bKEmpty + sk));
+                return true;
+            };
+            for (;; ++k) {
+                const long long item = read_item(k, ok);
+                if (ok) mbar_arrive(bar(bItemEmpty + (k & 1)));
+                if (!ok || item >= G.n_items) break;
+                const Item it = walk_item(decode_qtile(G, item));
+                if (!(ok = wait_bar(bar(bQFull), k & 1, abort_flag, p.status, kTimeoutCycles)))
+                    break;
+                TileWalk w;
+                uint32_t n = 0;
+                for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n) {
+                    const uint32_t sk = g % kKStages, sv = g % kVStages;
+                    if (!(ok = wait_bar(bar(bKFull + sk), (g / kKStages) & 1, abort_flag,
+                                        p.status, kTimeoutCycles)))
+                        break;
+                    tc_fence_after();
+                    mma_nt(sbuf(g), base + kQOff, base + kKOff + sk * kTileBytes, false);
+                    if (!(ok = wait_bar(bar(bVFull + sv), (g / kVStages) & 1, abort_flag,
+                                        p.status, kTimeoutCycles)))
+                        break;
+                    if (g > 0 && !(ok = wait_bar(bar(bSRead), (g - 1) & 1, abort_flag, p.status,
+                                                 kTimeoutCycles)))
+                        break;
+                    tc_fence_after();
+                    mma_nt(tmem + kColDP, base + kDOOff, base + kVOff + sv * kTileBytes, false);
+                    umma_commit(bar(bSdpFull));
+                    umma_commit(bar(bVEmpty + sv));
+                    if (n > 0 && !(ok = issue_dq(n, k))) break;
+                    ++g;
+                }
+                if (!ok) break;
+                umma_commit(bar(bQEmpty));  // every MMA reading this item's Q and dO is issued
+                if (!(ok = issue_dq(n, k))) break;
+                umma_commit(bar(bDqFull));
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                umma_commit(bar(bDrain));
+                drain_wait(bar(bDrain), 0, kDrainCycles);
+            }
+        }
+    } else if (warp < 4) {
+        // warp 2 owns TMEM; warp 3 is idle in this kernel
+    } else {
+        // ------------------------------------------------------------ softmax
+        regs_inc<kRegsSoftmax>();
+        const int wg = (warp - 4) >> 2;        // key columns [64 wg, 64 wg + 64)
+        const int r = (warp & 3) * 32 + lane;  // query row of the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int c0 = 64 * wg;
+        const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
+        uint32_t g = 0;
+        int k = 0;
+        bool ok = true;
+        for (;; ++k) {
+            const long long item = read_item(k, ok);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bItemEmpty + (k & 1)));
+            if (item >= G.n_items) break;
+            const QTile t = decode_qtile(G, item);
+            const Item it = walk_item(t);
+            const int64_t row = (int64_t)(t.b * G.Hq + t.h) * p.S + (int64_t)t.i * p.Sb +
+                                (int64_t)t.qt * kT + r;
+            const bool row_ok = t.qt < nt - 1 || r < p.rem;
+            const float nl2 = row_ok ? -p.lse[row] * kLog2e : 0.f;
+            const float dl = row_ok ? p.delta[row] : 0.f;
+            const uint64_t nl2x2 = f2_pack(nl2, nl2), ndl2 = f2_pack(-dl, -dl);
+            TileWalk w;
+            for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++g) {
+                const int kind = fold_kind(G.rg, t.i, w.j, t.qt, w.kt);
+                ok = wait_bar(bar(bSdpFull), g & 1, abort_flag, p.status, kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sb = tmem + lane_off + ((g & 1) ? kColS1 : kColS0);
+                uint32_t sr[2][32], dp[2][32];
+                tmem_ld32(sb + c0, sr[0]);
+                tmem_ld32(sb + c0 + 32, sr[1]);
+                tmem_ld32(tmem + lane_off + kColDP + c0, dp[0]);
+                tmem_ld32(tmem + lane_off + kColDP + c0 + 32, dp[1]);
+                tmem_wait_ld();
+                reg_fence(sr[0]);
+                reg_fence(sr[1]);
+                reg_fence(dp[0]);
+                reg_fence(dp[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bSRead));
+                // visible iff key column <= lim
+                int lim = (kind == kIncl) ? r : (kind == kStrict) ? r - 1 : kT - 1;
+                if (w.kt == nt - 1 && p.rem - 1 < lim) lim = p.rem - 1;
+                if (!row_ok || kind == kNone) lim = -1;
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int c = c0 + cc * 32 + e;
+                        float a0, a1;
+                        f2_unpack(f2_fma(f2_pack_u(sr[cc][e], sr[cc][e + 1]), sl2x2, nl2x2), a0, a1);
+                        const float p0 = (c <= lim) ? ex2_approx(a0) : 0.f;
+                        const float p1 = (c + 1 <= lim) ? ex2_approx(a1) : 0.f;
+                        const uint64_t dd = f2_add(f2_pack_u(dp[cc][e], dp[cc][e + 1]), ndl2);
+                        float d0, d1;
+                        f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+                        pk[cc * 16 + e / 2] = pack_bf16x2(d0, d1);
+                    }
+                }
+                // both warpgroups must have read S before dS goes over it
+                ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tmem_st32(sb + 32 * wg, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bDsFull + (g & 1)));
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue
+            ok = wait_bar(bar(bDqFull), k & 1, abort_flag, p.status, kTimeoutCycles);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t sc2 = f2_pack(p.scale, p.scale);
+            uint4* drow = reinterpret_cast<uint4*>(p.dq + row * kD + c0);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + kColDQ + c0 + cc * 32, o);
+                tmem_wait_ld();
+                reg_fence(o);
+                uint32_t pkd[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float lo, hi;
+                    f2_unpack(f2_mul(f2_pack_u(o[e], o[e + 1]), sc2), lo, hi);
+                    pkd[e / 2] = pack_bf16x2(lo, hi);
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        drow[cc * 4 + e] =
+                            make_uint4(pkd[4 * e], pkd[4 * e + 1], pkd[4 * e + 2], pkd[4 * e + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bDqEmpty));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ============================================================== dk/dv kernel
+namespace dkv {
+constexpr int kQStages = 2, kDOStages = 2;
+constexpr int kKOff = 0, kVOff = kTileBytes, kQOff = 2 * kTileBytes;
+constexpr int kDOOff = kQOff + kQStages * kTileBytes;
+constexpr int kVecOff = kDOOff + kDOStages * kTileBytes;  // per stage: -lse*log2e[128], delta[128]
+constexpr int kVecBytes = 2 * kT * 4;
+constexpr int kBarOff = kVecOff + 2 * kVecBytes;
+enum {
+    bKVFull = 0, bKVEmpty, bQFull, bQEmpty = bQFull + kQStages, bDOFull = bQEmpty + kQStages,
+    bDOEmpty = bDOFull + kDOStages, bVecFull = bDOEmpty + kDOStages, bVecEmpty = bVecFull + 2,
+    bSFull = bVecEmpty + 2, bSRead, bPFull, bDPFull, bDPRead, bDsFull, bAccFull, bAccEmpty,
+    bDrain, bItemFull, bItemEmpty = bItemFull + 2, kNumBars = bItemEmpty + 2
+};
+constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 32 + 1024;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+// readers of a published item: the MMA issuer, the row-vector warp, eight softmax warps
+constexpr uint32_t kItemReaders = 10;
+}  // namespace dkv
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const Params p) {
+    using namespace dkv;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    float* vec = reinterpret_cast<float*>(gbase + kVecOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kBarOff + kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile long long* item_slot = reinterpret_cast<volatile long long*>(tmem_slot + 2);  // [2]
+    auto bar = [&](int idx) -> uint32_t { return base + kBarOff + idx * 8; };
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const TileGeom& G = p.G;
+    const int nt = G.rg.nt, heads = G.g;
+
+    if (tid == 0) {
+        mbar_init(bar(bKVFull), 1);
+        mbar_init(bar(bKVEmpty), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(bQFull + s), 1);
+            mbar_init(bar(bQEmpty + s), 1);
+            mbar_init(bar(bDOFull + s), 1);
+            mbar_init(bar(bDOEmpty + s), 1);
+            mbar_init(bar(bVecFull + s), 32);
+            mbar_init(bar(bVecEmpty + s), 8);
+        }
+        mbar_init(bar(bSFull), 1);
+        mbar_init(bar(bSRead), 8);
+        mbar_init(bar(bPFull), 8);
+        mbar_init(bar(bDPFull), 1);
+        mbar_init(bar(bDPRead), 8);
+        mbar_init(bar(bDsFull), 8);
+        mbar_init(bar(bAccFull), 1);
+        mbar_init(bar(bAccEmpty), 8);
+        mbar_init(bar(bDrain), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(bItemFull + t), 1);
+            mbar_init(bar(bItemEmpty + t), kItemReaders);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto read_item = [&](int k, bool& ok) -> long long {
+        ok = wait_bar(bar(bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, kTimeoutCycles);
+        return ok ? item_slot[k & 1] : G.n_items;
+    };
+    // first row of query tile (head kvh*g + gi, shard i, tile qt)
+    auto qrow0 = [&](const KTile& t, const KeyWalk& w) -> int64_t {
+        return (int64_t)(t.b * G.Hq + t.kvh * heads + w.gi) * p.S + (int64_t)w.i * p.Sb +
+               (int64_t)w.qt * kT;
+    };
+
+    if (warp < 4) regs_dec<kRegsOther>();
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_q = policy_evict_last();
+            const uint64_t pol_kv = policy_evict_first();
+            uint32_t g = 0, kv_loads = 0;
+            int k = 0;
+            bool ok = true;
+            auto publish = [&](int kk, long long v) -> bool {
+                if (kk >= 2 && !wait_bar(bar(bItemEmpty + (kk & 1)), ((kk >> 1) - 1) & 1,
+                                         abort_flag, p.status, kTimeoutCycles))
+                    return false;
+                item_slot[kk & 1] = v;
+                mbar_arrive(bar(bItemFull + (kk & 1)));
+                return true;
+            };
+            auto load_ring = [&](int full, int empty, uint32_t off, const CUtensorMap* tm,
+                                 int row) -> bool {
+                const uint32_t st = g & 1, use = g >> 1;
+                if (use > 0 && !wait_bar(bar(empty + st), (use - 1) & 1, abort_flag, p.status,
+                                         kTimeoutCycles))
+                    return false;
+                mbar_arrive_expect_tx(bar(full + st), kTileBytes);
+                for (int bx = 0; bx < 2; ++bx)
+                    tma_load_2d(base + off + st * kTileBytes + bx * kBoxBytes, tm, bx * 64, row,
+                                bar(full + st), pol_q);
+                return true;
+            };
+            uint32_t q_issued = 0, do_issued = 0;
+            long long item = (long long)atomicAdd(p.work, 1u);
+            ok = publish(0, item);
+            for (; ok && item < G.n_items; ++k) {
+                const long long next = (long long)atomicAdd(p.work, 1u);
+                if (!(ok = publish(k + 1, next))) break;
+                const KTile t = decode_ktile(G, item);
+                item = next;
+                if (k > 0 && !(ok = wait_bar(bar(bKVEmpty), (k - 1) & 1, abort_flag, p.status,
+                                             kTimeoutCycles)))
+                    break;
+                mbar_arrive_expect_tx(bar(bKVFull), 2 * kTileBytes);
+                ++kv_loads;
+                const int krow = (int)((int64_t)(t.b * G.Hkv + t.kvh) * p.S +
+                                       (int64_t)t.j * p.Sb + (int64_t)t.kt * kT);
+                for (int bx = 0; bx < 2; ++bx) {
+                    tma_load_2d(base + kKOff + bx * kBoxBytes, &tm_k, bx * 64, krow, bar(bKVFull),
+                                pol_kv);
+                    tma_load_2d(base + kVOff + bx * kBoxBytes, &tm_v, bx * 64, krow, bar(bKVFull),
+                                pol_kv);
+                }
+                KeyWalk w;
+                for (w.start(G.rg, t.j, t.kt, heads); !w.done(G.rg);
+                     w.next(G.rg, t.j, t.kt, heads), ++g) {
+                    const int row = (int)qrow0(t, w);
+                    if (!(ok = load_ring(bQFull, bQEmpty, kQOff, &tm_q, row))) break;
+                    q_issued = g + 1;
+                    if (!(ok = load_ring(bDOFull, bDOEmpty, kDOOff, &tm_do, row))) break;
+                    do_issued = g + 1;
+                }
+            }
+            if (!ok) {
+                // let every copy that may still be in flight land before exit
+                if (kv_loads > 0) drain_wait(bar(bKVFull), (kv_loads - 1) & 1, kDrainCycles);
+                for (uint32_t x = q_issued > 2 ? q_issued - 2 : 0; x < q_issued; ++x)
+                    drain_wait(bar(bQFull + (x & 1)), (x >> 1) & 1, kDrainCycles);
+                for (uint32_t x = do_issued > 2 ? do_issued - 2 : 0; x < do_issued; ++x)
+                    drain_wait(bar(bDOFull + (x & 1)), (x >> 1) & 1, kDrainCycles);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // Pipe order: S(0) dP(0) | dV(n) S(n+1) dK(n) dP(n+1) | ... so that the
+        // softmax of tile n+1 overlaps dK(n) and dV(n+1) overlaps its dS part.
+        if (lane == 0) {
+            uint32_t g = 0;
+            int k = 0;
+            bool ok = true;
+            auto issue_s = [&](uint32_t gg) -> bool {
+                if (!wait_bar(bar(bQFull + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status,
+                              kTimeoutCycles))
+                    return false;
+                tc_fence_after();
+                mma_nt(tmem + kColS, base + kKOff, base + kQOff + (gg & 1) * kTileBytes, false);
+                umma_commit(bar(bSFull));
+                return true;
+            };
+            auto issue_dp = [&](uint32_t gg) -> bool {
+                if (!wait_bar(bar(bDOFull + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status,
+                              kTimeoutCycles))
+                    return false;
+                tc_fence_after();
+                mma_nt(tmem + kColDP, base + kVOff, base + kDOOff + (gg & 1) * kTileBytes, false);
+                umma_commit(bar(bDPFull));
+                return true;
+            };
+            for (;; ++k) {
+                const long long item = read_item(k, ok);
+                if (ok) mbar_arrive(bar(bItemEmpty + (k & 1)));
+                if (!ok || item >= G.n_items) break;
+                const KTile t = decode_ktile(G, item);
+                if (!(ok = wait_bar(bar(bKVFull), k & 1, abort_flag, p.status, kTimeoutCycles)))
+                    break;
+                KeyWalk w;
+                w.start(G.rg, t.j, t.kt, heads);
+                if (!(ok = issue_s(g)) || !(ok = issue_dp(g))) break;
+                for (uint32_t n = 0; !w.done(G.rg); ++n, ++g) {
+                    KeyWalk nx = w;
+                    nx.next(G.rg, t.j, t.kt, heads);
+                    const bool more = !nx.done(G.rg);
+                    if (!(ok = wait_bar(bar(bPFull), g & 1, abort_flag, p.status, kTimeoutCycles)))
+                        break;
+                    if (n == 0 && k > 0 &&
+                        !(ok = wait_bar(bar(bAccEmpty), (k - 1) & 1, abort_flag, p.status,
+                                        kTimeoutCycles)))
+                        break;
+                    tc_fence_after();
+                    mma_tn(tmem + kColDV, tmem + kColS, base + kDOOff + (g & 1) * kTileBytes, n > 0);
+                    umma_commit(bar(bDOEmpty + (g & 1)));
+                    if (more && !(ok = issue_s(g + 1))) break;
+                    if (!(ok = wait_bar(bar(bDsFull), g & 1, abort_flag, p.status, kTimeoutCycles)))
+                        break;
+                    tc_fence_after();
+                    mma_tn(tmem + kColDK, tmem + kColDP, base + kQOff + (g & 1) * kTileBytes, n > 0);
+                    umma_commit(bar(bQEmpty + (g & 1)));
+                    if (more && !(ok = issue_dp(g + 1))) break;
+                    w = nx;
+                }
+                if (!ok) break;
+                umma_commit(bar(bKVEmpty));
+                umma_commit(bar(bAccFull));
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                umma_commit(bar(bDrain));
+                drain_wait(bar(bDrain), 0, kDrainCycles);
+            }
+        }
+    } else if (warp == 2) {
+        // TMEM owner
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ row vectors
+        // -lse * log2(e) and delta of the 128 query rows of each tile, into a
+        // two-stage ring that the softmax warps read.
+        uint32_t g = 0;
+        int k = 0;
+        bool ok = true;
+        for (;; ++k) {
+            const long long item = read_item(k, ok);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bItemEmpty + (k & 1)));
+            if (item >= G.n_items) break;
+            const KTile t = decode_ktile(G, item);
+            KeyWalk w;
+            for (w.start(G.rg, t.j, t.kt, heads); !w.done(G.rg);
+                 w.next(G.rg, t.j, t.kt, heads), ++g) {
+                const uint32_t st = g & 1, use = g >> 1;
+                ok = use == 0 || wait_bar(bar(bVecEmpty + st), (use - 1) & 1, abort_flag, p.status,
+                                          kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                const int64_t row0 = qrow0(t, w);
+                float* vs = vec + st * (2 * kT);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int l = lane + 32 * m;
+                    const bool valid = w.qt < nt - 1 || l < p.rem;
+                    vs[l] = valid ? -p.lse[row0 + l] * kLog2e : 0.f;
+                    vs[kT + l] = valid ? p.delta[row0 + l] : 0.f;
+                }
+                mbar_arrive(bar(bVecFull + st));
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        regs_inc<kRegsSoftmax>();
+        const int wg = (warp - 4) >> 2;        // query columns [64 wg, 64 wg + 64)
+        const int c = (warp & 3) * 32 + lane;  // key row of the tile == TMEM lane
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int q0 = 64 * wg;
+        const uint64_t sl2x2 = f2_pack(p.sl2, p.sl2);
+        uint32_t g = 0;
+        int k = 0;
+        bool ok = true;
+        for (;; ++k) {
+            const long long item = read_item(k, ok);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bItemEmpty + (k & 1)));
+            if (item >= G.n_items) break;
+            const KTile t = decode_ktile(G, item);
+            const bool key_ok = t.kt < nt - 1 || c < p.rem;
+            KeyWalk w;
+            for (w.start(G.rg, t.j, t.kt, heads); !w.done(G.rg);
+                 w.next(G.rg, t.j, t.kt, heads), ++g) {
+                const int kind = fold_kind(G.rg, w.i, t.j, w.qt, t.kt);
+                // pair (query column q, key row c) visible iff lo <= q < hi
+                int lo = (kind == kIncl) ? c : (kind == kStrict) ? c + 1 : 0;
+                const int hi = (w.qt == nt - 1) ? p.rem : kT;
+                if (!key_ok || kind == kNone) lo = kT;
+                const float* vs = vec + (g & 1) * (2 * kT);
+                // ---- P^T = exp2(S^T scale log2e - lse log2e), over S^T
+                ok = wait_bar(bar(bSFull), g & 1, abort_flag, p.status, kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t sr[2][32];
+                tmem_ld32(tmem + lane_off + kColS + q0, sr[0]);
+                tmem_ld32(tmem + lane_off + kColS + q0 + 32, sr[1]);
+                tmem_wait_ld();
+                reg_fence(sr[0]);
+                reg_fence(sr[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bSRead));
+                ok = wait_bar(bar(bVecFull + (g & 1)), (g >> 1) & 1, abort_flag, p.status,
+                              kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                float pf[2][32];
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int q = q0 + cc * 32 + e;
+                        float a0, a1;
+                        f2_unpack(f2_fma(f2_pack_u(sr[cc][e], sr[cc][e + 1]), sl2x2,
+                                         f2_pack(vs[q], vs[q + 1])),
+                                  a0, a1);
+                        pf[cc][e] = (q >= lo && q < hi) ? ex2_approx(a0) : 0.f;
+                        pf[cc][e + 1] = (q + 1 >= lo && q + 1 < hi) ? ex2_approx(a1) : 0.f;
+                        pk[cc * 16 + e / 2] = pack_bf16x2(pf[cc][e], pf[cc][e + 1]);
+                    }
+                }
+                ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tmem_st32(tmem + lane_off + kColS + 32 * wg, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bPFull));
+                // ---- dS^T = P^T (dP^T - delta), over dP^T
+                ok = wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tc_fence_after();
+                uint32_t dp[2][32];
+                tmem_ld32(tmem + lane_off + kColDP + q0, dp[0]);
+                tmem_ld32(tmem + lane_off + kColDP + q0 + 32, dp[1]);
+                tmem_wait_ld();
+                reg_fence(dp[0]);
+                reg_fence(dp[1]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bDPRead));
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int q = q0 + cc * 32 + e;
+                        const uint64_t dd = f2_add(f2_pack_u(dp[cc][e], dp[cc][e + 1]),
+                                                   f2_pack(-vs[kT + q], -vs[kT + q + 1]));
+                        float d0, d1;
+                        f2_unpack(f2_mul(f2_pack(pf[cc][e], pf[cc][e + 1]), dd), d0, d1);
+                        pk[cc * 16 + e / 2] = pack_bf16x2(d0, d1);
+                    }
+                }
+                ok = wait_bar(bar(bDPRead), g & 1, abort_flag, p.status, kTimeoutCycles);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                tmem_st32(tmem + lane_off + kColDP + 32 * wg, pk);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(bDsFull));
+                    mbar_arrive(bar(bVecEmpty + (g & 1)));
+                }
+            }
+            if (!ok) break;
+            // ---------------------------------------------------------- epilogue
+            ok = wait_bar(bar(bAccFull), k & 1, abort_flag, p.status, kTimeoutCycles);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            const int64_t krow = (int64_t)(t.b * G.Hkv + t.kvh) * p.S + (int64_t)t.j * p.Sb +
+                                 (int64_t)t.kt * kT + c;
+            const uint64_t sc2 = f2_pack(p.scale, p.scale), one2 = f2_pack(1.f, 1.f);
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {  // dV, then dK (times scale)
+                const uint32_t col = which ? kColDK : kColDV;
+                const uint64_t mul = which ? sc2 : one2;
+                uint4* drow = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + krow * kD + q0);
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + col + q0 + cc * 32, o);
+                    tmem_wait_ld();
+                    reg_fence(o);
+                    uint32_t pkd[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float lo2, hi2;
+                        f2_unpack(f2_mul(f2_pack_u(o[e], o[e + 1]), mul), lo2, hi2);
+                        pkd[e / 2] = pack_bf16x2(lo2, hi2);
+                    }
+                    if (key_ok) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            drow[cc * 4 + e] = make_uint4(pkd[4 * e], pkd[4 * e + 1],
+                                                          pkd[4 * e + 2], pkd[4 * e + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bAccEmpty));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+// kernel 0: dq_kernel over query tiles; kernel 1: dkv_kernel over key tiles
+static int launch_one(const BwdProblem& pr, int which, unsigned int* status, unsigned int* work,
+                      int sm_count, cudaStream_t stream) {
+    CUtensorMap mq, mdo, mk, mv;
+    const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
+    if (!encode_rows_bf16(&mq, pr.q, q_rows, kD) || !encode_rows_bf16(&mdo, pr.dout, q_rows, kD) ||
+        !encode_rows_bf16(&mk, pr.k, kv_rows, kD) || !encode_rows_bf16(&mv, pr.v, kv_rows, kD))
+        return RA_ERR_CUDA;
+    Params P;
+    const int Sb = (int)(pr.S / pr.N);
+    const int nt = (Sb + kT - 1) / kT;
+    P.G = make_tile_geom(pr.B, pr.Hq, pr.Hkv, pr.N, nt, pr.causal, pr.striped, which == 1);
+    P.S = pr.S;
+    P.Sb = Sb;
+    P.rem = Sb - (nt - 1) * kT;
+    P.sl2 = (float)((double)pr.scale * 1.4426950408889634);
+    P.scale = pr.scale;
+    P.lse = pr.lse;
+    P.delta = pr.delta;
+    P.dq = static_cast<__nv_bfloat16*>(pr.dq);
+    P.dk = static_cast<__nv_bfloat16*>(pr.dk);
+    P.dv = static_cast<__nv_bfloat16*>(pr.dv);
+    P.status = status;
+    P.work = work;
+    if (P.G.n_items <= 0) return RA_OK;
+    if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
+    auto kern = which ? dkv_kernel : dq_kernel;
+    const int smem = which ? dkv::kSmemBytes : dqk::kSmemBytes;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return RA_ERR_CUDA;
+    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
+    kern<<<(unsigned)grid, kThreads, smem, stream>>>(mq, mdo, mk, mv, P);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+}  // namespace tcb
+
+bool tc_bwd_supported(const BwdProblem& p) {
+    if (p.dtype != RA_BF16 || p.D != tcb::kD) return false;
+    if (p.S % p.N) return false;
+    const int64_t Sb = p.S / p.N;
+    if (p.striped == kZigzag && Sb % (2 * tcb::kT)) return false;
+    if (Sb > (1ll << 30)) return false;
+    if ((int64_t)p.B * p.Hq * p.S >= (1ll << 31) || (int64_t)p.B * p.Hkv * p.S >= (1ll << 31))
+        return false;
+    return true;
+}
+
+int launch_bwd_tc(const BwdProblem& p, unsigned int* status, unsigned int* work, int sm_count,
+                  cudaStream_t stream) {
+    if (!tc_bwd_supported(p)) return RA_ERR_UNSUPPORTED;
+    if (!work) return RA_ERR_INVALID_ARG;
+    // both kernels take items from the same counter, zeroed before each launch
+    int rc = tcb::launch_one(p, 0, status, work, sm_count, stream);
+    if (rc) return rc;
+    return tcb::launch_one(p, 1, status, work, sm_count, stream);
+}
+
+}  // namespace ra

@@ -1,5 +1,5 @@
 // Ring fold schedule and persistent work decomposition, shared by the host
-// planner (ra_plan) and the kernels.
+// planners (ra_plan, ra_plan_backward) and the kernels.
 //
 // Ring schedule ("Ring Attention" glossary page, "Como funciona a atencao em
 // anel"): query shard i folds key/value shard j = (i - s) mod N at step s.
@@ -69,6 +69,146 @@ RA_HD int fold_kind(const RingGeom& g, int i, int j, int qt, int kt) {
     if (kt >= nk) return kNone;
     return (kt == qt && dk != kNone) ? dk : kFull;
 }
+
+// Query tiles of shard i that see key tile kt of shard j: qt in [*q_lo, *q_hi).
+// The transpose of shard_span: for every (i, j, qt, kt), qt lies in the range
+// exactly when fold_kind(g, i, j, qt, kt) != kNone.
+RA_HD void key_span(const RingGeom& g, int i, int j, int kt, int* q_lo, int* q_hi) {
+    *q_lo = 0;
+    *q_hi = g.nt;
+    if (!g.causal) return;
+    if (g.striped == kContiguous) {
+        if (j == i) *q_lo = kt;
+        else if (j > i) *q_hi = 0;
+        return;
+    }
+    if (g.striped == kStriped) {
+        *q_lo = kt;
+        return;
+    }
+    const int h = g.nt / 2;  // zigzag
+    if (j == i) *q_lo = kt;
+    else if (j < i) { if (kt >= h) *q_hi = 0; }
+    else *q_lo = h;
+}
+
+// Work items of the backward kernels, one 128-row tile each, numbered group
+// major ((b, kv head) outer) and, inside a group, longest work first.
+//  * query tiles (dq kernel): the fold list of (i, qt); within a group,
+//    index lam * W + w with lam the cost level (as for the forward) and w the
+//    query head and shard;
+//  * key tiles (dk/dv kernel): the transposed list of (j, kt), visited by
+//    every query head of the group.  Cost of (j, kt) in live query tiles:
+//    non-causal and striped N*nt resp. N*(nt - kt) (order kt, then j);
+//    contiguous (N-1-j)*nt + nt - kt (order j, then kt); zigzag (h = nt/2)
+//    N*nt - (j*h + kt) for kt < h, then j*h + nt - kt for kt >= h.
+struct TileGeom {
+    RingGeom rg;
+    int B, Hq, Hkv, g;
+    long long per_group;  // items per (b, kv head)
+    long long n_items;
+};
+
+RA_HD TileGeom make_tile_geom(int B, int Hq, int Hkv, int N, int nt, int causal, int striped,
+                              bool key_tiles) {
+    TileGeom G;
+    G.rg.N = N; G.rg.nt = nt; G.rg.causal = causal; G.rg.striped = striped;
+    G.B = B; G.Hq = Hq; G.Hkv = Hkv; G.g = Hq / Hkv;
+    G.per_group = (long long)N * nt * (key_tiles ? 1 : G.g);
+    G.n_items = (long long)B * Hkv * G.per_group;
+    return G;
+}
+
+struct QTile {
+    int b, kvh, h, i, qt;
+};
+
+RA_HD QTile decode_qtile(const TileGeom& G, long long item) {
+    QTile t;
+    const long long grp = item / G.per_group, rem = item % G.per_group;
+    t.b = (int)(grp / G.Hkv);
+    t.kvh = (int)(grp % G.Hkv);
+    const int N = G.rg.N, nt = G.rg.nt;
+    if (G.rg.causal && G.rg.striped == kContiguous) {
+        const int lam = (int)(rem / G.g), w = (int)(rem % G.g);
+        const int gt = N * nt - 1 - lam;
+        t.i = gt / nt;
+        t.qt = gt % nt;
+        t.h = t.kvh * G.g + w;
+    } else {
+        const int W = N * G.g;
+        const int lam = (int)(rem / W), w = (int)(rem % W);
+        t.qt = nt - 1 - lam;
+        t.i = w / G.g;
+        t.h = t.kvh * G.g + w % G.g;
+    }
+    return t;
+}
+
+struct KTile {
+    int b, kvh, j, kt;
+};
+
+RA_HD KTile decode_ktile(const TileGeom& G, long long item) {
+    KTile t;
+    const long long grp = item / G.per_group;
+    const int e = (int)(item % G.per_group);
+    t.b = (int)(grp / G.Hkv);
+    t.kvh = (int)(grp % G.Hkv);
+    const int N = G.rg.N, nt = G.rg.nt;
+    if (G.rg.causal && G.rg.striped == kContiguous) {
+        t.j = e / nt;
+        t.kt = e % nt;
+    } else if (G.rg.causal && G.rg.striped == kZigzag) {
+        const int h = nt / 2;
+        if (e < N * h) {
+            t.j = e / h;
+            t.kt = e % h;
+        } else {
+            const int e2 = e - N * h;
+            t.j = N - 1 - e2 / h;
+            t.kt = h + e2 % h;
+        }
+    } else {
+        t.kt = e / N;
+        t.j = e % N;
+    }
+    return t;
+}
+
+// Visiting order of the dk/dv kernel for key tile kt of shard j: ring steps
+// s ascending (query shard i = (j + s) mod N, where the block is at step s),
+// then the query heads of the GQA group (gi < heads), then the query tiles
+// that see the key tile, ascending.  Steps with no such tile are skipped.
+struct KeyWalk {
+    int s, i, gi, qt, q_lo, q_hi;
+    RA_HD void start(const RingGeom& g, int j, int kt, int heads) {
+        s = -1;
+        advance_shard(g, j, kt);
+        (void)heads;
+    }
+    RA_HD void advance_shard(const RingGeom& g, int j, int kt) {
+        for (;;) {
+            ++s;
+            if (s >= g.N) return;
+            i = j + s;
+            if (i >= g.N) i -= g.N;
+            key_span(g, i, j, kt, &q_lo, &q_hi);
+            if (q_lo < q_hi) {
+                gi = 0;
+                qt = q_lo;
+                return;
+            }
+        }
+    }
+    RA_HD bool done(const RingGeom& g) const { return s >= g.N; }
+    RA_HD void next(const RingGeom& g, int j, int kt, int heads) {
+        if (++qt < q_hi) return;
+        qt = q_lo;
+        if (++gi < heads) return;
+        advance_shard(g, j, kt);
+    }
+};
 
 // Persistent work items of the tensor-core kernel.  An item is two 128-row
 // query tiles ("slots") that share every key/value tile they stream:

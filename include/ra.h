@@ -203,15 +203,34 @@ int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, 
             int64_t cap, int64_t* n_items);
 
 /*
+ * ra_plan_backward (host only, no GPU): the visiting order of one key tile in
+ * the backward's dk/dv pass.  For key tile kt of shard j (rows
+ * [kt*tile, (kt+1)*tile) of the shard), writes n_items entries of 4 int32,
+ * (s, i, qt, kind): ring steps s ascending, where the block (and the
+ * gradient accumulators travelling with it) is at query shard
+ * i = (j + s) mod N; then the query tiles qt of shard i that hold at least
+ * one (query, key) pair the mask leaves visible, ascending; kind as in
+ * ra_plan for the pair (query tile qt of shard i, key tile kt of shard j).
+ * Every query head of the GQA group is visited with the same list (heads
+ * between the step and the query tiles).  Each pair appears exactly once
+ * across the key tiles, as in ra_plan.
+ *   items: int32[cap][4] or NULL.  Same size rules as ra_plan.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_CAPACITY (*n_items is still set).
+ */
+int ra_plan_backward(int64_t S, int N, int causal, int striped, int tile, int j, int kt,
+                     int32_t* items, int64_t cap, int64_t* n_items);
+
+/*
  * ra_fold_log: run the tensor-core kernel in its logging variant and record
  * the order in which each query tile was folded.
  *   Same tensor arguments as ra_forward (bf16 only).
- *   log: device int32 buffer of B*Hq*S/128 * max_entries * 4 entries.  For the
- *        query tile (b, h, i, qt), at index ((b*Hq + h)*N + i)*(Sb/128) + qt,
- *        entry n is (s, j, kt, kind) of its n-th live fold; unused entries are
- *        left as written by the caller.
- *   counts: device int32[B*Hq*S/128]: number of live folds recorded per tile.
- *   max_entries >= N * Sb / 128.
+ *   log: device int32 buffer of B*Hq*N*nt * max_entries * 4 entries, with
+ *        nt = ceil(Sb/128) query tiles per shard.  For the query tile
+ *        (b, h, i, qt), at index ((b*Hq + h)*N + i)*nt + qt, entry n is
+ *        (s, j, kt, kind) of its n-th live fold; unused entries are left as
+ *        written by the caller.
+ *   counts: device int32[B*Hq*N*nt]: number of live folds recorded per tile.
+ *   max_entries >= N * nt.
  * The logging variant computes the same outputs as ra_forward.
  * Errors: as ra_forward, plus RA_ERR_UNSUPPORTED outside the tensor-core
  * kernel's envelope.
@@ -236,6 +255,58 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
 int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out, float* lse,
                          int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped,
                          float scale, int64_t timeout_cycles, void* stream);
+
+/*
+ * ra_backward: gradients of ra_forward with respect to q, k and v.
+ *   q, k, v [shapes of ra_forward] (read): the forward's inputs.
+ *   out [B, Hq, S, D] (read), lse [B, Hq, S] float32 (read, not NULL): the
+ *       forward's outputs for these inputs.
+ *   dout [B, Hq, S, D] (read): dL/dout.
+ *   dq [B, Hq, S, D], dk [B, Hkv, S, D], dv [B, Hkv, S, D] (written): dL/dq,
+ *       dL/dk, dL/dv in the same dtype and shard-major layout as the inputs.
+ *   workspace (device, caller-owned, 16-byte aligned, read and written):
+ *       workspace_bytes >= the size ra_backward_workspace reports for the
+ *       shape.  Holds the per-row terms delta; nothing in it outlives the
+ *       call.
+ * The pages name training as the use of the method (1M-token LLM training;
+ * end-to-end training throughput under Striped Attention; PyTorch's
+ * context_parallel replacing scaled dot-product attention when training)
+ * but do not write the backward out.  It is the chain rule of the forward's
+ * definition.  For query row t, visible key u, P_tu = exp(scale q_t.k_u -
+ * lse_t):
+ *   delta_t = dout_t . out_t
+ *   dv_u = sum_t P_tu dout_t          dS_tu = P_tu (dout_t . v_u - delta_t)
+ *   dq_t = scale sum_u dS_tu k_u      dk_u = scale sum_t dS_tu q_t
+ * and a key/value head's gradient sums over the query heads that read it.
+ * The fold follows the forward's ring: dq of query shard i accumulates over
+ * key/value shards j = (i - s) mod N, and the accumulators of dk and dv of
+ * shard j travel with it, visiting query shards i = (j + s) mod N, s =
+ * 0..N-1.  Shards and tiles without a visible pair are skipped.
+ * Kernels: the tcgen05 tensor-core backward for bf16, D = 128 (any Sb for
+ * contiguous and striped shards, Sb % 256 == 0 for zigzag), else the fp32
+ * SIMT backward (f32 or bf16, D <= 128).  ra_backward_ex chooses explicitly.
+ * Neither uses atomics: for fixed inputs the gradients are the same bits on
+ * every call.
+ * Errors: as ra_forward; RA_ERR_CAPACITY when workspace_bytes is too small;
+ * RA_ERR_UNSUPPORTED for D > 128.
+ */
+int ra_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                int64_t workspace_bytes, int B, int Hq, int Hkv, int64_t S, int D, int N,
+                int causal, int striped, float scale, int dtype, void* stream);
+
+/* ra_backward with an explicit kernel choice (RA_KERNEL_*).  RA_KERNEL_TC
+ * returns RA_ERR_UNSUPPORTED outside its envelope. */
+int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
+                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                   void* workspace, int64_t workspace_bytes, int B, int Hq, int Hkv, int64_t S,
+                   int D, int N, int causal, int striped, float scale, int dtype, int kernel,
+                   void* stream);
+
+/* ra_backward_workspace (host only): bytes of workspace ra_backward needs for
+ * the shape: 4*B*Hq*S for delta, rounded up to 256 (D does not enter).
+ * Errors: RA_ERR_INVALID_ARG (non-positive sizes or a null bytes pointer). */
+int ra_backward_workspace(int B, int Hq, int64_t S, int D, int64_t* bytes);
 
 /*
  * ra_check: synchronise `stream`, then read and clear this device's status

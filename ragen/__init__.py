@@ -23,7 +23,7 @@ import subprocess
 
 import numpy as np
 
-from .workloads import WORKLOADS, Workload, TENSOR_Q, TENSOR_K, TENSOR_V  # noqa: F401
+from .workloads import WORKLOADS, Workload, TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_DO  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ragen.c")

@@ -1,7 +1,8 @@
 """The named attention workloads and their input recipe.
 
 Every workload draws q, k and v i.i.d. N(0, 1) from ``ragen`` with
-seed = 1000 * workload index and tensor ids 0 (q), 1 (k), 2 (v); bf16
+seed = 1000 * workload index and tensor ids 0 (q), 1 (k), 2 (v); the backward
+draws dL/dout the same way with tensor id 3, shaped like q; bf16
 workloads round each sample to bfloat16 (nearest even).  Tensors are laid out
 shard-major: q is [B, Hq, S, D], k and v are [B, Hkv, S, D], and virtual
 device i of N owns rows [i*S/N, (i+1)*S/N) of every (b, h) slice.  Under the
@@ -11,7 +12,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-TENSOR_Q, TENSOR_K, TENSOR_V = 0, 1, 2
+TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_DO = 0, 1, 2, 3
 
 
 @dataclass(frozen=True)

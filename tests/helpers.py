@@ -17,6 +17,29 @@ TOL = {"f32": dict(max_abs=1e-5, mean_abs=1e-5, lse=1e-4),
        "bf16": dict(max_abs=2e-2, mean_abs=2e-3, lse=2e-3)}
 
 
+# Gradient tolerance, per tensor (dq, dk or dv) against the float64 oracle:
+#   every row:  |got_row - ref_row| <= row_rtol |ref_row| + row_atol median_row|ref|
+#                                      + floor
+#   the tensor: |got - ref|_F       <= fro * |ref|_F
+# fp32: the SIMT kernel's fp32 sums of up to S terms, about 1e-6 relative.
+# bf16: each output element is rounded once (2^-9 relative) and the
+# tensor-core kernel also rounds P and dS to bf16 before its products, another
+# 2^-9 per term with random sign, so a row's relative error stays near 2^-8;
+# the bounds give that a factor 4 (normwise 2^-7) to 8 (per row 2^-5).  The
+# median term covers rows whose exact gradient vanishes (the first causal
+# row's dq is exactly zero); the floor covers a tensor whose rows all vanish
+# (one token), where what is left is the rounding of dP - delta, about
+# eps |dout| |v| scale |k| (1e-6 in fp32 at these sizes).  A key tile missing
+# from or doubled in the fold moves the rows it feeds by well over 2^-5 at the
+# tested sizes.
+# On top of this, every row of dq and dk gets the effect of delta_t = dO_t.O_t
+# being formed from the stored output (rounded to the output dtype) rather
+# than the exact one; where a row's weights concentrate on one key,
+# dP - delta cancels and this term dominates (see ``delta_error_bounds``).
+TOL_BWD = {"f32": dict(row_rtol=1e-4, row_atol=1e-5, floor=1e-5, fro=1e-5),
+           "bf16": dict(row_rtol=2.0 ** -5, row_atol=2.0 ** -7, floor=1e-3, fro=2.0 ** -7)}
+
+
 def gen(seed, shape, dtype, tensor_id):
     n = int(np.prod(shape))
     if dtype == "bf16":
@@ -121,3 +144,81 @@ def sampled_reference(seed, wl_shapes, rows, causal, striped, N, scale=None):
             out_o[idxs[sl]] = o
             out_l[idxs[sl]] = l
     return out_o, out_l
+
+
+def grad_inputs(seed, B, Hq, S, D, dtype):
+    """dL/dout for the backward tests: N(0, 1) with tensor id TENSOR_DO."""
+    return gen(seed, (B, Hq, S, D), dtype, ragen.TENSOR_DO)
+
+
+def backward_reference(q, k, v, dout, N, causal, layout, dtype, scale=None):
+    """Oracle dq, dk, dv for shard-major inputs, returned shard-major (float64),
+    from the plain gradient definition on token-order tensors."""
+    qf, kf, vf, gf = (oracle.to_token_order(to_f64(x, dtype), N, layout) for x in (q, k, v, dout))
+    grads = oracle.attention_backward(qf, kf, vf, gf, causal, scale)
+    return tuple(oracle.to_shard_major(g, N, layout) for g in grads)
+
+
+def delta_error_bounds(q, k, v, dout, N, causal, layout, dtype, scale=None, lam=8.0):
+    """Per-row bounds (shard-major [B, H, S]) on how far dq and dk move when
+    delta_t = dO_t . O_t uses the stored output instead of the exact one.
+
+    The stored output differs from the exact O by its rounding to the output
+    dtype (at most u |O_td|, u = 2^-9 for bf16 and 2^-24 for fp32) and by the
+    forward's rounding of each weight P_tu to that dtype before the P.V
+    product (sum_u e_u P_tu v_ud with |e_u| <= u).  These are sums of
+    independent roundings of random sign, so their size is taken as lam
+    standard deviations of such a sum (the probabilistic rounding-error
+    analysis of Higham and Mary, SIAM J. Sci. Comput. 2019), lam = 8:
+        |d delta_t| <= lam u sqrt(sum_d dout_td^2 (O_td^2 + sum_u P_tu^2 v_ud^2)).
+    Since dS_tu = P_tu (dP_tu - delta_t), a change of delta_t moves
+        dq_t by exactly scale d delta_t sum_u P_tu k_u,
+        dk_u by scale sum_t P_tu d delta_t q_t, whose terms have independent
+             signs: scale sqrt(sum_t (P_tu |d delta_t| |q_t|)^2);
+    dv does not involve delta.  O, lse and P come from the oracle."""
+    u = 2.0 ** -9 if dtype == "bf16" else 2.0 ** -24
+    qf, kf, vf, gf = (oracle.to_token_order(to_f64(x, dtype), N, layout) for x in (q, k, v, dout))
+    B, Hq, S, D = qf.shape
+    g = Hq // kf.shape[1]
+    sc = 1.0 / math.sqrt(D) if not scale else scale
+    o, lse = oracle.full_attention(qf, kf, vf, causal, scale)
+    bq = np.zeros((B, Hq, S))
+    bk2 = np.zeros((B, kf.shape[1], S))
+    pos = np.arange(S)
+    for b in range(B):
+        for h in range(Hq):
+            K, V = kf[b, h // g], vf[b, h // g]
+            for r0 in range(0, S, 256):
+                r1 = min(S, r0 + 256)
+                s = (qf[b, h, r0:r1] @ K.T) * sc - lse[b, h, r0:r1, None]
+                if causal:
+                    s = np.where(pos[None, :] <= pos[r0:r1, None], s, -np.inf)
+                P = np.exp(s)
+                var_o = o[b, h, r0:r1] ** 2 + (P ** 2) @ (V ** 2)
+                dd = lam * u * np.sqrt((gf[b, h, r0:r1] ** 2 * var_o).sum(axis=1))
+                bq[b, h, r0:r1] = sc * dd * np.linalg.norm(P @ K, axis=1)
+                w = dd * np.linalg.norm(qf[b, h, r0:r1], axis=1)
+                bk2[b, h // g] += ((sc * P * w[:, None]) ** 2).sum(axis=0)
+    to_sm = lambda x: oracle.to_shard_major(x[..., None], N, layout)[..., 0]
+    return to_sm(bq), to_sm(np.sqrt(bk2))
+
+
+def assert_grad_close(got, ref, dtype, what="", extra=None):
+    """The row-wise and normwise gradient bounds of TOL_BWD, plus ``extra``
+    (per row, e.g. from ``delta_error_bounds``) when given."""
+    tol = TOL_BWD[dtype]
+    got = np.asarray(got, np.float64).reshape(-1, ref.shape[-1])
+    ref = np.asarray(ref, np.float64).reshape(-1, ref.shape[-1])
+    ext = np.zeros(len(ref)) if extra is None else np.asarray(extra, np.float64).reshape(-1)
+    assert np.isfinite(got).all(), f"{what}: non-finite gradient"
+    err = np.linalg.norm(got - ref, axis=1)
+    nrm = np.linalg.norm(ref, axis=1)
+    bound = tol["row_rtol"] * nrm + tol["row_atol"] * float(np.median(nrm)) + tol["floor"] + ext
+    worst = int(np.argmax(err - bound))
+    assert (err <= bound).all(), \
+        f"{what}: row {worst} error {err[worst]:.3e} > bound {bound[worst]:.3e} (|ref| {nrm[worst]:.3e})"
+    total = float(np.linalg.norm(got - ref))
+    fro = total / max(float(np.linalg.norm(ref)), 1e-300)
+    assert total <= tol["fro"] * float(np.linalg.norm(ref)) + float(np.linalg.norm(ext)) + \
+        tol["floor"], f"{what}: normwise error {fro:.3e} > {tol['fro']:.3e}"
+    return fro, float((err / np.maximum(nrm, 1e-300)).max())

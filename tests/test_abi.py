@@ -127,3 +127,50 @@ def test_plan_with_a_partial_last_tile(lib, causal, striped, S, N, T):
         for qt in range(nt):
             assert ra.plan(S, N, causal, striped, i, qt, tile=T) == by_tile.get((i, qt), []), \
                 (i, qt)
+
+
+def test_backward_host_validation(lib):
+    """ra_backward refuses bad arguments on the host (no device needed)."""
+    n = ctypes.c_int64()
+    assert lib.ra_backward_workspace(2, 4, 1000, 128, ctypes.byref(n)) == ra.RA_OK
+    assert n.value == 32000  # delta: 4 bytes for each of 2*4*1000 rows, already 256-aligned
+    assert lib.ra_backward_workspace(1, 1, 10, 8, ctypes.byref(n)) == ra.RA_OK and n.value == 256
+    assert lib.ra_backward_workspace(0, 4, 1000, 128, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert lib.ra_backward_workspace(1, 1, 10, 8, None) == ra.RA_ERR_INVALID_ARG
+    p = ctypes.c_void_p(16 * 1024)  # never dereferenced: validation fails first
+
+    def call(D=64, ws=1 << 30, nulls=(), kernel=ra.RA_KERNEL_AUTO, S=256):
+        a = [p] * 10
+        for i in nulls:
+            a[i] = None
+        return ra.ra_backward_ex(*a, ws, 1, 2, 1, S, D, 2, 1, 1, 0.0, ra.RA_BF16, kernel, None)
+
+    assert call(nulls=(4,)) == ra.RA_ERR_INVALID_ARG      # lse
+    assert call(nulls=(9,)) == ra.RA_ERR_INVALID_ARG      # workspace
+    assert call(nulls=(6,)) == ra.RA_ERR_INVALID_ARG      # dq
+    assert call(D=192) == ra.RA_ERR_UNSUPPORTED
+    assert call(ws=100) == ra.RA_ERR_CAPACITY
+    assert call(kernel=9) == ra.RA_ERR_INVALID_ARG
+    assert call(S=255) == ra.RA_ERR_INVALID_ARG           # S % N
+
+
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True),
+                                            (True, 2)])
+@pytest.mark.parametrize("S,N,T", [(512, 4, 32), (768, 3, 64), (256, 1, 128), (1024, 8, 16),
+                                   (600, 3, 64), (130, 1, 16)])
+def test_plan_backward_equals_transposed_bruteforce(lib, causal, striped, S, N, T):
+    """Bit-exact: the dk/dv visiting order of every key tile is the oracle's
+    brute-force schedule read by key tile, steps ascending (the block is at
+    query shard i = (j + s) mod N at step s), then query tiles ascending."""
+    if striped == 2 and (S // N) % (2 * T):
+        pytest.skip("zigzag needs whole-tile chunks")
+    ref = oracle.fold_schedule(S, N, causal, striped, T, T)
+    by_key = {}
+    for (i, qt, s, j, kt, kind) in ref:
+        assert (i - j) % N == s
+        by_key.setdefault((j, kt), []).append((s, i, qt, kind))
+    nt = -(-(S // N) // T)
+    for j in range(N):
+        for kt in range(nt):
+            want = sorted(by_key.get((j, kt), []))
+            assert ra.plan_backward(S, N, causal, striped, j, kt, tile=T) == want, (j, kt)
