@@ -49,10 +49,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", default="forward",
-                    choices=["forward", "merge", "stripe", "f32", "ulysses"],
-                    help="forward: the ring-attention step (default); merge / stripe: the "
-                         "HBM-bound helpers on the workload's output / query tensors; f32: the "
-                         "fp32 SIMT path on the workload")
+                    choices=["forward", "backward", "merge", "stripe", "f32", "ulysses"],
+                    help="forward: the ring-attention step (default); backward: ra_backward "
+                         "(dq, dk, dv) on the workload; merge / stripe: the HBM-bound helpers "
+                         "on the workload's output / query tensors; f32: the fp32 SIMT path on "
+                         "the workload")
     return ap.parse_args()
 
 
@@ -351,6 +352,86 @@ def aux_arm(args, wl):
         print(json.dumps(line), flush=True)
     return 0
 
+def backward_arm(args, wl):
+    """Times ra_backward (delta, then the dq and dk/dv kernels) on the
+    workload.  FLOPs follow the usual convention of 2.5 times the forward's
+    (five tile GEMMs per visible tile pair against the forward's two); the
+    two-kernel design executes seven, which the line also reports."""
+    import torch
+    import ragen
+    import exact_long_context_order_b300 as ra
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    ra.lib()
+    if wl.dtype != "bf16":
+        raise SystemExit("the backward bench runs bf16 workloads")
+    qs, kvs = wl.shapes()
+    dev = []
+    for tid, shape in ((ragen.TENSOR_Q, qs), (ragen.TENSOR_K, kvs), (ragen.TENSOR_V, kvs),
+                       (ragen.TENSOR_DO, qs)):
+        h = torch.empty(shape, dtype=torch.int16, pin_memory=True)
+        ragen.normal_bf16(wl.seed, tid, h.numel(), out=h.numpy().reshape(-1).view(np.uint16))
+        dev.append(h.to("cuda").view(torch.bfloat16))
+    q, k, v, dout = dev
+    stream = torch.cuda.current_stream()
+    out, lse = ra.forward(q, k, v, wl.N, causal=wl.causal, striped=wl.striped, stream=stream)
+    rc, need = ra.ra_backward_workspace(wl.B, wl.Hq, wl.S, wl.D)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+
+    def step():
+        return ra.backward(q, k, v, out, lse, dout, wl.N, causal=wl.causal, striped=wl.striped,
+                           workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ra.check(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s_ in range(args.steps):
+        ev[s_][0].record(stream)
+        step()
+        ev[s_][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    rc = ra.ra_check(ra._stream_handle(stream))
+    if rc != ra.RA_OK:
+        raise SystemExit(f"device status after timed region: {ra.ra_strerror(rc)}")
+    ms = t0.elapsed_time(t1) / args.steps
+    call_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    flops = 2.5 * wl.flops()
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+    value = flops / (ms * 1e-3) / 1e12
+    achieved = flops / (call_ms * 1e-3) / 1e12
+    line = {
+        "metric": "attention backward TFLOP/s (bf16, causal-adj, 2.5x forward FLOPs)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(wl.describe(), op="backward", l2="inputs larger than L2 (no flush)",
+                       flops_per_step=flops, executed_gemm_flops_per_step=3.5 * wl.flops()),
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "ra_backward: delta, ra::tcb::dq_kernel, ra::tcb::dkv_kernel",
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "frac_of_sustained": achieved / peak_sus,
+                     "executed_frac": 1.4 * achieved / peak},
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------------- our arm
 def main():
     args = parse()
@@ -358,6 +439,8 @@ def main():
     wl = ragen.WORKLOADS[args.workload]
     if args.impl == "reference":
         return reference_arm(args, wl)
+    if args.op == "backward":
+        return backward_arm(args, wl)
     if args.op != "forward":
         return aux_arm(args, wl)
 

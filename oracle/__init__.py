@@ -46,5 +46,7 @@ from .attention import (  # noqa: F401
     toy_ring_no_max,
     ulysses_exchange,
     attention_backward,
+    attention_backward_rows,
+    backward_uniform_scores,
     ring_attention_backward,
 )

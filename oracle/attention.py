@@ -283,6 +283,75 @@ def attention_backward(q, k, v, dout, causal: bool, scale=None, chunk: int = 512
     return dq, dk, dv
 
 
+def attention_backward_rows(qrows, qpos, dorows, k, v, kpos, causal: bool, scale: float):
+    """dq for a set of query rows of one head, from the plain definition.
+
+    For each query row t (position qpos[t], dL/dout row dorows[t]) against
+    the keys k, v of its key/value head (positions kpos): P_t = softmax of
+    the visible scores, dP_tu = dO_t . v_u, dS_tu = P_tu (dP_tu - sum_u'
+    P_tu' dP_tu'), dq_t = scale sum_u dS_tu k_u -- the rows of
+    ``attention_backward``'s dq, for rows chosen by the caller.
+    """
+    qrows = np.asarray(qrows, np.float64)
+    dorows = np.asarray(dorows, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    s = (qrows @ k.T) * scale
+    if causal:
+        s = np.where(np.asarray(kpos)[None, :] <= np.asarray(qpos)[:, None], s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    m = np.where(np.isfinite(m), m, 0.0)
+    e = np.exp(s - m)
+    den = e.sum(axis=1, keepdims=True)
+    P = e / np.where(den > 0, den, 1.0)
+    dP = dorows @ v.T
+    dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+    return scale * (dS @ k)
+
+
+def backward_uniform_scores(q, v, dout, causal: bool, scale=None, dk_rows=None):
+    """dk and dv of the plain definition when every score is zero (K = 0),
+    token order, float64, by prefix sums.
+
+    Every query row t then weighs its n_t visible keys equally (n_t = t + 1
+    under the causal mask, S otherwise), and the definition reduces to
+        dv_u = sum over rows t that see u of dO_t / n_t
+        m_t  = dO_t . (mean of the v_u row t sees)          (= sum_u P_tu dP_tu)
+        dk_u = scale sum over rows t that see u of (dO_t . v_u - m_t) q_t / n_t
+    (dq is zero, as every k_u is).  A key/value head's gradients sum over the
+    query heads that read it.  q [B, Hq, S, D], v [B, Hkv, S, D], dout like q.
+    Returns dv [B, Hkv, S, D] and dk for the key positions in ``dk_rows``
+    ([B, Hkv, len(dk_rows), D]; all rows when None).
+    """
+    q = np.asarray(q, np.float64)
+    v = np.asarray(v, np.float64)
+    dout = np.asarray(dout, np.float64)
+    B, Hq, S, D = q.shape
+    Hkv = v.shape[1]
+    g = Hq // Hkv
+    sc = _scale(D, scale)
+    rows = np.arange(S) if dk_rows is None else np.asarray(dk_rows, np.int64)
+    n = np.arange(1, S + 1, dtype=np.float64) if causal else np.full(S, float(S))
+    dv = np.zeros((B, Hkv, S, D))
+    dk = np.zeros((B, Hkv, len(rows), D))
+    for b in range(B):
+        for h in range(Hq):
+            V, dO, Q = v[b, h // g], dout[b, h], q[b, h]
+            w = dO / n[:, None]
+            if causal:
+                dv[b, h // g] += np.cumsum(w[::-1], axis=0)[::-1]    # sum over t >= u
+                vbar = np.cumsum(V, axis=0) / n[:, None]             # mean of v_0..v_t
+            else:
+                dv[b, h // g] += w.sum(axis=0)[None, :]
+                vbar = np.broadcast_to(V.mean(axis=0), V.shape)
+            m = (dO * vbar).sum(axis=1)
+            for e, u in enumerate(rows):
+                t0 = u if causal else 0
+                c = (dO[t0:] @ V[u] - m[t0:]) / n[t0:]
+                dk[b, h // g, e] += sc * (c @ Q[t0:])
+    return dk, dv
+
+
 def ring_attention_backward(q, k, v, dout, N: int, causal: bool, striped, scale=None):
     """Backward of ``ring_attention`` folded in ring order, float64.
 

@@ -138,3 +138,40 @@ def test_ring_backward_scale_argument():
     np.testing.assert_allclose(a[0], b[0] * r, rtol=0, atol=1e-12)
     np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-12)
     np.testing.assert_allclose(a[2], b[2], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal,layout", [(False, 0), (True, 1), (True, 2)])
+def test_backward_rows_equal_the_full_gradient(causal, layout):
+    """The per-row dq (used on sampled rows at full size) equals the rows of
+    the plain gradient, rows taken in shard-major order with their token
+    positions."""
+    B, Hq, Hkv, S, D, N = 1, 2, 1, 64, 8, 4
+    q, k, v = rnd((B, Hq, S, D), 81), rnd((B, Hkv, S, D), 82), rnd((B, Hkv, S, D), 83)
+    dout = rnd((B, Hq, S, D), 84)
+    dq, _, _ = oracle.attention_backward(q, k, v, dout, causal)
+    pos = oracle.positions(S, N, layout)
+    sm = [oracle.to_shard_major(x, N, layout) for x in (q, k, v, dout)]
+    dq_sm = oracle.to_shard_major(dq, N, layout)
+    rows = [0, 5, 17, 40, 63]
+    for h in range(Hq):
+        got = oracle.attention_backward_rows(sm[0][0, h, rows], pos[rows], sm[3][0, h, rows],
+                                             sm[1][0, 0], sm[2][0, 0], pos, causal,
+                                             1 / math.sqrt(D))
+        np.testing.assert_allclose(got, dq_sm[0, h, rows], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_uniform_score_closed_form_equals_the_full_gradient(causal):
+    """With K = 0 the prefix-sum closed form (used at full size) equals the
+    plain gradient."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 50, 6
+    q, v = rnd((B, Hq, S, D), 91), rnd((B, Hkv, S, D), 92)
+    dout = rnd((B, Hq, S, D), 93)
+    k = np.zeros((B, Hkv, S, D))
+    _, dk, dv = oracle.attention_backward(q, k, v, dout, causal)
+    rows = [0, 1, 13, 49]
+    dk_cf, dv_cf = oracle.backward_uniform_scores(q, v, dout, causal, dk_rows=rows)
+    np.testing.assert_allclose(dv_cf, dv, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk_cf, dk[:, :, rows], rtol=0, atol=1e-12)
+    dk_all, _ = oracle.backward_uniform_scores(q, v, dout, causal)
+    np.testing.assert_allclose(dk_all, dk, rtol=0, atol=1e-12)
