@@ -97,23 +97,29 @@ def kernel_source_hash():
     h = hashlib.sha256()
     for rel in ("exact_long_context_order_b300/csrc/ra_tc.cu",
                 "exact_long_context_order_b300/csrc/ptx.cuh",
-                "exact_long_context_order_b300/csrc/schedule.cuh"):
+                "exact_long_context_order_b300/csrc/schedule.cuh",
+                "exact_long_context_order_b300/csrc/waits.cuh",
+                "exact_long_context_order_b300/csrc/tmap.h"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(workload_name):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"tc_fwd_{workload_name}.md")
-    if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(kernel source ([0-9a-f]+)\)", text)
-    if not m or m.group(2) != kernel_source_hash():
-        return None
-    return float(m.group(1))
+    """DRAM bytes per launch of the forward kernel on this workload, from a
+    committed ncu summary line
+        traffic_bytes_per_launch[<workload name>]: <bytes> (kernel source <hash>)
+    if one was taken on the current kernel source (else None)."""
+    pat = re.compile(r"traffic_bytes_per_launch\[([^\]]+)\]:\s*([0-9.eE+]+)\s*"
+                     r"\(kernel source ([0-9a-f]+)\)")
+    pdir = os.path.join(ROOT, "profiles")
+    for fn in sorted(os.listdir(pdir)) if os.path.isdir(pdir) else []:
+        if not fn.endswith(".md"):
+            continue
+        for m in pat.finditer(open(os.path.join(pdir, fn)).read()):
+            if m.group(1) == workload_name and m.group(3) == kernel_source_hash():
+                return float(m.group(2))
+    return None
 
 
 # ---------------------------------------------------------------- clocks
