@@ -33,7 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention TFLOP/s & tokens/s (bf16, causal-adj) at S=128K; % of BF16 tensor peak"
-KERNEL_NAME = "ra::tc::fwd_kernel<128, false>"
+KERNEL_NAME = "ra::tc::fwd_kernel<128, false, false, false>"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 

@@ -15,7 +15,7 @@
 // kernel gives each thread one key row of shard j; its accumulators travel
 // with the block like the block itself, visiting query shards
 // i = (j + s) mod N, s = 0..N-1, and within each the query heads of its GQA
-// group.  Visibility comes from token positions, as in the SIMT forward.
+// group (the tensor-core kernel enters the same cyclic order at device 0).  Visibility comes from token positions, as in the SIMT forward.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

@@ -36,6 +36,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -98,7 +99,9 @@ struct Params {
     long long timeout_cycles;  // self test only: limit of every bounded wait
 };
 
-template <int D, bool LOG, bool SELFTEST>
+// RAGGED: the shard size is not a multiple of the tile, so each shard's last
+// query and key tile is partial (compiled out of the common case).
+template <int D, bool LOG, bool SELFTEST, bool RAGGED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // visible iff col <= lim: the diagonal masks, and on a shard's
                     // last (partial) key tile the columns past the shard's end
                     int lim = (kind == kIncl) ? r : (kind == kStrict) ? r - 1 : kT - 1;
-                    if (w.kt == G.rg.nt - 1 && p.rem - 1 < lim) lim = p.rem - 1;
+                    if (RAGGED && w.kt == G.rg.nt - 1 && p.rem - 1 < lim) lim = p.rem - 1;
                     if (lim < kT - 1) {
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -520,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t row = (int64_t)(it.b * G.Hq + it.h[t]) * p.S + (int64_t)it.i * p.Sb +
                                     (int64_t)qt * kT + r;
                 // a shard's last tile may hold fewer than 128 real rows
-                const bool row_ok = qt < G.rg.nt - 1 || r < p.rem;
+                const bool row_ok = !RAGGED || qt < G.rg.nt - 1 || r < p.rem;
                 const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
                 const uint64_t inv2 = f2_pack(inv_l, inv_l);
                 uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
-template <int D, bool LOG>
+template <int D, bool LOG, bool RAGGED>
 static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* status,
                        unsigned int* work, int sm_count, cudaStream_t stream,
                        long long timeout_cycles, int withhold_first_k) {
@@ -596,7 +599,8 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     P.timeout_cycles = timeout_cycles > 0 ? timeout_cycles : kTimeoutCycles;
     if (P.G.n_items <= 0) return RA_OK;
     if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
-    auto kern = withhold_first_k ? fwd_kernel<D, false, true> : fwd_kernel<D, LOG, false>;
+    auto kern = withhold_first_k ? fwd_kernel<D, false, true, RAGGED>
+                                 : fwd_kernel<D, LOG, false, RAGGED>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return RA_ERR_CUDA;
@@ -624,15 +628,21 @@ int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, un
               int sm_count, cudaStream_t stream, long long timeout_cycles, int withhold_first_k) {
     if (!tc_supported(p)) return RA_ERR_UNSUPPORTED;
     if (!work) return RA_ERR_INVALID_ARG;
-    if (p.D == 128)
-        return flog ? tc::launch_impl<128, true>(p, flog, status, work, sm_count, stream,
-                                                 timeout_cycles, withhold_first_k)
-                    : tc::launch_impl<128, false>(p, flog, status, work, sm_count, stream,
-                                                  timeout_cycles, withhold_first_k);
-    return flog ? tc::launch_impl<64, true>(p, flog, status, work, sm_count, stream,
-                                            timeout_cycles, withhold_first_k)
-                : tc::launch_impl<64, false>(p, flog, status, work, sm_count, stream,
-                                             timeout_cycles, withhold_first_k);
+    const bool ragged = (p.S / p.N) % tc::kT != 0;
+    auto go = [&](auto d, auto lg, auto rg) {
+        return tc::launch_impl<decltype(d)::value, decltype(lg)::value, decltype(rg)::value>(
+            p, flog, status, work, sm_count, stream, timeout_cycles, withhold_first_k);
+    };
+    using T = std::true_type;
+    using F = std::false_type;
+    using D128 = std::integral_constant<int, 128>;
+    using D64 = std::integral_constant<int, 64>;
+    if (p.D == 128) {
+        if (flog) return ragged ? go(D128{}, T{}, T{}) : go(D128{}, T{}, F{});
+        return ragged ? go(D128{}, F{}, T{}) : go(D128{}, F{}, F{});
+    }
+    if (flog) return ragged ? go(D64{}, T{}, T{}) : go(D64{}, T{}, F{});
+    return ragged ? go(D64{}, F{}, T{}) : go(D64{}, F{}, F{});
 }
 
 }  // namespace ra

@@ -15,9 +15,10 @@
 //    dP = dO V^T (SS MMAs into TMEM); the softmax warps form dS in registers
 //    and write it (bf16) over S; dQ += dS K (A from TMEM, K read MN-major).
 //  * dkv_kernel: one 128-row key tile per work item.  Its dK and dV
-//    accumulators travel with the block: it visits the query shards
-//    i = (j + s) mod N, s = 0..N-1, and in each the query tiles that see it,
-//    for every query head of its GQA group.  Per query tile: S^T = K Q^T and
+//    accumulators travel with the block round the ring in its cyclic order,
+//    entering it at device 0 (query shards i = 0..N-1, so that blocks running
+//    together read the same query tiles from L2), and in each shard the
+//    query tiles that see it, for every query head of its GQA group.  Per query tile: S^T = K Q^T and
 //    dP^T = V dO^T; P^T and dS^T (bf16) are written over them; dV += P^T dO
 //    and dK += dS^T Q (A from TMEM, dO and Q read MN-major).
 // Both kernels recompute S and dP, so a tile pair costs 7 tile GEMMs where a
@@ -375,20 +376,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (w.kt == nt - 1 && p.rem - 1 < lim) lim = p.rem - 1;
                 if (!row_ok || kind == kNone) lim = -1;
                 uint32_t pk[32];
+                // dS for two columns c, c + 1 of pair index e of chunk cc
+                auto ds2 = [&](int cc, int e, float p0, float p1) {
+                    const uint64_t dd = f2_add(f2_pack_u(dp[cc][e], dp[cc][e + 1]), ndl2);
+                    float d0, d1;
+                    f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
+                    pk[cc * 16 + e / 2] = pack_bf16x2(d0, d1);
+                };
+                if (lim >= kT - 1) {  // every pair of the tile is visible
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
+                    for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int c = c0 + cc * 32 + e;
-                        float a0, a1;
-                        f2_unpack(f2_fma(f2_pack_u(sr[cc][e], sr[cc][e + 1]), sl2x2, nl2x2), a0, a1);
-                        const float p0 = (c <= lim) ? ex2_approx(a0) : 0.f;
-                        const float p1 = (c + 1 <= lim) ? ex2_approx(a1) : 0.f;
-                        const uint64_t dd = f2_add(f2_pack_u(dp[cc][e], dp[cc][e + 1]), ndl2);
-                        float d0, d1;
-                        f2_unpack(f2_mul(f2_pack(p0, p1), dd), d0, d1);
-                        pk[cc * 16 + e / 2] = pack_bf16x2(d0, d1);
-                    }
+                        for (int e = 0; e < 32; e += 2) {
+                            float a0, a1;
+                            f2_unpack(f2_fma(f2_pack_u(sr[cc][e], sr[cc][e + 1]), sl2x2, nl2x2),
+                                      a0, a1);
+                            ds2(cc, e, ex2_approx(a0), ex2_approx(a1));
+                        }
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const int c = c0 + cc * 32 + e;
+                            float a0, a1;
+                            f2_unpack(f2_fma(f2_pack_u(sr[cc][e], sr[cc][e + 1]), sl2x2, nl2x2),
+                                      a0, a1);
+                            ds2(cc, e, (c <= lim) ? ex2_approx(a0) : 0.f,
+                                (c + 1 <= lim) ? ex2_approx(a1) : 0.f);
+                        }
                 }
                 // both warpgroups must have read S before dS goes over it
                 ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, kTimeoutCycles);
@@ -749,19 +765,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 float pf[2][32];
                 uint32_t pk[32];
+                const float4* nl4 = reinterpret_cast<const float4*>(vs + q0);
+                // x = S^T scale log2e - lse log2e for four columns
+                auto exps = [&](int cc, int e, float* x) {
+                    const float4 nl = nl4[(cc * 32 + e) / 4];
+                    f2_unpack(f2_fma(f2_pack_u(sr[cc][e], sr[cc][e + 1]), sl2x2,
+                                     f2_pack(nl.x, nl.y)),
+                              x[0], x[1]);
+                    f2_unpack(f2_fma(f2_pack_u(sr[cc][e + 2], sr[cc][e + 3]), sl2x2,
+                                     f2_pack(nl.z, nl.w)),
+                              x[2], x[3]);
+                };
+                if (lo == 0 && hi == kT) {  // every pair of the tile is visible
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
+                    for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int q = q0 + cc * 32 + e;
-                        float a0, a1;
-                        f2_unpack(f2_fma(f2_pack_u(sr[cc][e], sr[cc][e + 1]), sl2x2,
-                                         f2_pack(vs[q], vs[q + 1])),
-                                  a0, a1);
-                        pf[cc][e] = (q >= lo && q < hi) ? ex2_approx(a0) : 0.f;
-                        pf[cc][e + 1] = (q + 1 >= lo && q + 1 < hi) ? ex2_approx(a1) : 0.f;
-                        pk[cc * 16 + e / 2] = pack_bf16x2(pf[cc][e], pf[cc][e + 1]);
-                    }
+                        for (int e = 0; e < 32; e += 4) {
+                            float x[4];
+                            exps(cc, e, x);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) pf[cc][e + m] = ex2_approx(x[m]);
+                            pk[cc * 16 + e / 2] = pack_bf16x2(pf[cc][e], pf[cc][e + 1]);
+                            pk[cc * 16 + e / 2 + 1] = pack_bf16x2(pf[cc][e + 2], pf[cc][e + 3]);
+                        }
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4) {
+                            float x[4];
+                            exps(cc, e, x);
+#pragma unroll
+                            for (int m = 0; m < 4; ++m) {
+                                const int q = q0 + cc * 32 + e + m;
+                                pf[cc][e + m] = (q >= lo && q < hi) ? ex2_approx(x[m]) : 0.f;
+                            }
+                            pk[cc * 16 + e / 2] = pack_bf16x2(pf[cc][e], pf[cc][e + 1]);
+                            pk[cc * 16 + e / 2 + 1] = pack_bf16x2(pf[cc][e + 2], pf[cc][e + 3]);
+                        }
                 }
                 ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, kTimeoutCycles);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -783,16 +824,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(bDPRead));
+                const float4* dl4 = reinterpret_cast<const float4*>(vs + kT + q0);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int q = q0 + cc * 32 + e;
-                        const uint64_t dd = f2_add(f2_pack_u(dp[cc][e], dp[cc][e + 1]),
-                                                   f2_pack(-vs[kT + q], -vs[kT + q + 1]));
-                        float d0, d1;
-                        f2_unpack(f2_mul(f2_pack(pf[cc][e], pf[cc][e + 1]), dd), d0, d1);
-                        pk[cc * 16 + e / 2] = pack_bf16x2(d0, d1);
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 dl = dl4[(cc * 32 + e) / 4];
+                        float d[4];
+                        f2_unpack(f2_mul(f2_pack(pf[cc][e], pf[cc][e + 1]),
+                                         f2_add(f2_pack_u(dp[cc][e], dp[cc][e + 1]),
+                                                f2_pack(-dl.x, -dl.y))),
+                                  d[0], d[1]);
+                        f2_unpack(f2_mul(f2_pack(pf[cc][e + 2], pf[cc][e + 3]),
+                                         f2_add(f2_pack_u(dp[cc][e + 2], dp[cc][e + 3]),
+                                                f2_pack(-dl.z, -dl.w))),
+                                  d[2], d[3]);
+                        pk[cc * 16 + e / 2] = pack_bf16x2(d[0], d[1]);
+                        pk[cc * 16 + e / 2 + 1] = pack_bf16x2(d[2], d[3]);
                     }
                 }
                 ok = wait_bar(bar(bDPRead), g & 1, abort_flag, p.status, kTimeoutCycles);

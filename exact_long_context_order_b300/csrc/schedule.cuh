@@ -176,23 +176,28 @@ RA_HD KTile decode_ktile(const TileGeom& G, long long item) {
     return t;
 }
 
-// Visiting order of the dk/dv kernel for key tile kt of shard j: ring steps
-// s ascending (query shard i = (j + s) mod N, where the block is at step s),
-// then the query heads of the GQA group (gi < heads), then the query tiles
-// that see the key tile, ascending.  Steps with no such tile are skipped.
+// Visiting order of the dk/dv kernel for key tile kt of shard j.  The block
+// and its gradient accumulators go round the ring in its cyclic order, but
+// every block enters it at device 0 rather than at its own device j: query
+// shards i = 0, 1, ..., N-1, where the block arrives at ring step
+// s = (i - j) mod N.  Blocks running at the same time then read the same
+// query shards while those are in L2.  Within a shard: the query heads of
+// the GQA group (gi < heads), then the query tiles that see the key tile,
+// ascending.  Shards with no such tile are skipped.
 struct KeyWalk {
     int s, i, gi, qt, q_lo, q_hi;
     RA_HD void start(const RingGeom& g, int j, int kt, int heads) {
-        s = -1;
+        i = -1;
+        s = 0;
         advance_shard(g, j, kt);
         (void)heads;
     }
     RA_HD void advance_shard(const RingGeom& g, int j, int kt) {
         for (;;) {
-            ++s;
-            if (s >= g.N) return;
-            i = j + s;
-            if (i >= g.N) i -= g.N;
+            ++i;
+            if (i >= g.N) return;
+            s = i - j;
+            if (s < 0) s += g.N;
             key_span(g, i, j, kt, &q_lo, &q_hi);
             if (q_lo < q_hi) {
                 gi = 0;
@@ -201,7 +206,7 @@ struct KeyWalk {
             }
         }
     }
-    RA_HD bool done(const RingGeom& g) const { return s >= g.N; }
+    RA_HD bool done(const RingGeom& g) const { return i >= g.N; }
     RA_HD void next(const RingGeom& g, int j, int kt, int heads) {
         if (++qt < q_hi) return;
         qt = q_lo;

@@ -206,11 +206,13 @@ int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, 
  * ra_plan_backward (host only, no GPU): the visiting order of one key tile in
  * the backward's dk/dv pass.  For key tile kt of shard j (rows
  * [kt*tile, (kt+1)*tile) of the shard), writes n_items entries of 4 int32,
- * (s, i, qt, kind): ring steps s ascending, where the block (and the
- * gradient accumulators travelling with it) is at query shard
- * i = (j + s) mod N; then the query tiles qt of shard i that hold at least
- * one (query, key) pair the mask leaves visible, ascending; kind as in
- * ra_plan for the pair (query tile qt of shard i, key tile kt of shard j).
+ * (s, i, qt, kind).  The block and the gradient accumulators travelling with
+ * it go round the ring in its cyclic order, entering it at device 0: query
+ * shards i = 0, 1, ..., N-1 ascending, s = (i - j) mod N being the ring step
+ * at which block j reaches device i; then the query tiles qt of shard i that
+ * hold at least one (query, key) pair the mask leaves visible, ascending;
+ * kind as in ra_plan for the pair (query tile qt of shard i, key tile kt of
+ * shard j).
  * Every query head of the GQA group is visited with the same list (heads
  * between the step and the query tiles).  Each pair appears exactly once
  * across the key tiles, as in ra_plan.
@@ -278,10 +280,11 @@ int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out,
  *   dv_u = sum_t P_tu dout_t          dS_tu = P_tu (dout_t . v_u - delta_t)
  *   dq_t = scale sum_u dS_tu k_u      dk_u = scale sum_t dS_tu q_t
  * and a key/value head's gradient sums over the query heads that read it.
- * The fold follows the forward's ring: dq of query shard i accumulates over
- * key/value shards j = (i - s) mod N, and the accumulators of dk and dv of
- * shard j travel with it, visiting query shards i = (j + s) mod N, s =
- * 0..N-1.  Shards and tiles without a visible pair are skipped.
+ * The fold follows the ring: dq of query shard i accumulates over key/value
+ * shards j = (i - s) mod N in the forward's order, and the accumulators of
+ * dk and dv of shard j travel with the block round the ring in its cyclic
+ * order, entering it at device 0 (ra_plan_backward lists the order).
+ * Shards and tiles without a visible pair are skipped.
  * Kernels: the tcgen05 tensor-core backward for bf16, D = 128 (any Sb for
  * contiguous and striped shards, Sb % 256 == 0 for zigzag), else the fp32
  * SIMT backward (f32 or bf16, D <= 128).  ra_backward_ex chooses explicitly.

@@ -160,8 +160,9 @@ def test_backward_host_validation(lib):
                                    (600, 3, 64), (130, 1, 16)])
 def test_plan_backward_equals_transposed_bruteforce(lib, causal, striped, S, N, T):
     """Bit-exact: the dk/dv visiting order of every key tile is the oracle's
-    brute-force schedule read by key tile, steps ascending (the block is at
-    query shard i = (j + s) mod N at step s), then query tiles ascending."""
+    brute-force schedule read by key tile: query shards ascending (the block
+    goes round the ring entering at device 0, reaching shard i at step
+    s = (i - j) mod N), then query tiles ascending."""
     if striped == 2 and (S // N) % (2 * T):
         pytest.skip("zigzag needs whole-tile chunks")
     ref = oracle.fold_schedule(S, N, causal, striped, T, T)
@@ -172,5 +173,5 @@ def test_plan_backward_equals_transposed_bruteforce(lib, causal, striped, S, N, 
     nt = -(-(S // N) // T)
     for j in range(N):
         for kt in range(nt):
-            want = sorted(by_key.get((j, kt), []))
+            want = sorted(by_key.get((j, kt), []), key=lambda e: (e[1], e[2]))
             assert ra.plan_backward(S, N, causal, striped, j, kt, tile=T) == want, (j, kt)
