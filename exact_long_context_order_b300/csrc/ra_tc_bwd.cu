@@ -25,9 +25,11 @@
 // single kernel reducing dQ across key tiles would cost 5.
 //
 // Both use one CTA per SM (384 threads): warp 0 lane 0 issues TMA copies,
-// warp 1 lane 0 issues MMAs, warp 2 owns TMEM, warp 3 (dkv only) stages the
-// per-row lse and delta of each query tile, and warps 4-11 are two
-// warpgroups that split the 128 columns of each score tile.  Every mbarrier
+// lane 0 of two warps issues MMAs (one thread cannot issue a tile's MMAs as
+// fast as the tensor core runs them): warps 1 and 3 in dq_kernel, warps 1
+// and 2 in dkv_kernel, where warp 3 stages the per-row lse and delta of each
+// query tile; warp 2 owns TMEM; warps 4-11 are two warpgroups that split the
+// 128 columns of each score tile.  Every mbarrier
 // wait is bounded; on time-out a kernel records kStatusTimeout, drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -109,13 +111,13 @@ constexpr int kVOff = kKOff + kKStages * kTileBytes;
 constexpr int kBarOff = kVOff + kVStages * kTileBytes;
 enum {
     bQFull = 0, bQEmpty, bKFull, bKEmpty = bKFull + kKStages, bVFull = bKEmpty + kKStages,
-    bVEmpty = bVFull + kVStages, bSdpFull = bVEmpty + kVStages, bSRead, bDsFull,
-    bDqFull = bDsFull + 2, bDqEmpty, bDrain, bItemFull, bItemEmpty = bItemFull + 2,
-    kNumBars = bItemEmpty + 2
+    bVEmpty = bVFull + kVStages, bSFull = bVEmpty + kVStages, bDPFull = bSFull + 2, bSRead,
+    bDsFull, bDqFull = bDsFull + 2, bDqEmpty, bDrain, bItemFull = bDrain + 2,
+    bItemEmpty = bItemFull + 2, kNumBars = bItemEmpty + 2
 };
 constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 32 + 1024;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColDP = 256, kColDQ = 384;
-constexpr uint32_t kItemReaders = 9;  // the MMA issuer and eight softmax warps
+constexpr uint32_t kItemReaders = 10;  // two MMA issuers and eight softmax warps
 }  // namespace dqk
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(bar(bQFull), 1);
-        mbar_init(bar(bQEmpty), 1);
+        mbar_init(bar(bQEmpty), 2);  // S reads Q (issuer A), dP reads dO (issuer B)
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(bKFull + s), 1);
             mbar_init(bar(bKEmpty + s), 1);
@@ -146,13 +148,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bVFull + s), 1);
             mbar_init(bar(bVEmpty + s), 1);
         }
-        mbar_init(bar(bSdpFull), 1);
+        mbar_init(bar(bSFull + 0), 1);
+        mbar_init(bar(bSFull + 1), 1);
+        mbar_init(bar(bDPFull), 1);
         mbar_init(bar(bSRead), 8);
         mbar_init(bar(bDsFull + 0), 8);
         mbar_init(bar(bDsFull + 1), 8);
         mbar_init(bar(bDqFull), 1);
         mbar_init(bar(bDqEmpty), 8);
         mbar_init(bar(bDrain), 1);
+        mbar_init(bar(bDrain + 1), 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(bItemFull + t), 1);
             mbar_init(bar(bItemEmpty + t), kItemReaders);
@@ -261,11 +266,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     drain_wait(bar(bVFull + pos % kVStages), (pos / kVStages) & 1, kDrainCycles);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Per key tile n: S(n) into S[n&1], dP(n) into DP, then dQ += dS(n-1) K(n-1)
-        // once the softmax has written dS(n-1) over S[(n-1)&1].
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ MMA issuers
+        // Lane 0 of warp 1 (A): S(n) into S[n&1], then dQ += dS(n-1) K(n-1) once the
+        // softmax has written dS(n-1) over S[(n-1)&1].  Lane 0 of warp 3 (B):
+        // dP(n) into DP once the softmax has read dP(n-1).  Two threads, because
+        // one cannot issue the tile's MMAs as fast as the tensor core runs them.
+        // "S ready" is doubled by tile parity: A may run a tile ahead of B.
         if (lane == 0) {
+            const bool is_a = (warp == 1);
             uint32_t g = 0;  // key tiles issued so far (ring positions of K and V)
             int k = 0;
             bool ok = true;
@@ -294,38 +303,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 TileWalk w;
                 uint32_t n = 0;
                 for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n) {
-                    const uint32_t sk = g % kKStages, sv = g % kVStages;
-                    if (!(ok = wait_bar(bar(bKFull + sk), (g / kKStages) & 1, abort_flag,
-                                        p.status, kTimeoutCycles)))
-                        break;
-                    tc_fence_after();
-                    mma_nt(sbuf(g), base + kQOff, base + kKOff + sk * kTileBytes, false);
-                    if (!(ok = wait_bar(bar(bVFull + sv), (g / kVStages) & 1, abort_flag,
-                                        p.status, kTimeoutCycles)))
-                        break;
-                    if (g > 0 && !(ok = wait_bar(bar(bSRead), (g - 1) & 1, abort_flag, p.status,
-                                                 kTimeoutCycles)))
-                        break;
-                    tc_fence_after();
-                    mma_nt(tmem + kColDP, base + kDOOff, base + kVOff + sv * kTileBytes, false);
-                    umma_commit(bar(bSdpFull));
-                    umma_commit(bar(bVEmpty + sv));
-                    if (n > 0 && !(ok = issue_dq(n, k))) break;
+                    if (is_a) {
+                        const uint32_t sk = g % kKStages;
+                        if (!(ok = wait_bar(bar(bKFull + sk), (g / kKStages) & 1, abort_flag,
+                                            p.status, kTimeoutCycles)))
+                            break;
+                        tc_fence_after();
+                        mma_nt(sbuf(g), base + kQOff, base + kKOff + sk * kTileBytes, false);
+                        umma_commit(bar(bSFull + (g & 1)));
+                        if (n > 0 && !(ok = issue_dq(n, k))) break;
+                    } else {
+                        const uint32_t sv = g % kVStages;
+                        if (!(ok = wait_bar(bar(bVFull + sv), (g / kVStages) & 1, abort_flag,
+                                            p.status, kTimeoutCycles)))
+                            break;
+                        if (g > 0 && !(ok = wait_bar(bar(bSRead), (g - 1) & 1, abort_flag,
+                                                     p.status, kTimeoutCycles)))
+                            break;
+                        tc_fence_after();
+                        mma_nt(tmem + kColDP, base + kDOOff, base + kVOff + sv * kTileBytes, false);
+                        umma_commit(bar(bDPFull));
+                        umma_commit(bar(bVEmpty + sv));
+                    }
                     ++g;
                 }
                 if (!ok) break;
-                umma_commit(bar(bQEmpty));  // every MMA reading this item's Q and dO is issued
-                if (!(ok = issue_dq(n, k))) break;
-                umma_commit(bar(bDqFull));
+                umma_commit(bar(bQEmpty));  // this issuer's MMAs reading Q (A) or dO (B) are issued
+                if (is_a) {
+                    if (!(ok = issue_dq(n, k))) break;
+                    umma_commit(bar(bDqFull));
+                }
             }
             if (!ok) {
                 *abort_flag = 1;
-                umma_commit(bar(bDrain));
-                drain_wait(bar(bDrain), 0, kDrainCycles);
+                umma_commit(bar(bDrain + (is_a ? 0 : 1)));
+                drain_wait(bar(bDrain + (is_a ? 0 : 1)), 0, kDrainCycles);
             }
         }
     } else if (warp < 4) {
-        // warp 2 owns TMEM; warp 3 is idle in this kernel
+        // warp 2 owns TMEM
     } else {
         // ------------------------------------------------------------ softmax
         regs_inc<kRegsSoftmax>();
@@ -354,7 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             TileWalk w;
             for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++g) {
                 const int kind = fold_kind(G.rg, t.i, w.j, t.qt, w.kt);
-                ok = wait_bar(bar(bSdpFull), g & 1, abort_flag, p.status, kTimeoutCycles);
+                ok = wait_bar(bar(bSFull + (g & 1)), (g >> 1) & 1, abort_flag, p.status,
+                              kTimeoutCycles) &&
+                     wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, kTimeoutCycles);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sb = tmem + lane_off + ((g & 1) ? kColS1 : kColS0);
@@ -451,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -468,12 +487,12 @@ enum {
     bKVFull = 0, bKVEmpty, bQFull, bQEmpty = bQFull + kQStages, bDOFull = bQEmpty + kQStages,
     bDOEmpty = bDOFull + kDOStages, bVecFull = bDOEmpty + kDOStages, bVecEmpty = bVecFull + 2,
     bSFull = bVecEmpty + 2, bSRead, bPFull, bDPFull, bDPRead, bDsFull, bAccFull, bAccEmpty,
-    bDrain, bItemFull, bItemEmpty = bItemFull + 2, kNumBars = bItemEmpty + 2
+    bDrain, bItemFull = bDrain + 2, bItemEmpty = bItemFull + 2, kNumBars = bItemEmpty + 2
 };
 constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 32 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
-// readers of a published item: the MMA issuer, the row-vector warp, eight softmax warps
-constexpr uint32_t kItemReaders = 10;
+// readers of a published item: two MMA issuers, the row-vector warp, eight softmax warps
+constexpr uint32_t kItemReaders = 11;
 }  // namespace dkv
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -495,13 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = G.rg.nt, heads = G.g;
 
     if (tid == 0) {
+        // stages and accumulators used by both MMA issuers complete on two commits
         mbar_init(bar(bKVFull), 1);
-        mbar_init(bar(bKVEmpty), 1);
+        mbar_init(bar(bKVEmpty), 2);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(bQFull + s), 1);
-            mbar_init(bar(bQEmpty + s), 1);
+            mbar_init(bar(bQEmpty + s), 2);
             mbar_init(bar(bDOFull + s), 1);
-            mbar_init(bar(bDOEmpty + s), 1);
+            mbar_init(bar(bDOEmpty + s), 2);
             mbar_init(bar(bVecFull + s), 32);
             mbar_init(bar(bVecEmpty + s), 8);
         }
@@ -511,9 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(bDPFull), 1);
         mbar_init(bar(bDPRead), 8);
         mbar_init(bar(bDsFull), 8);
-        mbar_init(bar(bAccFull), 1);
+        mbar_init(bar(bAccFull), 2);
         mbar_init(bar(bAccEmpty), 8);
         mbar_init(bar(bDrain), 1);
+        mbar_init(bar(bDrain + 1), 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(bItemFull + t), 1);
             mbar_init(bar(bItemEmpty + t), kItemReaders);
@@ -615,30 +636,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     drain_wait(bar(bDOFull + (x & 1)), (x >> 1) & 1, kDrainCycles);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // Pipe order: S(0) dP(0) | dV(n) S(n+1) dK(n) dP(n+1) | ... so that the
-        // softmax of tile n+1 overlaps dK(n) and dV(n+1) overlaps its dS part.
+    } else if (warp == 1 || warp == 2) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two issuer threads on disjoint tensor memory, because one thread cannot
+        // issue the tile's 32 MMAs as fast as the tensor core runs them:
+        //   lane 0 of warp 1: S^T(n) into S, then dV += P^T(n) dO(n) reading S;
+        //   lane 0 of warp 2: dP^T(n) into dP, then dK += dS^T(n) Q(n) reading dP.
+        // Each keeps its own in-order reuse (S(n+1) after dV(n), dP(n+1) after
+        // dK(n)); stages and accumulators both read complete on two commits.
         if (lane == 0) {
+            const bool is_s = (warp == 1);
             uint32_t g = 0;
             int k = 0;
             bool ok = true;
-            auto issue_s = [&](uint32_t gg) -> bool {
-                if (!wait_bar(bar(bQFull + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status,
+            // S^T(gg) = K Q(gg)^T or dP^T(gg) = V dO(gg)^T
+            auto issue_first = [&](uint32_t gg) -> bool {
+                const int full = is_s ? bQFull : bDOFull;
+                if (!wait_bar(bar(full + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status,
                               kTimeoutCycles))
                     return false;
                 tc_fence_after();
-                mma_nt(tmem + kColS, base + kKOff, base + kQOff + (gg & 1) * kTileBytes, false);
-                umma_commit(bar(bSFull));
-                return true;
-            };
-            auto issue_dp = [&](uint32_t gg) -> bool {
-                if (!wait_bar(bar(bDOFull + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status,
-                              kTimeoutCycles))
-                    return false;
-                tc_fence_after();
-                mma_nt(tmem + kColDP, base + kVOff, base + kDOOff + (gg & 1) * kTileBytes, false);
-                umma_commit(bar(bDPFull));
+                if (is_s)
+                    mma_nt(tmem + kColS, base + kKOff, base + kQOff + (gg & 1) * kTileBytes, false);
+                else
+                    mma_nt(tmem + kColDP, base + kVOff, base + kDOOff + (gg & 1) * kTileBytes,
+                           false);
+                umma_commit(bar(is_s ? bSFull : bDPFull));
                 return true;
             };
             for (;; ++k) {
@@ -650,27 +673,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 KeyWalk w;
                 w.start(G.rg, t.j, t.kt, heads);
-                if (!(ok = issue_s(g)) || !(ok = issue_dp(g))) break;
+                if (!(ok = issue_first(g))) break;
                 for (uint32_t n = 0; !w.done(G.rg); ++n, ++g) {
                     KeyWalk nx = w;
                     nx.next(G.rg, t.j, t.kt, heads);
                     const bool more = !nx.done(G.rg);
-                    if (!(ok = wait_bar(bar(bPFull), g & 1, abort_flag, p.status, kTimeoutCycles)))
+                    // P^T(n) resp. dS^T(n) written by the softmax
+                    if (!(ok = wait_bar(bar(is_s ? bPFull : bDsFull), g & 1, abort_flag, p.status,
+                                        kTimeoutCycles)))
                         break;
                     if (n == 0 && k > 0 &&
                         !(ok = wait_bar(bar(bAccEmpty), (k - 1) & 1, abort_flag, p.status,
                                         kTimeoutCycles)))
                         break;
                     tc_fence_after();
-                    mma_tn(tmem + kColDV, tmem + kColS, base + kDOOff + (g & 1) * kTileBytes, n > 0);
-                    umma_commit(bar(bDOEmpty + (g & 1)));
-                    if (more && !(ok = issue_s(g + 1))) break;
-                    if (!(ok = wait_bar(bar(bDsFull), g & 1, abort_flag, p.status, kTimeoutCycles)))
-                        break;
-                    tc_fence_after();
-                    mma_tn(tmem + kColDK, tmem + kColDP, base + kQOff + (g & 1) * kTileBytes, n > 0);
-                    umma_commit(bar(bQEmpty + (g & 1)));
-                    if (more && !(ok = issue_dp(g + 1))) break;
+                    if (is_s) {
+                        mma_tn(tmem + kColDV, tmem + kColS, base + kDOOff + (g & 1) * kTileBytes,
+                               n > 0);
+                        umma_commit(bar(bDOEmpty + (g & 1)));
+                        umma_commit(bar(bQEmpty + (g & 1)));  // S(n) read Q(n)
+                    } else {
+                        mma_tn(tmem + kColDK, tmem + kColDP, base + kQOff + (g & 1) * kTileBytes,
+                               n > 0);
+                        umma_commit(bar(bQEmpty + (g & 1)));
+                        umma_commit(bar(bDOEmpty + (g & 1)));  // dP(n) read dO(n)
+                    }
+                    if (more && !(ok = issue_first(g + 1))) break;
                     w = nx;
                 }
                 if (!ok) break;
@@ -679,12 +707,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 *abort_flag = 1;
-                umma_commit(bar(bDrain));
-                drain_wait(bar(bDrain), 0, kDrainCycles);
+                umma_commit(bar(bDrain + (is_s ? 0 : 1)));
+                drain_wait(bar(bDrain + (is_s ? 0 : 1)), 0, kDrainCycles);
             }
         }
-    } else if (warp == 2) {
-        // TMEM owner
     } else if (warp == 3) {
         // ------------------------------------------------------------ row vectors
         // -lse * log2(e) and delta of the 128 query rows of each tile, into a
@@ -897,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 2) {
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
