@@ -576,6 +576,9 @@ def main():
     peak = float(peaks["bf16_tflops"])
     peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
     achieved = flops / (launch_avg_ms * 1e-3) / 1e12
+    traffic = profiled_traffic(wl.name)
+    # exponentials the softmax evaluates: one per visible (query, key) pair
+    pairs = wl.B * wl.Hq * (wl.S * (wl.S + 1) / 2 if wl.causal else wl.S * wl.S)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
@@ -588,9 +591,15 @@ def main():
         "frac_of_bf16_peak": value / world / peak,
         "gpu_launches": args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(wl.name),
+                     "frac": achieved / peak, "traffic": traffic,
                      "kernel": KERNEL_NAME, "peak_source": f"{peak_src} bf16_tflops (burst)",
-                     "frac_of_sustained": achieved / peak_sus},
+                     "frac_of_sustained": achieved / peak_sus,
+                     "launch_ms_mean": launch_avg_ms,
+                     "launch_ms_median": float(np.median(per_launch_ms)),
+                     "exp_per_s": pairs / (launch_avg_ms * 1e-3),
+                     "hbm_gbs": (traffic / (launch_avg_ms * 1e-3) / 1e9) if traffic else None,
+                     "hbm_frac": (traffic / (launch_avg_ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]))
+                     if traffic else None},
         "clocks": clk,
         "e2e": e2e,
     }

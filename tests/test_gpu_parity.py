@@ -299,7 +299,7 @@ def test_noncausal_8k_every_row(ra):
 
 @pytest.mark.parametrize("name,n_rows", [("causal_32k_contig", 768), ("causal_32k_striped", 768),
                                          ("causal_32k_zigzag", 768), ("gqa_128k", 768),
-                                         ("long_1m", 384)])
+                                         ("gqa_128k_ragged", 768), ("long_1m", 384)])
 def test_full_size_sampled_rows(ra, name, n_rows):
     import torch
     wl = WORKLOADS[name]
