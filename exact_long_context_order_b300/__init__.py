@@ -49,6 +49,9 @@ _SIGNATURES = {
     "ra_backward_ex": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32,
                         _i32, _i64, _i32, _i32, _i32, _i32, _f32, _i32, _i32, _vp], _i32),
     "ra_backward_workspace": ([_i32, _i32, _i64, _i32, _c.POINTER(_i64)], _i32),
+    "ra_watchdog_selftest_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+                                       _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32, _f32,
+                                       _i64, _i32, _vp], _i32),
     "ra_check": ([_vp], _i32),
     "ra_strerror": ([_i32], _c.c_char_p),
     "ra_tile_config": ([_c.POINTER(_i32), _c.POINTER(_i32)], _i32),
@@ -153,6 +156,14 @@ def ra_backward_workspace(B, Hq, S, D):
     n = _i64()
     rc = lib().ra_backward_workspace(B, Hq, S, D, ctypes.byref(n))
     return rc, n.value
+
+
+def ra_watchdog_selftest_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace,
+                                  workspace_bytes, B, Hq, Hkv, S, D, N, causal, striped, scale,
+                                  timeout_cycles, which, stream):
+    return lib().ra_watchdog_selftest_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace,
+                                               workspace_bytes, B, Hq, Hkv, S, D, N, causal,
+                                               striped, scale, timeout_cycles, which, stream)
 
 
 def ra_check(stream):

@@ -76,6 +76,11 @@ bool tc_bwd_supported(const BwdProblem& p);
 // dk/dv kernel, each zeroing the work counter on `stream` before it starts.
 int launch_bwd_tc(const BwdProblem& p, unsigned int* status, unsigned int* work, int sm_count,
                   cudaStream_t stream);
+// Failure-detection self test of one backward kernel (which: 0 dq, 1 dk/dv):
+// its first K (dq) or Q (dk/dv) tile is never loaded and every wait is
+// bounded by timeout_cycles, so the kernel reports kStatusTimeout and returns.
+int launch_bwd_tc_selftest(const BwdProblem& p, unsigned int* status, unsigned int* work,
+                           int sm_count, cudaStream_t stream, long long timeout_cycles, int which);
 
 int launch_ulysses(const void* src, void* dst, int64_t B, int64_t H, int64_t S, int N,
                    int64_t row_bytes, int inverse, cudaStream_t stream);

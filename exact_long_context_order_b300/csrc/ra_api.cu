@@ -213,6 +213,48 @@ int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
     return rc;
 }
 
+int ra_watchdog_selftest_backward(const void* q, const void* k, const void* v, const void* out,
+                                  const float* lse, const void* dout, void* dq, void* dk,
+                                  void* dv, void* workspace, int64_t workspace_bytes, int B,
+                                  int Hq, int Hkv, int64_t S, int D, int N, int causal,
+                                  int striped, float scale, int64_t timeout_cycles, int which,
+                                  void* stream) {
+    int rc = validate_forward(q, k, v, out, nullptr, B, Hq, Hkv, S, D, N, RA_BF16, striped);
+    if (rc) return rc;
+    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
+    if (timeout_cycles < 100000 || timeout_cycles > 4000000000ll) return RA_ERR_INVALID_ARG;
+    if (which != 0 && which != 1) return RA_ERR_INVALID_ARG;
+    if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv) || !aligned16(workspace))
+        return RA_ERR_ALIGN;
+    const int64_t need = backward_workspace_bytes(B, Hq, S, D);
+    if (need < 0) return RA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return RA_ERR_CAPACITY;
+    unsigned int* status = nullptr;
+    int sms = 0;
+    if ((rc = device_state(&status, &sms))) return rc;
+    ra::BwdProblem p;
+    p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse; p.dout = dout;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.delta = static_cast<float*>(workspace);
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.N = N;
+    p.causal = causal ? 1 : 0;
+    p.striped = striped;
+    p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
+    p.dtype = RA_BF16;
+    if (!ra::tc_bwd_supported(p)) return RA_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = ra::launch_bwd_delta(p, st))) {
+        if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+        return rc;
+    }
+    unsigned int* work = nullptr;
+    if ((rc = work_slot(&work))) return rc;
+    rc = ra::launch_bwd_tc_selftest(p, status, work, sms, st, timeout_cycles, which);
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
 int ra_backward(const void* q, const void* k, const void* v, const void* out, const float* lse,
                 const void* dout, void* dq, void* dk, void* dv, void* workspace,
                 int64_t workspace_bytes, int B, int Hq, int Hkv, int64_t S, int D, int N,

@@ -99,6 +99,7 @@ struct Params {
     __nv_bfloat16* dv;
     unsigned int* status;
     unsigned int* work;
+    long long timeout_cycles;  // self test only: limit of every bounded wait
 };
 
 // ============================================================== dq kernel
@@ -120,6 +121,9 @@ constexpr uint32_t kColS0 = 0, kColS1 = 128, kColDP = 256, kColDQ = 384;
 constexpr uint32_t kItemReaders = 10;  // two MMA issuers and eight softmax warps
 }  // namespace dqk
 
+// SELFTEST: the failure-detection self test (the first K tile is never
+// loaded, every wait is bounded by p.timeout_cycles).
+template <bool SELFTEST>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -136,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const TileGeom& G = p.G;
     const int nt = G.rg.nt;
+    // limits of the bounded waits (the self test uses a short one)
+    const long long wlim = SELFTEST ? p.timeout_cycles : kTimeoutCycles;
+    const long long dlim = SELFTEST ? p.timeout_cycles : kDrainCycles;
 
     if (tid == 0) {
         mbar_init(bar(bQFull), 1);
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     auto read_item = [&](int k, bool& ok) -> long long {
-        ok = wait_bar(bar(bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, kTimeoutCycles);
+        ok = wait_bar(bar(bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, wlim);
         return ok ? item_slot[k & 1] : G.n_items;
     };
     auto walk_item = [&](const QTile& t) {
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             auto publish = [&](int kk, long long v) -> bool {
                 if (kk >= 2 && !wait_bar(bar(bItemEmpty + (kk & 1)), ((kk >> 1) - 1) & 1,
-                                         abort_flag, p.status, kTimeoutCycles))
+                                         abort_flag, p.status, wlim))
                     return false;
                 item_slot[kk & 1] = v;
                 mbar_arrive(bar(bItemFull + (kk & 1)));
@@ -219,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Item it = walk_item(t);
                 item = next;
                 if (k > 0 && !(ok = wait_bar(bar(bQEmpty), (k - 1) & 1, abort_flag, p.status,
-                                             kTimeoutCycles)))
+                                             wlim)))
                     break;
                 mbar_arrive_expect_tx(bar(bQFull), 2 * kTileBytes);
                 ++q_loads;
@@ -237,15 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int row = (int)(kvrow0 + (int64_t)w.j * p.Sb + (int64_t)w.kt * kT);
                     const uint32_t sk = tiles % kKStages, uk = tiles / kKStages;
                     if (uk > 0 && !(ok = wait_bar(bar(bKEmpty + sk), (uk - 1) & 1, abort_flag,
-                                                  p.status, kTimeoutCycles)))
+                                                  p.status, wlim)))
                         break;
-                    mbar_arrive_expect_tx(bar(bKFull + sk), kTileBytes);
-                    for (int bx = 0; bx < 2; ++bx)
-                        tma_load_2d(base + kKOff + sk * kTileBytes + bx * kBoxBytes, &tm_k,
-                                    bx * 64, row, bar(bKFull + sk), pol_kv);
+                    if (!(SELFTEST && tiles == 0)) {  // self test: K of the first tile never comes
+                        mbar_arrive_expect_tx(bar(bKFull + sk), kTileBytes);
+                        for (int bx = 0; bx < 2; ++bx)
+                            tma_load_2d(base + kKOff + sk * kTileBytes + bx * kBoxBytes, &tm_k,
+                                        bx * 64, row, bar(bKFull + sk), pol_kv);
+                    }
                     const uint32_t sv = tiles % kVStages, uv = tiles / kVStages;
                     if (uv > 0 && !(ok = wait_bar(bar(bVEmpty + sv), (uv - 1) & 1, abort_flag,
-                                                  p.status, kTimeoutCycles))) {
+                                                  p.status, wlim))) {
                         ++tiles;  // K of this tile is in flight
                         break;
                     }
@@ -257,13 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 // let every copy that may still be in flight land before exit
-                if (q_loads > 0) drain_wait(bar(bQFull), (q_loads - 1) & 1, kDrainCycles);
+                if (q_loads > 0) drain_wait(bar(bQFull), (q_loads - 1) & 1, dlim);
                 for (uint32_t pos = tiles > (uint32_t)kKStages ? tiles - kKStages : 0; pos < tiles;
                      ++pos)
-                    drain_wait(bar(bKFull + pos % kKStages), (pos / kKStages) & 1, kDrainCycles);
+                    drain_wait(bar(bKFull + pos % kKStages), (pos / kKStages) & 1, dlim);
                 for (uint32_t pos = tiles > (uint32_t)kVStages ? tiles - kVStages : 0; pos < tiles;
                      ++pos)
-                    drain_wait(bar(bVFull + pos % kVStages), (pos / kVStages) & 1, kDrainCycles);
+                    drain_wait(bar(bVFull + pos % kVStages), (pos / kVStages) & 1, dlim);
             }
         }
     } else if (warp == 1 || warp == 3) {
@@ -282,10 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_dq = [&](uint32_t n, int kk) -> bool {
                 // dq of tile g-1: needs its dS and, for the item's first, a drained DQ
                 if (!wait_bar(bar(bDsFull + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag,
-                              p.status, kTimeoutCycles))
+                              p.status, wlim))
                     return false;
                 if (n == 1 && kk > 0 &&
-                    !wait_bar(bar(bDqEmpty), (kk - 1) & 1, abort_flag, p.status, kTimeoutCycles))
+                    !wait_bar(bar(bDqEmpty), (kk - 1) & 1, abort_flag, p.status, wlim))
                     return false;
                 tc_fence_after();
                 const uint32_t sk = (g - 1) % kKStages;
@@ -298,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) mbar_arrive(bar(bItemEmpty + (k & 1)));
                 if (!ok || item >= G.n_items) break;
                 const Item it = walk_item(decode_qtile(G, item));
-                if (!(ok = wait_bar(bar(bQFull), k & 1, abort_flag, p.status, kTimeoutCycles)))
+                if (!(ok = wait_bar(bar(bQFull), k & 1, abort_flag, p.status, wlim)))
                     break;
                 TileWalk w;
                 uint32_t n = 0;
@@ -306,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (is_a) {
                         const uint32_t sk = g % kKStages;
                         if (!(ok = wait_bar(bar(bKFull + sk), (g / kKStages) & 1, abort_flag,
-                                            p.status, kTimeoutCycles)))
+                                            p.status, wlim)))
                             break;
                         tc_fence_after();
                         mma_nt(sbuf(g), base + kQOff, base + kKOff + sk * kTileBytes, false);
@@ -315,10 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const uint32_t sv = g % kVStages;
                         if (!(ok = wait_bar(bar(bVFull + sv), (g / kVStages) & 1, abort_flag,
-                                            p.status, kTimeoutCycles)))
+                                            p.status, wlim)))
                             break;
                         if (g > 0 && !(ok = wait_bar(bar(bSRead), (g - 1) & 1, abort_flag,
-                                                     p.status, kTimeoutCycles)))
+                                                     p.status, wlim)))
                             break;
                         tc_fence_after();
                         mma_nt(tmem + kColDP, base + kDOOff, base + kVOff + sv * kTileBytes, false);
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {
                 *abort_flag = 1;
                 umma_commit(bar(bDrain + (is_a ? 0 : 1)));
-                drain_wait(bar(bDrain + (is_a ? 0 : 1)), 0, kDrainCycles);
+                drain_wait(bar(bDrain + (is_a ? 0 : 1)), 0, dlim);
             }
         }
     } else if (warp < 4) {
@@ -371,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++g) {
                 const int kind = fold_kind(G.rg, t.i, w.j, t.qt, w.kt);
                 ok = wait_bar(bar(bSFull + (g & 1)), (g >> 1) & 1, abort_flag, p.status,
-                              kTimeoutCycles) &&
-                     wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, kTimeoutCycles);
+                              wlim) &&
+                     wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sb = tmem + lane_off + ((g & 1) ? kColS1 : kColS0);
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                 }
                 // both warpgroups must have read S before dS goes over it
-                ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, kTimeoutCycles);
+                ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tmem_st32(sb + 32 * wg, pk);
                 tmem_wait_st();
@@ -435,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
-            ok = wait_bar(bar(bDqFull), k & 1, abort_flag, p.status, kTimeoutCycles);
+            ok = wait_bar(bar(bDqFull), k & 1, abort_flag, p.status, wlim);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const uint64_t sc2 = f2_pack(p.scale, p.scale);
@@ -495,6 +504,9 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 constexpr uint32_t kItemReaders = 11;
 }  // namespace dkv
 
+// SELFTEST: the failure-detection self test (the first Q tile is never
+// loaded, every wait is bounded by p.timeout_cycles).
+template <bool SELFTEST>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -512,6 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const TileGeom& G = p.G;
     const int nt = G.rg.nt, heads = G.g;
+    // limits of the bounded waits (the self test uses a short one)
+    const long long wlim = SELFTEST ? p.timeout_cycles : kTimeoutCycles;
+    const long long dlim = SELFTEST ? p.timeout_cycles : kDrainCycles;
 
     if (tid == 0) {
         // stages and accumulators used by both MMA issuers complete on two commits
@@ -558,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     auto read_item = [&](int k, bool& ok) -> long long {
-        ok = wait_bar(bar(bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, kTimeoutCycles);
+        ok = wait_bar(bar(bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, wlim);
         return ok ? item_slot[k & 1] : G.n_items;
     };
     // first row of query tile (head kvh*g + gi, shard i, tile qt)
@@ -578,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             auto publish = [&](int kk, long long v) -> bool {
                 if (kk >= 2 && !wait_bar(bar(bItemEmpty + (kk & 1)), ((kk >> 1) - 1) & 1,
-                                         abort_flag, p.status, kTimeoutCycles))
+                                         abort_flag, p.status, wlim))
                     return false;
                 item_slot[kk & 1] = v;
                 mbar_arrive(bar(bItemFull + (kk & 1)));
@@ -588,8 +603,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  int row) -> bool {
                 const uint32_t st = g & 1, use = g >> 1;
                 if (use > 0 && !wait_bar(bar(empty + st), (use - 1) & 1, abort_flag, p.status,
-                                         kTimeoutCycles))
+                                         wlim))
                     return false;
+                if (SELFTEST && g == 0 && full == bQFull) return true;  // Q(0) never comes
                 mbar_arrive_expect_tx(bar(full + st), kTileBytes);
                 for (int bx = 0; bx < 2; ++bx)
                     tma_load_2d(base + off + st * kTileBytes + bx * kBoxBytes, tm, bx * 64, row,
@@ -605,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const KTile t = decode_ktile(G, item);
                 item = next;
                 if (k > 0 && !(ok = wait_bar(bar(bKVEmpty), (k - 1) & 1, abort_flag, p.status,
-                                             kTimeoutCycles)))
+                                             wlim)))
                     break;
                 mbar_arrive_expect_tx(bar(bKVFull), 2 * kTileBytes);
                 ++kv_loads;
@@ -629,11 +645,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) {
                 // let every copy that may still be in flight land before exit
-                if (kv_loads > 0) drain_wait(bar(bKVFull), (kv_loads - 1) & 1, kDrainCycles);
+                if (kv_loads > 0) drain_wait(bar(bKVFull), (kv_loads - 1) & 1, dlim);
                 for (uint32_t x = q_issued > 2 ? q_issued - 2 : 0; x < q_issued; ++x)
-                    drain_wait(bar(bQFull + (x & 1)), (x >> 1) & 1, kDrainCycles);
+                    drain_wait(bar(bQFull + (x & 1)), (x >> 1) & 1, dlim);
                 for (uint32_t x = do_issued > 2 ? do_issued - 2 : 0; x < do_issued; ++x)
-                    drain_wait(bar(bDOFull + (x & 1)), (x >> 1) & 1, kDrainCycles);
+                    drain_wait(bar(bDOFull + (x & 1)), (x >> 1) & 1, dlim);
             }
         }
     } else if (warp == 1 || warp == 2) {
@@ -653,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_first = [&](uint32_t gg) -> bool {
                 const int full = is_s ? bQFull : bDOFull;
                 if (!wait_bar(bar(full + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status,
-                              kTimeoutCycles))
+                              wlim))
                     return false;
                 tc_fence_after();
                 if (is_s)
@@ -669,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) mbar_arrive(bar(bItemEmpty + (k & 1)));
                 if (!ok || item >= G.n_items) break;
                 const KTile t = decode_ktile(G, item);
-                if (!(ok = wait_bar(bar(bKVFull), k & 1, abort_flag, p.status, kTimeoutCycles)))
+                if (!(ok = wait_bar(bar(bKVFull), k & 1, abort_flag, p.status, wlim)))
                     break;
                 KeyWalk w;
                 w.start(G.rg, t.j, t.kt, heads);
@@ -680,11 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool more = !nx.done(G.rg);
                     // P^T(n) resp. dS^T(n) written by the softmax
                     if (!(ok = wait_bar(bar(is_s ? bPFull : bDsFull), g & 1, abort_flag, p.status,
-                                        kTimeoutCycles)))
+                                        wlim)))
                         break;
                     if (n == 0 && k > 0 &&
                         !(ok = wait_bar(bar(bAccEmpty), (k - 1) & 1, abort_flag, p.status,
-                                        kTimeoutCycles)))
+                                        wlim)))
                         break;
                     tc_fence_after();
                     if (is_s) {
@@ -708,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {
                 *abort_flag = 1;
                 umma_commit(bar(bDrain + (is_s ? 0 : 1)));
-                drain_wait(bar(bDrain + (is_s ? 0 : 1)), 0, kDrainCycles);
+                drain_wait(bar(bDrain + (is_s ? 0 : 1)), 0, dlim);
             }
         }
     } else if (warp == 3) {
@@ -730,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  w.next(G.rg, t.j, t.kt, heads), ++g) {
                 const uint32_t st = g & 1, use = g >> 1;
                 ok = use == 0 || wait_bar(bar(bVecEmpty + st), (use - 1) & 1, abort_flag, p.status,
-                                          kTimeoutCycles);
+                                          wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 const int64_t row0 = qrow0(t, w);
                 float* vs = vec + st * (2 * kT);
@@ -774,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!key_ok || kind == kNone) lo = kT;
                 const float* vs = vec + (g & 1) * (2 * kT);
                 // ---- P^T = exp2(S^T scale log2e - lse log2e), over S^T
-                ok = wait_bar(bar(bSFull), g & 1, abort_flag, p.status, kTimeoutCycles);
+                ok = wait_bar(bar(bSFull), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[2][32];
@@ -787,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(bSRead));
                 ok = wait_bar(bar(bVecFull + (g & 1)), (g >> 1) & 1, abort_flag, p.status,
-                              kTimeoutCycles);
+                              wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 float pf[2][32];
                 uint32_t pk[32];
@@ -830,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[cc * 16 + e / 2 + 1] = pack_bf16x2(pf[cc][e + 2], pf[cc][e + 3]);
                         }
                 }
-                ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, kTimeoutCycles);
+                ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tmem_st32(tmem + lane_off + kColS + 32 * wg, pk);
                 tmem_wait_st();
@@ -838,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(bPFull));
                 // ---- dS^T = P^T (dP^T - delta), over dP^T
-                ok = wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, kTimeoutCycles);
+                ok = wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t dp[2][32];
@@ -869,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[cc * 16 + e / 2 + 1] = pack_bf16x2(d[2], d[3]);
                     }
                 }
-                ok = wait_bar(bar(bDPRead), g & 1, abort_flag, p.status, kTimeoutCycles);
+                ok = wait_bar(bar(bDPRead), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tmem_st32(tmem + lane_off + kColDP + 32 * wg, pk);
                 tmem_wait_st();
@@ -882,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // ---------------------------------------------------------- epilogue
-            ok = wait_bar(bar(bAccFull), k & 1, abort_flag, p.status, kTimeoutCycles);
+            ok = wait_bar(bar(bAccFull), k & 1, abort_flag, p.status, wlim);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const int64_t krow = (int64_t)(t.b * G.Hkv + t.kvh) * p.S + (int64_t)t.j * p.Sb +
@@ -932,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host side
 // kernel 0: dq_kernel over query tiles; kernel 1: dkv_kernel over key tiles
 static int launch_one(const BwdProblem& pr, int which, unsigned int* status, unsigned int* work,
-                      int sm_count, cudaStream_t stream) {
+                      int sm_count, cudaStream_t stream, long long timeout_cycles = 0) {
     CUtensorMap mq, mdo, mk, mv;
     const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
     if (!encode_rows_bf16(&mq, pr.q, q_rows, kD) || !encode_rows_bf16(&mdo, pr.dout, q_rows, kD) ||
@@ -954,9 +970,12 @@ static int launch_one(const BwdProblem& pr, int which, unsigned int* status, uns
     P.dv = static_cast<__nv_bfloat16*>(pr.dv);
     P.status = status;
     P.work = work;
+    P.timeout_cycles = timeout_cycles > 0 ? timeout_cycles : kTimeoutCycles;
     if (P.G.n_items <= 0) return RA_OK;
     if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
-    auto kern = which ? dkv_kernel : dq_kernel;
+    const bool st = timeout_cycles > 0;
+    auto kern = which ? (st ? dkv_kernel<true> : dkv_kernel<false>)
+                      : (st ? dq_kernel<true> : dq_kernel<false>);
     const int smem = which ? dkv::kSmemBytes : dqk::kSmemBytes;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
@@ -977,6 +996,13 @@ bool tc_bwd_supported(const BwdProblem& p) {
     if ((int64_t)p.B * p.Hq * p.S >= (1ll << 31) || (int64_t)p.B * p.Hkv * p.S >= (1ll << 31))
         return false;
     return true;
+}
+
+int launch_bwd_tc_selftest(const BwdProblem& p, unsigned int* status, unsigned int* work,
+                           int sm_count, cudaStream_t stream, long long timeout_cycles, int which) {
+    if (!tc_bwd_supported(p)) return RA_ERR_UNSUPPORTED;
+    if (!work || timeout_cycles <= 0 || (which != 0 && which != 1)) return RA_ERR_INVALID_ARG;
+    return tcb::launch_one(p, which, status, work, sm_count, stream, timeout_cycles);
 }
 
 int launch_bwd_tc(const BwdProblem& p, unsigned int* status, unsigned int* work, int sm_count,

@@ -312,6 +312,27 @@ int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
 int ra_backward_workspace(int B, int Hq, int64_t S, int D, int64_t* bytes);
 
 /*
+ * ra_watchdog_selftest_backward: the failure-detection self test of one
+ * backward tensor-core kernel (which = 0: the dq kernel, 1: the dk/dv
+ * kernel), the counterpart of ra_watchdog_selftest.  Arguments as
+ * ra_backward (bf16, tensor-core shapes) plus timeout_cycles (1e5 .. 4e9
+ * SM clock cycles): the kernel's first K (dq) or Q (dk/dv) tile copy is never
+ * issued and every wait is bounded by timeout_cycles, so the waits that
+ * depend on it run out; the kernel records RA_ERR_TIMEOUT in the device
+ * status word, lets its copies and MMAs in flight finish, frees its tensor
+ * memory and returns.  The gradients are left undefined.  Returns RA_OK once
+ * enqueued; ra_check(stream) then reports RA_ERR_TIMEOUT.
+ * Errors: as ra_backward; RA_ERR_INVALID_ARG for timeout_cycles out of range
+ * or `which` not 0 or 1; RA_ERR_UNSUPPORTED outside the tensor-core shapes.
+ */
+int ra_watchdog_selftest_backward(const void* q, const void* k, const void* v, const void* out,
+                                  const float* lse, const void* dout, void* dq, void* dk,
+                                  void* dv, void* workspace, int64_t workspace_bytes, int B,
+                                  int Hq, int Hkv, int64_t S, int D, int N, int causal,
+                                  int striped, float scale, int64_t timeout_cycles, int which,
+                                  void* stream);
+
+/*
  * ra_check: synchronise `stream`, then read and clear this device's status
  * word.  Returns RA_OK, RA_ERR_TIMEOUT, RA_ERR_BOUNDS or RA_ERR_CUDA (the
  * synchronisation itself failed; the CUDA error string is kept for
