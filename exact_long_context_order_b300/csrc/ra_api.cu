@@ -121,6 +121,34 @@ int64_t backward_workspace_bytes(int B, int Hq, int64_t S, int D) {
     return ((4 * (int64_t)B * Hq * S) + 255) / 256 * 256;
 }
 
+// Validates ra_backward's arguments on the host and fills the problem
+// (everything but the kernel choice).  Returns RA_OK or the error code.
+int prepare_backward(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     void* workspace, int64_t workspace_bytes, int B, int Hq, int Hkv, int64_t S,
+                     int D, int N, int causal, int striped, float scale, int dtype,
+                     ra::BwdProblem* p) {
+    int rc = validate_forward(q, k, v, out, nullptr, B, Hq, Hkv, S, D, N, dtype, striped);
+    if (rc) return rc;
+    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
+    if (D > 128) return RA_ERR_UNSUPPORTED;
+    if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv) || !aligned16(workspace))
+        return RA_ERR_ALIGN;
+    const int64_t need = backward_workspace_bytes(B, Hq, S, D);
+    if (need < 0) return RA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return RA_ERR_CAPACITY;
+    p->q = q; p->k = k; p->v = v; p->out = out; p->lse = lse; p->dout = dout;
+    p->dq = dq; p->dk = dk; p->dv = dv;
+    p->delta = static_cast<float*>(workspace);
+    p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->S = S; p->D = D; p->N = N;
+    p->causal = causal ? 1 : 0;
+    p->striped = striped;
+    p->scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
+    p->dtype = dtype;
+    return RA_OK;
+}
+
 }  // namespace
 
 int ra::device_status_word(unsigned int** status) { return device_state(status, nullptr); }
@@ -172,30 +200,15 @@ int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
                    void* workspace, int64_t workspace_bytes, int B, int Hq, int Hkv, int64_t S,
                    int D, int N, int causal, int striped, float scale, int dtype, int kernel,
                    void* stream) {
-    int rc = validate_forward(q, k, v, out, nullptr, B, Hq, Hkv, S, D, N, dtype, striped);
-    if (rc) return rc;
-    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
     if (kernel != RA_KERNEL_AUTO && kernel != RA_KERNEL_TC && kernel != RA_KERNEL_SIMT)
         return RA_ERR_INVALID_ARG;
-    if (D > 128) return RA_ERR_UNSUPPORTED;
-    if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
-        !aligned16(dv) || !aligned16(workspace))
-        return RA_ERR_ALIGN;
-    const int64_t need = backward_workspace_bytes(B, Hq, S, D);
-    if (need < 0) return RA_ERR_INVALID_ARG;
-    if (workspace_bytes < need) return RA_ERR_CAPACITY;
+    ra::BwdProblem p;
+    int rc = prepare_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B,
+                              Hq, Hkv, S, D, N, causal, striped, scale, dtype, &p);
+    if (rc) return rc;
     unsigned int* status = nullptr;
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
-    ra::BwdProblem p;
-    p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse; p.dout = dout;
-    p.dq = dq; p.dk = dk; p.dv = dv;
-    p.delta = static_cast<float*>(workspace);
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.N = N;
-    p.causal = causal ? 1 : 0;
-    p.striped = striped;
-    p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
-    p.dtype = dtype;
     const bool tc_ok = ra::tc_bwd_supported(p);
     if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -219,30 +232,16 @@ int ra_watchdog_selftest_backward(const void* q, const void* k, const void* v, c
                                   int Hq, int Hkv, int64_t S, int D, int N, int causal,
                                   int striped, float scale, int64_t timeout_cycles, int which,
                                   void* stream) {
-    int rc = validate_forward(q, k, v, out, nullptr, B, Hq, Hkv, S, D, N, RA_BF16, striped);
-    if (rc) return rc;
-    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
     if (timeout_cycles < 100000 || timeout_cycles > 4000000000ll) return RA_ERR_INVALID_ARG;
     if (which != 0 && which != 1) return RA_ERR_INVALID_ARG;
-    if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
-        !aligned16(dv) || !aligned16(workspace))
-        return RA_ERR_ALIGN;
-    const int64_t need = backward_workspace_bytes(B, Hq, S, D);
-    if (need < 0) return RA_ERR_INVALID_ARG;
-    if (workspace_bytes < need) return RA_ERR_CAPACITY;
+    ra::BwdProblem p;
+    int rc = prepare_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B,
+                              Hq, Hkv, S, D, N, causal, striped, scale, RA_BF16, &p);
+    if (rc) return rc;
+    if (!ra::tc_bwd_supported(p)) return RA_ERR_UNSUPPORTED;
     unsigned int* status = nullptr;
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
-    ra::BwdProblem p;
-    p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse; p.dout = dout;
-    p.dq = dq; p.dk = dk; p.dv = dv;
-    p.delta = static_cast<float*>(workspace);
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.D = D; p.N = N;
-    p.causal = causal ? 1 : 0;
-    p.striped = striped;
-    p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
-    p.dtype = RA_BF16;
-    if (!ra::tc_bwd_supported(p)) return RA_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = ra::launch_bwd_delta(p, st))) {
         if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());

@@ -112,6 +112,13 @@ TC_BF16 = [
     (1, 2, 2, 1000, 4, 128, True, 1),    # Sb = 250: ragged last tile, striped
     (1, 2, 1, 1000, 4, 128, True, 0),    # ragged, contiguous
     (1, 1, 1, 200, 2, 128, False, 0),    # one partial tile per shard
+    (1, 1, 1, 128, 1, 128, True, 0),     # a single tile
+    (2, 2, 2, 512, 1, 128, False, 0),    # B = 2, one ring device, no GQA
+    (1, 8, 1, 1024, 8, 128, True, 1),    # GQA group of 8, one tile per shard
+    (1, 2, 1, 2048, 16, 128, True, 0),   # 16 shards of one tile, contiguous
+    (1, 2, 1, 2048, 16, 128, True, 1),   # 16 shards of one tile, striped
+    (1, 2, 1, 130, 1, 128, True, 1),     # Sb = 130: ragged, one ring device
+    (2, 2, 2, 1536, 3, 128, True, 2),    # zigzag, B = 2, two tiles per chunk
 ]
 
 
@@ -122,6 +129,13 @@ def test_tc_backward_bf16(ra, B, Hq, Hkv, S, N, D, causal, layout):
     for name, g, r, e in zip(("dq", "dk", "dv"), got, ref, ext):
         fro, worst = assert_grad_close(g, r, "bf16", name, e)
         print(f"tc bf16 {S} {N} {layout} {name}: normwise {fro:.2e} worst row {worst:.2e}")
+
+
+def test_tc_backward_custom_scale(ra):
+    got, ref, ext = run_backward(ra, 7600, 1, 4, 2, 1024, 4, 128, True, 1, "bf16", "tc",
+                                 scale=0.05)
+    for name, g, r, e in zip(("dq", "dk", "dv"), got, ref, ext):
+        assert_grad_close(g, r, "bf16", name, e)
 
 
 def test_tc_backward_is_deterministic(ra):
