@@ -31,6 +31,8 @@ _SIGNATURES = {
                     _f32, _i32, _vp], _i32),
     "ra_forward_ex": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
                        _f32, _i32, _i32, _vp], _i32),
+    "ra_forward_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                         _i64, _i32, _i32, _i32, _i32, _f32, _i32, _vp], _i32),
     "ra_merge": ([_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp], _i32),
     "ra_stripe": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _vp], _i32),
     "ra_relayout": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _i32, _vp], _i32),
@@ -93,6 +95,14 @@ def ra_forward_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale
                   stream):
     return lib().ra_forward_ex(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped, scale,
                                dtype, kernel, stream)
+
+
+def ra_forward_host(q_h, k_h, v_h, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, B, Hq, Hkv, S, D,
+                    N, causal, striped, scale, dtype, stream):
+    """ra_forward on host buffers: H2D copies, the forward and D2H copies, all
+    enqueued on `stream` (host pointers, device staging pointers)."""
+    return lib().ra_forward_host(q_h, k_h, v_h, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, B, Hq,
+                                 Hkv, S, D, N, causal, striped, scale, dtype, stream)
 
 
 def ra_merge(out_a, lse_a, out_b, lse_b, rows, D, dtype, stream):

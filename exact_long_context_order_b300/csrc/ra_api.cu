@@ -262,6 +262,42 @@ int ra_backward(const void* q, const void* k, const void* v, const void* out, co
                           Hkv, S, D, N, causal, striped, scale, dtype, RA_KERNEL_AUTO, stream);
 }
 
+int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                    float* lse_host, void* q_dev, void* k_dev, void* v_dev, void* out_dev,
+                    float* lse_dev, int B, int Hq, int Hkv, int64_t S, int D, int N, int causal,
+                    int striped, float scale, int dtype, void* stream) {
+    if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID_ARG;
+    if ((lse_host != nullptr) != (lse_dev != nullptr)) return RA_ERR_INVALID_ARG;
+    int rc = validate_forward(q_dev, k_dev, v_dev, out_dev, lse_dev, B, Hq, Hkv, S, D, N, dtype,
+                              striped);
+    if (rc) return rc;
+    const int64_t esz = (dtype == RA_F32) ? 4 : 2;
+    const int64_t qbytes = (int64_t)B * Hq * S * D * esz, kvbytes = (int64_t)B * Hkv * S * D * esz;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(k_dev, k_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(v_dev, v_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) {
+        note_cuda(e);
+        return RA_ERR_CUDA;
+    }
+    if ((rc = ra_forward_ex(q_dev, k_dev, v_dev, out_dev, lse_dev, B, Hq, Hkv, S, D, N, causal,
+                            striped, scale, dtype, RA_KERNEL_AUTO, stream)))
+        return rc;
+    if ((e = cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, st)) !=
+        cudaSuccess) {
+        note_cuda(e);
+        return RA_ERR_CUDA;
+    }
+    if (lse_host &&
+        (e = cudaMemcpyAsync(lse_host, lse_dev, (int64_t)B * Hq * S * 4, cudaMemcpyDeviceToHost,
+                             st)) != cudaSuccess) {
+        note_cuda(e);
+        return RA_ERR_CUDA;
+    }
+    return RA_OK;
+}
+
 int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
                 int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
                 int32_t* log, int32_t* counts, int max_entries, void* stream) {

@@ -109,6 +109,27 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
                int Hkv, int64_t S, int D, int N, int causal, int striped, float scale, int dtype,
                void* stream);
 
+/*
+ * ra_forward_host: ra_forward on host tensors.  Enqueues on `stream` the
+ * copies of q, k, v from host to the caller's device staging buffers, the
+ * forward, and the copies of out (and lse, when lse_host is not NULL) back to
+ * the host.  Asynchronous: the host buffers must stay valid until the stream
+ * reaches the end of the call; page-locked (pinned) host memory makes the
+ * copies asynchronous and lets successive calls on two streams with two
+ * staging sets overlap one call's copies with the other's kernel.
+ *   q_host, k_host, v_host (read), out_host, lse_host (written; lse_host may
+ *   be NULL, then lse_dev must be NULL too): host memory with the layouts of
+ *   ra_forward.
+ *   q_dev, k_dev, v_dev, out_dev, lse_dev: device staging buffers of the same
+ *   sizes (caller-owned, 16-byte aligned), overwritten.
+ * Errors: as ra_forward; RA_ERR_INVALID_ARG for a NULL host pointer or an
+ * lse pair with one NULL; RA_ERR_CUDA when a copy cannot be enqueued.
+ */
+int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
+                    float* lse_host, void* q_dev, void* k_dev, void* v_dev, void* out_dev,
+                    float* lse_dev, int B, int Hq, int Hkv, int64_t S, int D, int N, int causal,
+                    int striped, float scale, int dtype, void* stream);
+
 /* ra_forward with an explicit kernel choice (RA_KERNEL_*).  RA_KERNEL_TC
  * returns RA_ERR_UNSUPPORTED when the shape is outside its envelope. */
 int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
