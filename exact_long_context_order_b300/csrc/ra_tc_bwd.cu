@@ -50,9 +50,10 @@ namespace ra {
 namespace tcb {
 
 constexpr int kT = 128;                    // query and key tile rows
-constexpr int kD = 128;                    // head dimension
+constexpr int kD = 128;                    // largest head dimension (sizes the smem slots)
 constexpr int kBoxBytes = kT * 128;        // 128 rows x 64 bf16 columns (128-byte swizzle)
-constexpr int kTileBytes = kT * kD * 2;    // two boxes
+constexpr int kTileBytes = kT * kD * 2;    // one smem slot: two boxes
+// A D = 64 tile fills the first box of its slot; D = 128 fills both.
 constexpr int kThreads = 384;
 constexpr long long kTimeoutCycles = 4000000000ll;
 constexpr long long kDrainCycles = 400000000ll;
@@ -61,23 +62,25 @@ constexpr long long kDrainCycles = 400000000ll;
 constexpr uint32_t kRegsOther = 80, kRegsSoftmax = 208;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// D (+)= A B^T for two K-major 128 x 128 bf16 tiles in smem (8 K-steps of 16).
+// D (+)= A B^T for two K-major 128 x HD bf16 tiles in smem (HD/16 K-steps of 16).
+template <int HD>
 __device__ __forceinline__ void mma_nt(uint32_t d_tm, uint32_t a_smem, uint32_t b_smem,
                                        bool acc) {
     constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
     const uint64_t da = make_sdesc(a_smem, 16, 1024, kLayoutSW128);
     const uint64_t db = make_sdesc(b_smem, 16, 1024, kLayoutSW128);
 #pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
+    for (int kk = 0; kk < HD / 16; ++kk) {
         const uint32_t off16 = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
         umma_ss(d_tm, da + off16, db + off16, idesc, (acc || kk > 0) ? 1u : 0u);
     }
 }
 
 // D (+)= A B: A is 128 x 128 bf16 in TMEM (two values per column), B a
-// row-major 128 x 128 tile in smem read MN-major (8 K-steps of 16 rows).
+// row-major 128 x HD tile in smem read MN-major (8 K-steps of 16 rows).
+template <int HD>
 __device__ __forceinline__ void mma_tn(uint32_t d_tm, uint32_t a_tm, uint32_t b_smem, bool acc) {
-    constexpr uint32_t idesc = make_idesc_bf16(128, kD, false, true);
+    constexpr uint32_t idesc = make_idesc_bf16(128, HD, false, true);
     const uint64_t db = make_sdesc(b_smem, kBoxBytes, 1024, kLayoutSW128);
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
@@ -123,7 +126,7 @@ constexpr uint32_t kItemReaders = 10;  // two MMA issuers and eight softmax warp
 
 // SELFTEST: the failure-detection self test (the first K tile is never
 // loaded, every wait is bounded by p.timeout_cycles).
-template <bool SELFTEST>
+template <int D, bool SELFTEST>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // limits of the bounded waits (the self test uses a short one)
     const long long wlim = SELFTEST ? p.timeout_cycles : kTimeoutCycles;
     const long long dlim = SELFTEST ? p.timeout_cycles : kDrainCycles;
+    constexpr int kLoadBytes = kT * D * 2;  // bytes of one q, k, v or dout tile
 
     if (tid == 0) {
         mbar_init(bar(bQFull), 1);
@@ -228,11 +232,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k > 0 && !(ok = wait_bar(bar(bQEmpty), (k - 1) & 1, abort_flag, p.status,
                                              wlim)))
                     break;
-                mbar_arrive_expect_tx(bar(bQFull), 2 * kTileBytes);
+                mbar_arrive_expect_tx(bar(bQFull), 2 * kLoadBytes);
                 ++q_loads;
                 const int qrow = (int)((int64_t)(t.b * G.Hq + t.h) * p.S + (int64_t)t.i * p.Sb +
                                        (int64_t)t.qt * kT);
-                for (int bx = 0; bx < 2; ++bx) {
+                for (int bx = 0; bx < D / 64; ++bx) {
                     tma_load_2d(base + kQOff + bx * kBoxBytes, &tm_q, bx * 64, qrow, bar(bQFull),
                                 pol_q);
                     tma_load_2d(base + kDOOff + bx * kBoxBytes, &tm_do, bx * 64, qrow,
@@ -247,8 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   p.status, wlim)))
                         break;
                     if (!(SELFTEST && tiles == 0)) {  // self test: K of the first tile never comes
-                        mbar_arrive_expect_tx(bar(bKFull + sk), kTileBytes);
-                        for (int bx = 0; bx < 2; ++bx)
+                        mbar_arrive_expect_tx(bar(bKFull + sk), kLoadBytes);
+                        for (int bx = 0; bx < D / 64; ++bx)
                             tma_load_2d(base + kKOff + sk * kTileBytes + bx * kBoxBytes, &tm_k,
                                         bx * 64, row, bar(bKFull + sk), pol_kv);
                     }
@@ -258,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++tiles;  // K of this tile is in flight
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(bVFull + sv), kTileBytes);
-                    for (int bx = 0; bx < 2; ++bx)
+                    mbar_arrive_expect_tx(bar(bVFull + sv), kLoadBytes);
+                    for (int bx = 0; bx < D / 64; ++bx)
                         tma_load_2d(base + kVOff + sv * kTileBytes + bx * kBoxBytes, &tm_v,
                                     bx * 64, row, bar(bVFull + sv), pol_kv);
                 }
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 tc_fence_after();
                 const uint32_t sk = (g - 1) % kKStages;
-                mma_tn(tmem + kColDQ, sbuf(g - 1), base + kKOff + sk * kTileBytes, n > 1);
+                mma_tn<D>(tmem + kColDQ, sbuf(g - 1), base + kKOff + sk * kTileBytes, n > 1);
                 umma_commit(bar(bKEmpty + sk));
                 return true;
             };
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             p.status, wlim)))
                             break;
                         tc_fence_after();
-                        mma_nt(sbuf(g), base + kQOff, base + kKOff + sk * kTileBytes, false);
+                        mma_nt<D>(sbuf(g), base + kQOff, base + kKOff + sk * kTileBytes, false);
                         umma_commit(bar(bSFull + (g & 1)));
                         if (n > 0 && !(ok = issue_dq(n, k))) break;
                     } else {
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      p.status, wlim)))
                             break;
                         tc_fence_after();
-                        mma_nt(tmem + kColDP, base + kDOOff, base + kVOff + sv * kTileBytes, false);
+                        mma_nt<D>(tmem + kColDP, base + kDOOff, base + kVOff + sv * kTileBytes, false);
                         umma_commit(bar(bDPFull));
                         umma_commit(bar(bVEmpty + sv));
                     }
@@ -448,11 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             const uint64_t sc2 = f2_pack(p.scale, p.scale);
-            uint4* drow = reinterpret_cast<uint4*>(p.dq + row * kD + c0);
+            const int e0 = (D / 2) * wg;  // dq columns of this warpgroup
+            uint4* drow = reinterpret_cast<uint4*>(p.dq + row * D + e0);
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kColDQ + c0 + cc * 32, o);
+                tmem_ld32(tmem + lane_off + kColDQ + e0 + cc * 32, o);
                 tmem_wait_ld();
                 reg_fence(o);
                 uint32_t pkd[16];
@@ -506,7 +511,7 @@ constexpr uint32_t kItemReaders = 11;
 
 // SELFTEST: the failure-detection self test (the first Q tile is never
 // loaded, every wait is bounded by p.timeout_cycles).
-template <bool SELFTEST>
+template <int D, bool SELFTEST>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -527,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // limits of the bounded waits (the self test uses a short one)
     const long long wlim = SELFTEST ? p.timeout_cycles : kTimeoutCycles;
     const long long dlim = SELFTEST ? p.timeout_cycles : kDrainCycles;
+    constexpr int kLoadBytes = kT * D * 2;  // bytes of one q, k, v or dout tile
 
     if (tid == 0) {
         // stages and accumulators used by both MMA issuers complete on two commits
@@ -606,8 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          wlim))
                     return false;
                 if (SELFTEST && g == 0 && full == bQFull) return true;  // Q(0) never comes
-                mbar_arrive_expect_tx(bar(full + st), kTileBytes);
-                for (int bx = 0; bx < 2; ++bx)
+                mbar_arrive_expect_tx(bar(full + st), kLoadBytes);
+                for (int bx = 0; bx < D / 64; ++bx)
                     tma_load_2d(base + off + st * kTileBytes + bx * kBoxBytes, tm, bx * 64, row,
                                 bar(full + st), pol_q);
                 return true;
@@ -623,11 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k > 0 && !(ok = wait_bar(bar(bKVEmpty), (k - 1) & 1, abort_flag, p.status,
                                              wlim)))
                     break;
-                mbar_arrive_expect_tx(bar(bKVFull), 2 * kTileBytes);
+                mbar_arrive_expect_tx(bar(bKVFull), 2 * kLoadBytes);
                 ++kv_loads;
                 const int krow = (int)((int64_t)(t.b * G.Hkv + t.kvh) * p.S +
                                        (int64_t)t.j * p.Sb + (int64_t)t.kt * kT);
-                for (int bx = 0; bx < 2; ++bx) {
+                for (int bx = 0; bx < D / 64; ++bx) {
                     tma_load_2d(base + kKOff + bx * kBoxBytes, &tm_k, bx * 64, krow, bar(bKVFull),
                                 pol_kv);
                     tma_load_2d(base + kVOff + bx * kBoxBytes, &tm_v, bx * 64, krow, bar(bKVFull),
@@ -673,9 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 tc_fence_after();
                 if (is_s)
-                    mma_nt(tmem + kColS, base + kKOff, base + kQOff + (gg & 1) * kTileBytes, false);
+                    mma_nt<D>(tmem + kColS, base + kKOff, base + kQOff + (gg & 1) * kTileBytes, false);
                 else
-                    mma_nt(tmem + kColDP, base + kVOff, base + kDOOff + (gg & 1) * kTileBytes,
+                    mma_nt<D>(tmem + kColDP, base + kVOff, base + kDOOff + (gg & 1) * kTileBytes,
                            false);
                 umma_commit(bar(is_s ? bSFull : bDPFull));
                 return true;
@@ -704,12 +710,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     tc_fence_after();
                     if (is_s) {
-                        mma_tn(tmem + kColDV, tmem + kColS, base + kDOOff + (g & 1) * kTileBytes,
+                        mma_tn<D>(tmem + kColDV, tmem + kColS, base + kDOOff + (g & 1) * kTileBytes,
                                n > 0);
                         umma_commit(bar(bDOEmpty + (g & 1)));
                         umma_commit(bar(bQEmpty + (g & 1)));  // S(n) read Q(n)
                     } else {
-                        mma_tn(tmem + kColDK, tmem + kColDP, base + kQOff + (g & 1) * kTileBytes,
+                        mma_tn<D>(tmem + kColDK, tmem + kColDP, base + kQOff + (g & 1) * kTileBytes,
                                n > 0);
                         umma_commit(bar(bQEmpty + (g & 1)));
                         umma_commit(bar(bDOEmpty + (g & 1)));  // dP(n) read dO(n)
@@ -908,11 +914,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int which = 0; which < 2; ++which) {  // dV, then dK (times scale)
                 const uint32_t col = which ? kColDK : kColDV;
                 const uint64_t mul = which ? sc2 : one2;
-                uint4* drow = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + krow * kD + q0);
+                const int e0 = (D / 2) * wg;  // dk/dv columns of this warpgroup
+                uint4* drow = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + krow * D + e0);
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
+                for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + col + q0 + cc * 32, o);
+                    tmem_ld32(tmem + lane_off + col + e0 + cc * 32, o);
                     tmem_wait_ld();
                     reg_fence(o);
                     uint32_t pkd[16];
@@ -951,8 +958,9 @@ static int launch_one(const BwdProblem& pr, int which, unsigned int* status, uns
                       int sm_count, cudaStream_t stream, long long timeout_cycles = 0) {
     CUtensorMap mq, mdo, mk, mv;
     const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
-    if (!encode_rows_bf16(&mq, pr.q, q_rows, kD) || !encode_rows_bf16(&mdo, pr.dout, q_rows, kD) ||
-        !encode_rows_bf16(&mk, pr.k, kv_rows, kD) || !encode_rows_bf16(&mv, pr.v, kv_rows, kD))
+    if (!encode_rows_bf16(&mq, pr.q, q_rows, pr.D) ||
+        !encode_rows_bf16(&mdo, pr.dout, q_rows, pr.D) ||
+        !encode_rows_bf16(&mk, pr.k, kv_rows, pr.D) || !encode_rows_bf16(&mv, pr.v, kv_rows, pr.D))
         return RA_ERR_CUDA;
     Params P;
     const int Sb = (int)(pr.S / pr.N);
@@ -974,8 +982,11 @@ static int launch_one(const BwdProblem& pr, int which, unsigned int* status, uns
     if (P.G.n_items <= 0) return RA_OK;
     if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
     const bool st = timeout_cycles > 0;
-    auto kern = which ? (st ? dkv_kernel<true> : dkv_kernel<false>)
-                      : (st ? dq_kernel<true> : dq_kernel<false>);
+    auto kern = pr.D == 64
+                    ? (which ? (st ? dkv_kernel<64, true> : dkv_kernel<64, false>)
+                             : (st ? dq_kernel<64, true> : dq_kernel<64, false>))
+                    : (which ? (st ? dkv_kernel<128, true> : dkv_kernel<128, false>)
+                             : (st ? dq_kernel<128, true> : dq_kernel<128, false>));
     const int smem = which ? dkv::kSmemBytes : dqk::kSmemBytes;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
@@ -988,7 +999,7 @@ static int launch_one(const BwdProblem& pr, int which, unsigned int* status, uns
 }  // namespace tcb
 
 bool tc_bwd_supported(const BwdProblem& p) {
-    if (p.dtype != RA_BF16 || p.D != tcb::kD) return false;
+    if (p.dtype != RA_BF16 || (p.D != 64 && p.D != 128)) return false;
     if (p.S % p.N) return false;
     const int64_t Sb = p.S / p.N;
     if (p.striped == kZigzag && Sb % (2 * tcb::kT)) return false;

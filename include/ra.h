@@ -306,8 +306,8 @@ int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out,
  * dk and dv of shard j travel with the block round the ring in its cyclic
  * order, entering it at device 0 (ra_plan_backward lists the order).
  * Shards and tiles without a visible pair are skipped.
- * Kernels: the tcgen05 tensor-core backward for bf16, D = 128 (any Sb for
- * contiguous and striped shards, Sb % 256 == 0 for zigzag), else the fp32
+ * Kernels: the tcgen05 tensor-core backward for bf16, D in {64, 128} (any Sb
+ * for contiguous and striped shards, Sb % 256 == 0 for zigzag), else the fp32
  * SIMT backward (f32 or bf16, D <= 128).  ra_backward_ex chooses explicitly.
  * Neither uses atomics: for fixed inputs the gradients are the same bits on
  * every call.

@@ -119,6 +119,10 @@ TC_BF16 = [
     (1, 2, 1, 2048, 16, 128, True, 1),   # 16 shards of one tile, striped
     (1, 2, 1, 130, 1, 128, True, 1),     # Sb = 130: ragged, one ring device
     (2, 2, 2, 1536, 3, 128, True, 2),    # zigzag, B = 2, two tiles per chunk
+    (1, 4, 2, 1024, 4, 64, True, 1),     # D = 64: one box per tile, striped GQA
+    (1, 2, 2, 512, 2, 64, False, 0),     # D = 64, non-causal
+    (1, 2, 1, 1000, 4, 64, True, 0),     # D = 64, ragged
+    (1, 2, 1, 2048, 4, 64, True, 2),     # D = 64, zigzag
 ]
 
 
