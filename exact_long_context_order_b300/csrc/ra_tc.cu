@@ -55,7 +55,9 @@ constexpr long long kTimeoutCycles = 4000000000ll;
 constexpr long long kDrainCycles = 400000000ll;
 // Register split: 384 threads launched at 168 registers (64512 in total);
 // warpgroup 0 (producer, MMA, TMEM owner) drops to 80, the two softmax
-// warpgroups rise to 208: 128*80 + 256*208 = 63488 <= 64512.
+// warpgroups rise to 208: 128*80 + 256*208 = 63488 <= 64512.  The softmax
+// writes P and rescales O 16 TMEM columns at a time so that its loop, which
+// holds the S row in 128 registers, does not spill at 208.
 constexpr uint32_t kRegsOther = 80, kRegsSoftmax = 208;
 
 template <int D>
@@ -376,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(C::bItemEmpty + (k & 1)));
             if (item >= G.n_items) break;
             const Item it = decode_item(G, item);
-            const int qt = it.qt[t];
+            const int qt = t ? it.qt[1] : it.qt[0];
+            const int hq = t ? it.h[1] : it.h[0];  // query head of this slot
             const bool valid = (t == 0) || it.valid1;
             float m_used = -INFINITY, l = 0.f;
             int n_logged = 0;
@@ -439,21 +442,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         l *= alpha;
                         if (n > 0) {
+                            // 16 columns at a time: the S row is live in 128 registers here
                             const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-                            for (int c = 0; c < D / 32; ++c) {
-                                uint32_t o[32];
-                                tmem_ld32(o_tm + c * 32, o);
+#pragma unroll 1
+                            for (int c = 0; c < D / 16; ++c) {
+                                uint32_t o[16];
+                                tmem_ld16(o_tm + c * 16, o);
                                 tmem_wait_ld();
                                 reg_fence(o);
 #pragma unroll
-                                for (int e = 0; e < 32; e += 2) {
+                                for (int e = 0; e < 16; e += 2) {
                                     float lo, hi;
                                     f2_unpack(f2_mul(f2_pack_u(o[e], o[e + 1]), a2), lo, hi);
                                     o[e] = __float_as_uint(lo);
                                     o[e + 1] = __float_as_uint(hi);
                                 }
-                                tmem_st32(o_tm + c * 32, o);
+                                tmem_st16(o_tm + c * 16, o);
                             }
                         }
                     }
@@ -461,28 +465,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t nmb2 = f2_pack(-mb, -mb);
                     uint64_t acc0 = 0, acc1 = 0;  // packed fp32 pairs (0.0f, 0.0f)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {  // P half h: keys [64h, 64h + 64)
-                        uint32_t pk[32];
+                    for (int c = 0; c < 4; ++c) {  // keys [32c, 32c + 32) -> P columns [16c, 16c + 16)
+                        uint32_t pk[16];
 #pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            const int c = 2 * h + cc;
-#pragma unroll
-                            for (int e = 0; e < 32; e += 4) {
-                                const uint64_t x01 = f2_fma(f2_pack_u(sr[c][e], sr[c][e + 1]), sl2x2, nmb2);
-                                const uint64_t x23 = f2_fma(f2_pack_u(sr[c][e + 2], sr[c][e + 3]), sl2x2, nmb2);
-                                float a0, a1, a2, a3;
-                                f2_unpack(x01, a0, a1);
-                                f2_unpack(x23, a2, a3);
-                                const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
-                                const float p2 = ex2_approx(a2), p3 = ex2_approx(a3);
-                                acc0 = f2_add(acc0, f2_pack(p0, p1));
-                                acc1 = f2_add(acc1, f2_pack(p2, p3));
-                                pk[cc * 16 + e / 2] = pack_bf16x2(p0, p1);
-                                pk[cc * 16 + e / 2 + 1] = pack_bf16x2(p2, p3);
-                            }
+                        for (int e = 0; e < 32; e += 4) {
+                            const uint64_t x01 = f2_fma(f2_pack_u(sr[c][e], sr[c][e + 1]), sl2x2, nmb2);
+                            const uint64_t x23 = f2_fma(f2_pack_u(sr[c][e + 2], sr[c][e + 3]), sl2x2, nmb2);
+                            float a0, a1, a2, a3;
+                            f2_unpack(x01, a0, a1);
+                            f2_unpack(x23, a2, a3);
+                            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+                            const float p2 = ex2_approx(a2), p3 = ex2_approx(a3);
+                            acc0 = f2_add(acc0, f2_pack(p0, p1));
+                            acc1 = f2_add(acc1, f2_pack(p2, p3));
+                            pk[e / 2] = pack_bf16x2(p0, p1);
+                            pk[e / 2 + 1] = pack_bf16x2(p2, p3);
                         }
-                        tmem_st32(s_tm + 32 * h, pk);
-                        if (h == 0) {  // first 64 keys of P are in TMEM: let P.V start on them
+                        tmem_st16(s_tm + 16 * c, pk);
+                        if (c == 1) {  // first 64 keys of P are in TMEM: let P.V start on them
                             tmem_wait_st();
                             tc_fence_before();
                             __syncwarp();
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(bar(C::bPHi + t));
                 if (LOG && valid && kind != kNone && r == 0) {
                     const int64_t unit =
-                        ((int64_t)(it.b * G.Hq + it.h[t]) * G.rg.N + it.i) * G.rg.nt + qt;
+                        ((int64_t)(it.b * G.Hq + hq) * G.rg.N + it.i) * G.rg.nt + qt;
                     if (n_logged < p.max_entries) {
                         int32_t* e = p.log + (unit * p.max_entries + n_logged) * 4;
                         e[0] = w.s;
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             if (valid) {
-                const int64_t row = (int64_t)(it.b * G.Hq + it.h[t]) * p.S + (int64_t)it.i * p.Sb +
+                const int64_t row = (int64_t)(it.b * G.Hq + hq) * p.S + (int64_t)it.i * p.Sb +
                                     (int64_t)qt * kT + r;
                 // a shard's last tile may hold fewer than 128 real rows
                 const bool row_ok = !RAGGED || qt < G.rg.nt - 1 || r < p.rem;
@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            : -INFINITY;
                 if (LOG && r == 0) {
                     const int64_t unit =
-                        ((int64_t)(it.b * G.Hq + it.h[t]) * G.rg.N + it.i) * G.rg.nt + qt;
+                        ((int64_t)(it.b * G.Hq + hq) * G.rg.N + it.i) * G.rg.nt + qt;
                     p.counts[unit] = n_logged;
                 }
             }
