@@ -25,11 +25,11 @@
 // single kernel reducing dQ across key tiles would cost 5.
 //
 // Both use one CTA per SM (384 threads): warp 0 lane 0 issues TMA copies,
-// lane 0 of two warps issues MMAs (one thread cannot issue a tile's MMAs as
-// fast as the tensor core runs them): warps 1 and 3 in dq_kernel, warps 1
-// and 2 in dkv_kernel, where warp 3 stages the per-row lse and delta of each
-// query tile; warp 2 owns TMEM; warps 4-11 are two warpgroups that split the
-// 128 columns of each score tile.  Every mbarrier
+// lane 0 of two warps issues MMAs (while one issuer waits for a softmax
+// signal, the other's GEMMs keep the tensor core busy): warps 1 and 3 in
+// dq_kernel, warps 1 and 2 in dkv_kernel, where warp 3 stages the per-row lse
+// and delta of each query tile; warp 2 owns TMEM; warps 4-11 are two
+// warpgroups that split the 128 columns of each score tile.  Every mbarrier
 // wait is bounded; on time-out a kernel records kStatusTimeout, drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -283,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuers
         // Lane 0 of warp 1 (A): S(n) into S[n&1], then dQ += dS(n-1) K(n-1) once the
         // softmax has written dS(n-1) over S[(n-1)&1].  Lane 0 of warp 3 (B):
-        // dP(n) into DP once the softmax has read dP(n-1).  Two threads, because
-        // one cannot issue the tile's MMAs as fast as the tensor core runs them.
+        // dP(n) into DP once the softmax has read dP(n-1).  Two threads, so that
+        // one's waits on the softmax overlap the other's GEMMs in the pipe.
         // "S ready" is doubled by tile parity: A may run a tile ahead of B.
         if (lane == 0) {
             const bool is_a = (warp == 1);
@@ -660,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == 2) {
         // ------------------------------------------------------------ MMA issuers
-        // Two issuer threads on disjoint tensor memory, because one thread cannot
-        // issue the tile's 32 MMAs as fast as the tensor core runs them:
+        // Two issuer threads on disjoint tensor memory, so that one's waits on
+        // the softmax overlap the other's GEMMs in the pipe:
         //   lane 0 of warp 1: S^T(n) into S, then dV += P^T(n) dO(n) reading S;
         //   lane 0 of warp 2: dP^T(n) into dP, then dK += dS^T(n) Q(n) reading dP.
         // Each keeps its own in-order reuse (S(n+1) after dV(n), dP(n+1) after
