@@ -84,16 +84,21 @@ int work_slot(unsigned int** slot) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// An empty problem (no batch entry or no token) is valid; nothing is read or
+// written, so its buffer pointers are not checked.
+bool empty_problem(int B, int64_t S) { return B == 0 || S == 0; }
+
 int validate_forward(const void* q, const void* k, const void* v, const void* out,
                      const float* lse, int B, int Hq, int Hkv, int64_t S, int D, int N, int dtype,
                      int layout) {
-    if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || S < 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
     if (S % N != 0 || Hq % Hkv != 0) return RA_ERR_INVALID_ARG;
     if (layout < RA_LAYOUT_CONTIGUOUS || layout > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
     if (layout == RA_LAYOUT_ZIGZAG && (S / N) % 2) return RA_ERR_INVALID_ARG;
     if (dtype != RA_BF16 && dtype != RA_F32) return RA_ERR_INVALID_ARG;
     if (D > 256) return RA_ERR_UNSUPPORTED;
+    if (empty_problem(B, S)) return RA_OK;
+    if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_ALIGN;
     if (lse && !aligned16(lse)) return RA_ERR_ALIGN;
     return RA_OK;
@@ -130,8 +135,10 @@ int prepare_backward(const void* q, const void* k, const void* v, const void* ou
                      ra::BwdProblem* p) {
     int rc = validate_forward(q, k, v, out, nullptr, B, Hq, Hkv, S, D, N, dtype, striped);
     if (rc) return rc;
-    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
     if (D > 128) return RA_ERR_UNSUPPORTED;
+    p->B = B; p->S = S;
+    if (empty_problem(B, S)) return RA_OK;
+    if (!lse || !dout || !dq || !dk || !dv || !workspace) return RA_ERR_INVALID_ARG;
     if (!aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
         !aligned16(dv) || !aligned16(workspace))
         return RA_ERR_ALIGN;
@@ -162,6 +169,7 @@ int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float*
     if (rc) return rc;
     if (kernel != RA_KERNEL_AUTO && kernel != RA_KERNEL_TC && kernel != RA_KERNEL_SIMT)
         return RA_ERR_INVALID_ARG;
+    if (empty_problem(B, S)) return RA_OK;
     unsigned int* status = nullptr;
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
@@ -188,7 +196,7 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
 }
 
 int ra_backward_workspace(int B, int Hq, int64_t S, int D, int64_t* bytes) {
-    if (!bytes || B <= 0 || Hq <= 0 || S <= 0 || D <= 0) return RA_ERR_INVALID_ARG;
+    if (!bytes || B < 0 || Hq <= 0 || S < 0 || D <= 0) return RA_ERR_INVALID_ARG;
     const int64_t wb = backward_workspace_bytes(B, Hq, S, D);
     if (wb < 0) return RA_ERR_INVALID_ARG;
     *bytes = wb;
@@ -206,6 +214,7 @@ int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
     int rc = prepare_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B,
                               Hq, Hkv, S, D, N, causal, striped, scale, dtype, &p);
     if (rc) return rc;
+    if (empty_problem(B, S)) return RA_OK;
     unsigned int* status = nullptr;
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
@@ -238,6 +247,7 @@ int ra_watchdog_selftest_backward(const void* q, const void* k, const void* v, c
     int rc = prepare_backward(q, k, v, out, lse, dout, dq, dk, dv, workspace, workspace_bytes, B,
                               Hq, Hkv, S, D, N, causal, striped, scale, RA_BF16, &p);
     if (rc) return rc;
+    if (empty_problem(B, S)) return RA_ERR_INVALID_ARG;  // the self test needs a kernel to run
     if (!ra::tc_bwd_supported(p)) return RA_ERR_UNSUPPORTED;
     unsigned int* status = nullptr;
     int sms = 0;
@@ -266,11 +276,12 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
                     float* lse_host, void* q_dev, void* k_dev, void* v_dev, void* out_dev,
                     float* lse_dev, int B, int Hq, int Hkv, int64_t S, int D, int N, int causal,
                     int striped, float scale, int dtype, void* stream) {
-    if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID_ARG;
     if ((lse_host != nullptr) != (lse_dev != nullptr)) return RA_ERR_INVALID_ARG;
     int rc = validate_forward(q_dev, k_dev, v_dev, out_dev, lse_dev, B, Hq, Hkv, S, D, N, dtype,
                               striped);
     if (rc) return rc;
+    if (empty_problem(B, S)) return RA_OK;
+    if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID_ARG;
     const int64_t esz = (dtype == RA_F32) ? 4 : 2;
     const int64_t qbytes = (int64_t)B * Hq * S * D * esz, kvbytes = (int64_t)B * Hkv * S * D * esz;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -303,6 +314,7 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
                 int32_t* log, int32_t* counts, int max_entries, void* stream) {
     int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16, striped);
     if (rc) return rc;
+    if (empty_problem(B, S)) return RA_ERR_INVALID_ARG;  // nothing to log
     if (!log || !counts || !aligned16(log) || ((uintptr_t)counts & 3u)) return RA_ERR_INVALID_ARG;
     const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
                                           scale, RA_BF16);
@@ -324,6 +336,7 @@ int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out,
                          float scale, int64_t timeout_cycles, void* stream) {
     int rc = validate_forward(q, k, v, out, lse, B, Hq, Hkv, S, D, N, RA_BF16, striped);
     if (rc) return rc;
+    if (empty_problem(B, S)) return RA_ERR_INVALID_ARG;  // the self test needs a kernel to run
     if (timeout_cycles < 100000 || timeout_cycles > 4000000000ll) return RA_ERR_INVALID_ARG;
     const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
                                           scale, RA_BF16);

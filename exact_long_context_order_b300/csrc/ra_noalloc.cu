@@ -51,10 +51,11 @@ int scratch_address(int dev, unsigned int** addr) {
 extern "C" int ra_forward_noalloc(const void* q, const void* k, const void* v, void* out,
                                   float* lse, int B, int Hq, int Hkv, int64_t S, int D, int N,
                                   int causal, int striped, float scale, void* stream) {
-    if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || S < 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
     if (S % N != 0 || Hq % Hkv != 0) return RA_ERR_INVALID_ARG;
     if (striped < RA_LAYOUT_CONTIGUOUS || striped > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
+    if (B == 0 || S == 0) return RA_OK;  // empty: nothing is read or written
+    if (!q || !k || !v || !out) return RA_ERR_INVALID_ARG;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
                           reinterpret_cast<uintptr_t>(lse);

@@ -95,7 +95,9 @@ enum { RA_FOLD_FULL = 0, RA_FOLD_INCL = 1, RA_FOLD_STRICT = 2 };
  *   out [B, Hq, S, D]  (written)   lse  [B, Hq, S] float32, natural log of the
  *                                  softmax normaliser per query row
  *                                  (written; may be NULL)
- *   B, Hq, Hkv, S, D, N > 0; S % N == 0; Hq % Hkv == 0.
+ *   Hq, Hkv, D, N > 0; B, S >= 0; S % N == 0; Hq % Hkv == 0.  An empty
+ *   problem (B == 0 or S == 0) is a no-op that returns RA_OK without any
+ *   CUDA call; its buffer pointers may then be NULL.
  * Computes, for each query shard i, the fold over ring steps s = 0..N-1 of
  * key/value shard j = (i - s) mod N (glossary page, "Como funciona": the
  * schedule and the numerator/denominator fold; aiunderstanding.org,
@@ -122,8 +124,9 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
  *   ra_forward.
  *   q_dev, k_dev, v_dev, out_dev, lse_dev: device staging buffers of the same
  *   sizes (caller-owned, 16-byte aligned), overwritten.
- * Errors: as ra_forward; RA_ERR_INVALID_ARG for a NULL host pointer or an
- * lse pair with one NULL; RA_ERR_CUDA when a copy cannot be enqueued.
+ * Errors: as ra_forward; RA_ERR_INVALID_ARG for a NULL host pointer (of a
+ * non-empty problem) or an lse pair with one NULL; RA_ERR_CUDA when a copy
+ * cannot be enqueued.
  */
 int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, void* out_host,
                     float* lse_host, void* q_dev, void* k_dev, void* v_dev, void* out_dev,
@@ -256,7 +259,7 @@ int ra_plan_backward(int64_t S, int N, int causal, int striped, int tile, int j,
  *   max_entries >= N * nt.
  * The logging variant computes the same outputs as ra_forward.
  * Errors: as ra_forward, plus RA_ERR_UNSUPPORTED outside the tensor-core
- * kernel's envelope.
+ * kernel's envelope and RA_ERR_INVALID_ARG for an empty problem.
  */
 int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
                 int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
@@ -273,7 +276,8 @@ int ra_fold_log(const void* q, const void* k, const void* v, void* out, float* l
  * hangs and the CUDA context stays usable.  out and lse are left undefined.
  * Returns RA_OK once the launch is enqueued; ra_check(stream) then reports
  * RA_ERR_TIMEOUT.  (Normal launches bound every wait at 4e9 cycles.)
- * Errors: as ra_forward; RA_ERR_INVALID_ARG for timeout_cycles out of range.
+ * Errors: as ra_forward; RA_ERR_INVALID_ARG for timeout_cycles out of range
+ * or an empty problem (the test needs a kernel to run).
  */
 int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out, float* lse,
                          int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped,
@@ -311,6 +315,8 @@ int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out,
  * SIMT backward (f32 or bf16, D <= 128).  ra_backward_ex chooses explicitly.
  * Neither uses atomics: for fixed inputs the gradients are the same bits on
  * every call.
+ * An empty problem (B == 0 or S == 0) is a no-op, as in ra_forward; every
+ * pointer may then be NULL and workspace_bytes 0.
  * Errors: as ra_forward; RA_ERR_CAPACITY when workspace_bytes is too small;
  * RA_ERR_UNSUPPORTED for D > 128.
  */
@@ -329,7 +335,8 @@ int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
 
 /* ra_backward_workspace (host only): bytes of workspace ra_backward needs for
  * the shape: 4*B*Hq*S for delta, rounded up to 256 (D does not enter).
- * Errors: RA_ERR_INVALID_ARG (non-positive sizes or a null bytes pointer). */
+ * Errors: RA_ERR_INVALID_ARG (negative B or S, non-positive Hq or D, or a
+ * null bytes pointer).  An empty problem needs 0 bytes. */
 int ra_backward_workspace(int B, int Hq, int64_t S, int D, int64_t* bytes);
 
 /*
@@ -343,8 +350,8 @@ int ra_backward_workspace(int B, int Hq, int64_t S, int D, int64_t* bytes);
  * status word, lets its copies and MMAs in flight finish, frees its tensor
  * memory and returns.  The gradients are left undefined.  Returns RA_OK once
  * enqueued; ra_check(stream) then reports RA_ERR_TIMEOUT.
- * Errors: as ra_backward; RA_ERR_INVALID_ARG for timeout_cycles out of range
- * or `which` not 0 or 1; RA_ERR_UNSUPPORTED outside the tensor-core shapes.
+ * Errors: as ra_backward; RA_ERR_INVALID_ARG for timeout_cycles out of range,
+ * `which` not 0 or 1 or an empty problem; RA_ERR_UNSUPPORTED outside the tensor-core shapes.
  */
 int ra_watchdog_selftest_backward(const void* q, const void* k, const void* v, const void* out,
                                   const float* lse, const void* dout, void* dq, void* dk,
@@ -381,6 +388,7 @@ int ra_check(void* stream);
  *   All calls share the one array: calls whose kernels may overlap on the GPU
  *   (different streams without ordering between them) race on it.  Order
  *   them on one stream or with events.
+ * An empty problem is a no-op, as in ra_forward.
  * Errors: as ra_forward; RA_ERR_UNSUPPORTED outside the tensor-core shapes;
  * RA_ERR_CAPACITY when the scratch the call needs exceeds the array (one
  * 32-bit counter, so at most 2^31 work items).

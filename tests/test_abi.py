@@ -59,7 +59,8 @@ def test_host_validation_rejects_before_any_device_work(lib):
     assert call(q=None) == ra.RA_ERR_INVALID_ARG
     assert call(S=255) == ra.RA_ERR_INVALID_ARG          # S % N
     assert call(Hq=3, Hkv=2) == ra.RA_ERR_INVALID_ARG    # Hq % Hkv
-    assert call(B=0) == ra.RA_ERR_INVALID_ARG
+    assert call(B=-1) == ra.RA_ERR_INVALID_ARG
+    assert call(N=0, S=0) == ra.RA_ERR_INVALID_ARG
     assert call(D=512) == ra.RA_ERR_UNSUPPORTED
     p2 = ctypes.c_void_p(16 * 1024)
     assert ra.ra_forward(p2, p2, p2, p2, None, 1, 1, 1, 6, 8, 2, 1, 2, 0.0, ra.RA_BF16,
@@ -135,7 +136,9 @@ def test_backward_host_validation(lib):
     assert lib.ra_backward_workspace(2, 4, 1000, 128, ctypes.byref(n)) == ra.RA_OK
     assert n.value == 32000  # delta: 4 bytes for each of 2*4*1000 rows, already 256-aligned
     assert lib.ra_backward_workspace(1, 1, 10, 8, ctypes.byref(n)) == ra.RA_OK and n.value == 256
-    assert lib.ra_backward_workspace(0, 4, 1000, 128, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert lib.ra_backward_workspace(-1, 4, 1000, 128, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert lib.ra_backward_workspace(1, 0, 1000, 128, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert lib.ra_backward_workspace(0, 4, 1000, 128, ctypes.byref(n)) == ra.RA_OK and n.value == 0
     assert lib.ra_backward_workspace(1, 1, 10, 8, None) == ra.RA_ERR_INVALID_ARG
     p = ctypes.c_void_p(16 * 1024)  # never dereferenced: validation fails first
 
@@ -175,3 +178,40 @@ def test_plan_backward_equals_transposed_bruteforce(lib, causal, striped, S, N, 
         for kt in range(nt):
             want = sorted(by_key.get((j, kt), []), key=lambda e: (e[1], e[2]))
             assert ra.plan_backward(S, N, causal, striped, j, kt, tile=T) == want, (j, kt)
+
+
+def test_empty_problems_are_noops_without_a_device(lib):
+    """B == 0 or S == 0: nothing to read or write.  The attention entry points
+    return RA_OK before any CUDA call (this test runs without a GPU), accept
+    NULL buffers, and still reject invalid non-size arguments; the self tests
+    and the fold log, which need a kernel, reject an empty problem."""
+    nul = None
+    for B, S in ((0, 256), (1, 0), (0, 0)):
+        assert ra.ra_forward(nul, nul, nul, nul, nul, B, 2, 1, S, 128, 2, 1, 1, 0.0, ra.RA_BF16,
+                             None) == ra.RA_OK
+        assert ra.ra_forward_ex(nul, nul, nul, nul, nul, B, 2, 1, S, 64, 2, 0, 2, 0.0, ra.RA_F32,
+                                ra.RA_KERNEL_TC, None) == ra.RA_OK
+        assert ra.ra_forward_noalloc(nul, nul, nul, nul, nul, B, 2, 1, S, 128, 2, 1, 1, 0.0,
+                                     None) == ra.RA_OK
+        assert ra.ra_forward_host(nul, nul, nul, nul, nul, nul, nul, nul, nul, nul, B, 2, 1, S,
+                                  128, 2, 1, 1, 0.0, ra.RA_BF16, None) == ra.RA_OK
+        assert ra.ra_backward(*([nul] * 10), 0, B, 2, 1, S, 128, 2, 1, 1, 0.0, ra.RA_BF16,
+                              None) == ra.RA_OK
+        assert ra.ra_watchdog_selftest(nul, nul, nul, nul, nul, B, 2, 1, S, 128, 2, 1, 1, 0.0,
+                                       1 << 20, None) == ra.RA_ERR_INVALID_ARG
+        assert ra.ra_watchdog_selftest_backward(*([nul] * 10), 0, B, 2, 1, S, 128, 2, 1, 1, 0.0,
+                                                1 << 20, 0, None) == ra.RA_ERR_INVALID_ARG
+    # the other arguments are still checked on an empty problem
+    assert ra.ra_forward(nul, nul, nul, nul, nul, 0, 3, 2, 256, 128, 2, 1, 1, 0.0, ra.RA_BF16,
+                         None) == ra.RA_ERR_INVALID_ARG   # Hq % Hkv
+    assert ra.ra_forward(nul, nul, nul, nul, nul, 0, 2, 1, 255, 128, 2, 1, 1, 0.0, ra.RA_BF16,
+                         None) == ra.RA_ERR_INVALID_ARG   # S % N
+    assert ra.ra_forward(nul, nul, nul, nul, nul, 1, 2, 1, 0, 512, 2, 1, 1, 0.0, ra.RA_BF16,
+                         None) == ra.RA_ERR_UNSUPPORTED   # D > 256
+    assert ra.ra_forward(nul, nul, nul, nul, nul, 1, 2, 1, 0, 128, 2, 1, 1, 0.0, 9,
+                         None) == ra.RA_ERR_INVALID_ARG   # dtype
+    assert ra.ra_backward(*([nul] * 10), 0, 0, 2, 1, 256, 192, 2, 1, 1, 0.0, ra.RA_BF16,
+                          None) == ra.RA_ERR_UNSUPPORTED  # backward D > 128
+    # a non-empty problem still needs its buffers
+    assert ra.ra_forward(nul, nul, nul, nul, nul, 1, 2, 1, 256, 128, 2, 1, 1, 0.0, ra.RA_BF16,
+                         None) == ra.RA_ERR_INVALID_ARG

@@ -313,3 +313,23 @@ def test_full_size_sampled_rows(ra, name, n_rows):
     assert torch.isfinite(out.view(-1, wl.D)[:: max(1, wl.S // 3)].float()).all()
     ro, rl = sampled_reference(wl.seed, wl.shapes(), rows, wl.causal, wl.striped, wl.N)
     assert_close(got_o, got_l, ro, rl, "bf16", wl.name)
+
+
+def test_empty_problems_leave_the_stream_usable(ra):
+    """B == 0 or S == 0 through the binding: empty outputs, no error, and the
+    next real call on the same stream still matches the oracle."""
+    import torch
+    for shape_q, shape_kv in (((0, 2, 256, 128), (0, 1, 256, 128)),
+                              ((1, 2, 0, 128), (1, 1, 0, 128))):
+        for dt in (torch.bfloat16, torch.float32):
+            q = torch.empty(shape_q, dtype=dt, device="cuda")
+            k = torch.empty(shape_kv, dtype=dt, device="cuda")
+            out, lse = ra.forward(q, k, k, 2, causal=True, striped=True)
+            assert out.shape == q.shape and lse.shape == shape_q[:3]
+            if dt == torch.bfloat16:
+                dq, dk, dv = ra.backward(q, k, k, out, lse, q, 2, causal=True, striped=True)
+                assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == k.shape
+    ra.check()
+    q, k, v = inputs(9100, 1, 2, 1, 512, 128, "bf16")
+    got = run(ra, q, k, v, 2, True, 1, "bf16")
+    assert_close(*got, *reference(q, k, v, 2, True, 1, "bf16"), "bf16")
