@@ -42,6 +42,8 @@ bool tc_supported(const FwdProblem& p);
 // Device address of the current device's status word (read by ra_check).
 int device_status_word(unsigned int** status);
 int launch_simt(const FwdProblem& p, unsigned int* status, cudaStream_t stream);
+// Host-only envelope checks, made before any CUDA call.
+bool simt_supported(const FwdProblem& p);
 int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_b, int64_t rows,
                  int D, int dtype, cudaStream_t stream);
 // layout: 1 striped, 2 zigzag (0 contiguous is the identity)
@@ -72,6 +74,8 @@ int launch_bwd_delta(const BwdProblem& p, cudaStream_t stream);
 int launch_bwd_simt(const BwdProblem& p, cudaStream_t stream);
 int launch_bwd_dkdv_simt(const BwdProblem& p, cudaStream_t stream);
 bool tc_bwd_supported(const BwdProblem& p);
+bool simt_bwd_supported(const BwdProblem& p);
+bool bwd_delta_supported(const BwdProblem& p);
 // Tensor-core backward (delta already computed): the dq kernel, then the
 // dk/dv kernel, each zeroing the work counter on `stream` before it starts.
 int launch_bwd_tc(const BwdProblem& p, unsigned int* status, unsigned int* work, int sm_count,

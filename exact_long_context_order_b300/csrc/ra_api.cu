@@ -170,15 +170,18 @@ int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float*
     if (kernel != RA_KERNEL_AUTO && kernel != RA_KERNEL_TC && kernel != RA_KERNEL_SIMT)
         return RA_ERR_INVALID_ARG;
     if (empty_problem(B, S)) return RA_OK;
+    const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
+                                          scale, dtype);
+    // the kernels' envelopes are host checks, made before any CUDA call
+    const bool tc_ok = ra::tc_supported(p);
+    if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
+    const bool use_tc = kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok);
+    if (!use_tc && !ra::simt_supported(p)) return RA_ERR_UNSUPPORTED;
     unsigned int* status = nullptr;
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
-    const ra::FwdProblem p = make_problem(q, k, v, out, lse, B, Hq, Hkv, S, D, N, causal, striped,
-                                          scale, dtype);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool tc_ok = ra::tc_supported(p);
-    if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
-    if (kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok)) {
+    if (use_tc) {
         unsigned int* work = nullptr;
         if ((rc = work_slot(&work))) return rc;
         rc = ra::launch_tc(p, nullptr, status, work, sms, st);
@@ -215,17 +218,21 @@ int ra_backward_ex(const void* q, const void* k, const void* v, const void* out,
                               Hq, Hkv, S, D, N, causal, striped, scale, dtype, &p);
     if (rc) return rc;
     if (empty_problem(B, S)) return RA_OK;
+    // the kernels' envelopes are host checks, made before any CUDA call
+    const bool tc_ok = ra::tc_bwd_supported(p);
+    if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
+    const bool use_tc = kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok);
+    if (!ra::bwd_delta_supported(p) || (!use_tc && !ra::simt_bwd_supported(p)))
+        return RA_ERR_UNSUPPORTED;
     unsigned int* status = nullptr;
     int sms = 0;
     if ((rc = device_state(&status, &sms))) return rc;
-    const bool tc_ok = ra::tc_bwd_supported(p);
-    if (kernel == RA_KERNEL_TC && !tc_ok) return RA_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if ((rc = ra::launch_bwd_delta(p, st))) {
         if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
         return rc;
     }
-    if (kernel == RA_KERNEL_TC || (kernel == RA_KERNEL_AUTO && tc_ok)) {
+    if (use_tc) {
         unsigned int* work = nullptr;
         if ((rc = work_slot(&work))) return rc;
         rc = ra::launch_bwd_tc(p, status, work, sms, st);

@@ -307,6 +307,16 @@ int launch_simt_d(const BwdProblem& pr, cudaStream_t stream) {
 
 }  // namespace bwd
 
+bool bwd_delta_supported(const BwdProblem& p) {
+    return ((int64_t)p.B * p.Hq * p.S + 7) / 8 <= 0x7fffffff;
+}
+
+bool simt_bwd_supported(const BwdProblem& p) {
+    // grids (row blocks, N, B*Hq) and (row blocks, N, B*Hkv)
+    return p.D <= 128 && (int64_t)p.B * p.Hq <= 65535 && (int64_t)p.B * p.Hkv <= 65535 &&
+           p.N <= 65535 && (p.S / p.N + 127) / 128 <= 0x7fffffff;
+}
+
 int launch_bwd_delta(const BwdProblem& p, cudaStream_t stream) {
     const int64_t rows = (int64_t)p.B * p.Hq * p.S;
     if (rows == 0) return RA_OK;

@@ -154,10 +154,14 @@ static int launch_d(const FwdProblem& pr, cudaStream_t stream) {
 
 }  // namespace simt
 
+bool simt_supported(const FwdProblem& p) {
+    // grid (row blocks, N, B*Hq): y and z are limited to 65535
+    return p.D <= 256 && (int64_t)p.B * p.Hq <= 65535 && p.N <= 65535 &&
+           (p.S / p.N + 127) / 128 <= 0x7fffffff;
+}
+
 int launch_simt(const FwdProblem& p, unsigned int* /*status*/, cudaStream_t stream) {
-    if (p.D > 256) return RA_ERR_UNSUPPORTED;
-    if ((int64_t)p.B * p.Hq > 65535 || p.N > 65535 || (p.S / p.N + 127) / 128 > 0x7fffffff)
-        return RA_ERR_UNSUPPORTED;
+    if (!simt_supported(p)) return RA_ERR_UNSUPPORTED;
     return p.dtype == RA_F32 ? simt::launch_d<float>(p, stream)
                              : simt::launch_d<__nv_bfloat16>(p, stream);
 }

@@ -105,7 +105,10 @@ enum { RA_FOLD_FULL = 0, RA_FOLD_INCL = 1, RA_FOLD_STRICT = 2 };
  * Under causal masking whole shards and key tiles with no visible pair are
  * skipped, never computed.
  * Errors: RA_ERR_INVALID_ARG, RA_ERR_ALIGN (q, k, v, out, lse not 16-byte
- * aligned), RA_ERR_UNSUPPORTED (D > 256, device not sm_103), RA_ERR_CUDA.
+ * aligned), RA_ERR_UNSUPPORTED (D > 256, device not sm_103, or a shape that
+ * no kernel takes: the tensor-core kernel needs B*Hq*S and B*Hkv*S below 2^31
+ * rows, the SIMT kernel B*Hq and N at most 65535; decided on the host before
+ * any CUDA call), RA_ERR_CUDA.
  */
 int ra_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq,
                int Hkv, int64_t S, int D, int N, int causal, int striped, float scale, int dtype,

@@ -215,3 +215,25 @@ def test_empty_problems_are_noops_without_a_device(lib):
     # a non-empty problem still needs its buffers
     assert ra.ra_forward(nul, nul, nul, nul, nul, 1, 2, 1, 256, 128, 2, 1, 1, 0.0, ra.RA_BF16,
                          None) == ra.RA_ERR_INVALID_ARG
+
+
+def test_size_limits_are_rejected_before_any_device_work(lib):
+    """Problems beyond a kernel's envelope (int32 TMA row coordinates, 65535
+    grid rows) are refused on the host, before any CUDA call: this test runs
+    without a GPU and passes placeholder pointers that are never touched."""
+    p = ctypes.c_void_p(16 * 1024)
+    fwd = lambda B, Hq, Hkv, S, D, N, kernel: ra.ra_forward_ex(
+        p, p, p, p, None, B, Hq, Hkv, S, D, N, 1, 1, 0.0, ra.RA_BF16, kernel, None)
+    # B*Hq*S = 2^31 rows: past the tensor-core kernel's int32 row coordinates
+    assert fwd(1, 1 << 14, 1, 1 << 17, 128, 16, ra.RA_KERNEL_TC) == ra.RA_ERR_UNSUPPORTED
+    # ... and B*Hq = 65536 query heads: past the SIMT kernel's grid, so no kernel fits
+    assert fwd(1, 1 << 16, 1, 1 << 15, 128, 8, ra.RA_KERNEL_AUTO) == ra.RA_ERR_UNSUPPORTED
+    # N = 65536 ring devices: past the SIMT kernel's grid
+    assert fwd(1, 1, 1, 1 << 16, 128, 1 << 16, ra.RA_KERNEL_SIMT) == ra.RA_ERR_UNSUPPORTED
+    # D = 256 is SIMT-only; the tensor-core kernel refuses it
+    assert fwd(1, 2, 1, 256, 256, 2, ra.RA_KERNEL_TC) == ra.RA_ERR_UNSUPPORTED
+    bwd = lambda B, Hq, Hkv, S, D, N, kernel: ra.ra_backward_ex(
+        *([p] * 10), 1 << 40, B, Hq, Hkv, S, D, N, 1, 1, 0.0, ra.RA_BF16, kernel, None)
+    assert bwd(1, 1 << 14, 1, 1 << 17, 128, 16, ra.RA_KERNEL_TC) == ra.RA_ERR_UNSUPPORTED
+    assert bwd(1, 1 << 16, 1, 1 << 15, 128, 8, ra.RA_KERNEL_AUTO) == ra.RA_ERR_UNSUPPORTED
+    assert bwd(1, 2, 1, 256, 32, 2, ra.RA_KERNEL_TC) == ra.RA_ERR_UNSUPPORTED  # D = 32
