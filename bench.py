@@ -529,8 +529,9 @@ def main():
 
     # ------------------------------------------------ end to end: host buffers through the C ABI
     # ra_forward_host per step: H2D copies of q, k, v, the forward, D2H of out
-    # and lse, all on one stream.  Steps alternate between two streams with two
-    # device staging sets, so one step's copies overlap the other's kernel.
+    # and lse, pipelined inside the call over chunks of KV-head groups.  Steps
+    # also alternate between two streams with two device staging sets, so one
+    # step's copies may overlap the other's kernel.
     e2e = None
     if not args.no_e2e:
         hdt = torch.int16 if wl.dtype == "bf16" else torch.float32
@@ -574,7 +575,9 @@ def main():
         e2e = {"value": aggregate_rate(world, flops, args.steps, e_ms) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e_ms / args.steps,
-               "how": "ra_forward_host per step, two streams and staging sets alternating"}
+               "how": "ra_forward_host per step (each call pipelines 8 chunks of KV-head "
+                      "groups: copies in, forward, copies out); two caller streams and "
+                      "staging sets alternate between steps"}
         # the e2e outputs must equal the device-resident run (same inputs)
         for oh in outs_h:
             if not torch.equal(oh.to("cuda").view(dtype), out):

@@ -3,6 +3,7 @@
 // point returns an RA_* status and never throws.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -156,6 +157,54 @@ int prepare_backward(const void* q, const void* k, const void* v, const void* ou
     return RA_OK;
 }
 
+// ra_forward_host's pipeline: per device, a host-to-device copy stream, a
+// device-to-host copy stream, two compute streams and the events that order
+// them.  Created on first use and kept for the life of the process.  The
+// enqueue sequence of one call holds g_pipe_mu, because every call re-records
+// the same events.
+constexpr int kHostChunks = 8;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr, comp[2] = {nullptr, nullptr};
+    cudaEvent_t fork = nullptr, join = nullptr, in[kHostChunks] = {}, done[kHostChunks] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[kMaxDevices];
+
+// The current device's pipeline; the caller holds g_pipe_mu.
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) { note_cuda(e); return RA_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    HostPipe& hp = g_pipe[dev];
+    if (!hp.ready) {
+        const unsigned sf = cudaStreamNonBlocking, ef = cudaEventDisableTiming;
+        cudaStream_t* streams[4] = {&hp.h2d, &hp.d2h, &hp.comp[0], &hp.comp[1]};
+        for (cudaStream_t* st : streams)
+            if (!*st && (e = cudaStreamCreateWithFlags(st, sf)) != cudaSuccess) {
+                note_cuda(e);
+                return RA_ERR_CUDA;
+            }
+        cudaEvent_t* events[2 + 2 * kHostChunks];
+        int n = 0;
+        events[n++] = &hp.fork;
+        events[n++] = &hp.join;
+        for (int c = 0; c < kHostChunks; ++c) {
+            events[n++] = &hp.in[c];
+            events[n++] = &hp.done[c];
+        }
+        for (int j = 0; j < n; ++j)
+            if (!*events[j] && (e = cudaEventCreateWithFlags(events[j], ef)) != cudaSuccess) {
+                note_cuda(e);
+                return RA_ERR_CUDA;
+            }
+        hp.ready = true;
+    }
+    *out = &hp;
+    return RA_OK;
+}
+
 }  // namespace
 
 int ra::device_status_word(unsigned int** status) { return device_state(status, nullptr); }
@@ -290,29 +339,86 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
     if (empty_problem(B, S)) return RA_OK;
     if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID_ARG;
     const int64_t esz = (dtype == RA_F32) ? 4 : 2;
-    const int64_t qbytes = (int64_t)B * Hq * S * D * esz, kvbytes = (int64_t)B * Hkv * S * D * esz;
+    const int64_t G = (int64_t)B * Hkv;  // (batch, KV head) groups
+    const int nch = (G >= 4 && G <= 0x7fffffff) ? (int)std::min<int64_t>(G, kHostChunks) : 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if ((e = cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(k_dev, k_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(v_dev, v_host, kvbytes, cudaMemcpyHostToDevice, st)) != cudaSuccess) {
-        note_cuda(e);
+    auto fail = [](cudaError_t err) {
+        note_cuda(err);
         return RA_ERR_CUDA;
+    };
+    if (nch == 1) {  // too few groups to pipeline: everything in order on the caller's stream
+        const int64_t qbytes = (int64_t)B * Hq * S * D * esz, kvbytes = G * S * D * esz;
+        if ((e = cudaMemcpyAsync(q_dev, q_host, qbytes, cudaMemcpyHostToDevice, st)) ||
+            (e = cudaMemcpyAsync(k_dev, k_host, kvbytes, cudaMemcpyHostToDevice, st)) ||
+            (e = cudaMemcpyAsync(v_dev, v_host, kvbytes, cudaMemcpyHostToDevice, st)))
+            return fail(e);
+        if ((rc = ra_forward_ex(q_dev, k_dev, v_dev, out_dev, lse_dev, B, Hq, Hkv, S, D, N, causal,
+                                striped, scale, dtype, RA_KERNEL_AUTO, stream)))
+            return rc;
+        if ((e = cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, st)))
+            return fail(e);
+        if (lse_host && (e = cudaMemcpyAsync(lse_host, lse_dev, (int64_t)B * Hq * S * 4,
+                                             cudaMemcpyDeviceToHost, st)))
+            return fail(e);
+        return RA_OK;
     }
-    if ((rc = ra_forward_ex(q_dev, k_dev, v_dev, out_dev, lse_dev, B, Hq, Hkv, S, D, N, causal,
-                            striped, scale, dtype, RA_KERNEL_AUTO, stream)))
-        return rc;
-    if ((e = cudaMemcpyAsync(out_host, out_dev, qbytes, cudaMemcpyDeviceToHost, st)) !=
-        cudaSuccess) {
-        note_cuda(e);
-        return RA_ERR_CUDA;
+    // Pipelined over chunks of consecutive (batch, KV head) groups.  A group's
+    // q heads, k, v, out and lse rows are contiguous, so a chunk is itself a
+    // problem (B' = its groups, Hq' = Hq / Hkv, Hkv' = 1) and the same kernels
+    // compute the same bits for it.  Chunk c's copies in run on the h2d
+    // stream, its forward on compute stream c % 2 (so a chunk's kernel can
+    // start on the SMs that the previous chunk's tail frees), its copies out
+    // on the d2h stream; all three are forked from and joined back to the
+    // caller's stream.
+    const ra::FwdProblem full = make_problem(q_dev, k_dev, v_dev, out_dev, lse_dev, B, Hq, Hkv, S,
+                                             D, N, causal, striped, scale, dtype);
+    if (!ra::tc_supported(full) && !ra::simt_supported(full)) return RA_ERR_UNSUPPORTED;
+    if ((rc = device_state(nullptr, nullptr))) return rc;
+    std::lock_guard<std::mutex> lk(g_pipe_mu);
+    HostPipe* hp = nullptr;
+    if ((rc = host_pipe(&hp))) return rc;
+    if ((e = cudaEventRecord(hp->fork, st))) return fail(e);
+    for (cudaStream_t s2 : {hp->h2d, hp->d2h, hp->comp[0], hp->comp[1]})
+        if ((e = cudaStreamWaitEvent(s2, hp->fork, 0))) return fail(e);
+    const int g = Hq / Hkv;
+    const int64_t qg = (int64_t)g * S * D * esz, kvg = S * D * esz, lg = (int64_t)g * S;
+    char* qd = static_cast<char*>(q_dev);
+    char* kd = static_cast<char*>(k_dev);
+    char* vd = static_cast<char*>(v_dev);
+    char* od = static_cast<char*>(out_dev);
+    const char* qh = static_cast<const char*>(q_host);
+    const char* kh = static_cast<const char*>(k_host);
+    const char* vh = static_cast<const char*>(v_host);
+    char* oh = static_cast<char*>(out_host);
+    for (int c = 0; c < nch; ++c) {
+        const int64_t g0 = G * c / nch, m = G * (c + 1) / nch - g0;
+        if ((e = cudaMemcpyAsync(qd + g0 * qg, qh + g0 * qg, m * qg, cudaMemcpyHostToDevice,
+                                 hp->h2d)) ||
+            (e = cudaMemcpyAsync(kd + g0 * kvg, kh + g0 * kvg, m * kvg, cudaMemcpyHostToDevice,
+                                 hp->h2d)) ||
+            (e = cudaMemcpyAsync(vd + g0 * kvg, vh + g0 * kvg, m * kvg, cudaMemcpyHostToDevice,
+                                 hp->h2d)) ||
+            (e = cudaEventRecord(hp->in[c], hp->h2d)))
+            return fail(e);
+        cudaStream_t cs = hp->comp[c & 1];
+        if ((e = cudaStreamWaitEvent(cs, hp->in[c], 0))) return fail(e);
+        if ((rc = ra_forward_ex(qd + g0 * qg, kd + g0 * kvg, vd + g0 * kvg, od + g0 * qg,
+                                lse_dev ? lse_dev + g0 * lg : nullptr, (int)m, g, 1, S, D, N,
+                                causal, striped, scale, dtype, RA_KERNEL_AUTO, cs)))
+            return rc;
+        if ((e = cudaEventRecord(hp->done[c], cs)) ||
+            (e = cudaStreamWaitEvent(hp->d2h, hp->done[c], 0)) ||
+            (e = cudaMemcpyAsync(oh + g0 * qg, od + g0 * qg, m * qg, cudaMemcpyDeviceToHost,
+                                 hp->d2h)))
+            return fail(e);
+        if (lse_host && (e = cudaMemcpyAsync(lse_host + g0 * lg, lse_dev + g0 * lg, m * lg * 4,
+                                             cudaMemcpyDeviceToHost, hp->d2h)))
+            return fail(e);
     }
-    if (lse_host &&
-        (e = cudaMemcpyAsync(lse_host, lse_dev, (int64_t)B * Hq * S * 4, cudaMemcpyDeviceToHost,
-                             st)) != cudaSuccess) {
-        note_cuda(e);
-        return RA_ERR_CUDA;
-    }
+    // every compute launch precedes a copy out, so the d2h stream's end joins all
+    if ((e = cudaEventRecord(hp->join, hp->d2h)) || (e = cudaStreamWaitEvent(st, hp->join, 0)))
+        return fail(e);
     return RA_OK;
 }
 

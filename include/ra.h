@@ -115,13 +115,21 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
                void* stream);
 
 /*
- * ra_forward_host: ra_forward on host tensors.  Enqueues on `stream` the
- * copies of q, k, v from host to the caller's device staging buffers, the
- * forward, and the copies of out (and lse, when lse_host is not NULL) back to
- * the host.  Asynchronous: the host buffers must stay valid until the stream
- * reaches the end of the call; page-locked (pinned) host memory makes the
- * copies asynchronous and lets successive calls on two streams with two
- * staging sets overlap one call's copies with the other's kernel.
+ * ra_forward_host: ra_forward on host tensors.  Enqueues the copies of q, k,
+ * v from host to the caller's device staging buffers, the forward, and the
+ * copies of out (and lse, when lse_host is not NULL) back to the host.
+ * With at least four (batch, KV head) groups (B*Hkv >= 4) the call pipelines
+ * up to eight chunks of consecutive groups: chunk c+1's copies in overlap
+ * chunk c's forward, and chunk c's copies out overlap later chunks'.  That
+ * work runs on streams the library creates for the device on first use (one
+ * copy stream per direction, two compute streams, kept until the process
+ * exits), forked from `stream` at the start of the call and joined back into
+ * it at the end, so `stream` orders the whole call as if it ran there; the
+ * outputs are the bits ra_forward computes.  Concurrent calls from several
+ * host threads are serialised while they enqueue.  Fewer groups run in order
+ * on `stream` itself.  Asynchronous: the host buffers must stay valid until
+ * `stream` reaches the end of the call; page-locked (pinned) host memory
+ * makes the copies asynchronous.
  *   q_host, k_host, v_host (read), out_host, lse_host (written; lse_host may
  *   be NULL, then lse_dev must be NULL too): host memory with the layouts of
  *   ra_forward.

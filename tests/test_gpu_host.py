@@ -49,3 +49,41 @@ def test_forward_host_equals_device_forward(ra):
     assert ra.ra_forward_host(P(hq), P(hk), P(hv), P(out_h), P(lse_h), *[P(x) for x in stage[:4]],
                               None, B, Hq, Hkv, S, D, N, 1, 1, 0.0, ra.RA_BF16,
                               None) == ra.RA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,N,D,dt", [
+    (2, 8, 4, 1024, 4, 128, "bf16"),    # 8 (batch, KV head) groups: one per chunk
+    (2, 10, 5, 512, 2, 64, "bf16"),     # 10 groups over 8 chunks: uneven chunks
+    (1, 12, 4, 1000, 4, 128, "bf16"),   # ragged shards (Sb = 250), 4 groups
+    (1, 4, 4, 256, 2, 32, "f32"),       # the SIMT kernel, 4 groups
+])
+def test_pipelined_forward_host_equals_device_forward(ra, B, Hq, Hkv, S, N, D, dt):
+    """With at least four (batch, KV head) groups the call pipelines chunks of
+    groups over internal copy and compute streams: same bits as ra.forward."""
+    import torch
+    q, k, v = inputs(8300 + S + Hq, B, Hq, Hkv, S, D, dt)
+    tq, tk, tv = (to_device(x, dt) for x in (q, k, v))
+    out0, lse0 = ra.forward(tq, tk, tv, N, causal=True, striped=1)
+    ra.check()
+    view = np.int16 if dt == "bf16" else np.float32
+    hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(x).view(view)).pin_memory()
+                  for x in (q, k, v))
+    out_h = torch.zeros(hq.shape, dtype=hq.dtype).pin_memory()
+    lse_h = torch.zeros((B, Hq, S), dtype=torch.float32).pin_memory()
+    stage = [torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv),
+             torch.empty_like(tq), torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")]
+    P = ra._ptr
+    dtype = ra.RA_BF16 if dt == "bf16" else ra.RA_F32
+    side = torch.cuda.Stream()
+    for with_lse in (True, False):
+        out_h.zero_()
+        lse_args = (P(lse_h), P(stage[4])) if with_lse else (None, None)
+        rc = ra.ra_forward_host(P(hq), P(hk), P(hv), P(out_h), lse_args[0],
+                                *[P(x) for x in stage[:4]], lse_args[1], B, Hq, Hkv, S, D, N,
+                                1, 1, 0.0, dtype, ra._stream_handle(side))
+        assert rc == ra.RA_OK, ra.ra_strerror(rc)
+        assert ra.ra_check(ra._stream_handle(side)) == ra.RA_OK
+        ref = out0.view(torch.int16) if dt == "bf16" else out0
+        assert torch.equal(out_h, ref.cpu())
+        if with_lse:
+            assert torch.equal(lse_h, lse0.cpu())
