@@ -58,6 +58,13 @@ def test_toy_f32_workload(ra):
     (1, 2, 1, 256, 8, 200, True, True),
     (1, 1, 1, 7, 1, 5, True, False),
     (1, 1, 1, 1, 1, 8, True, True),
+    # register-blocked kernel (D % 4 == 0, D <= 128): several 64-row blocks and
+    # 32-key chunks, ragged shards, every layout, D padded up to 32/64/128
+    (1, 2, 1, 1000, 4, 128, True, True),    # Sb = 250
+    (2, 2, 2, 640, 5, 32, False, False),    # Sb = 128
+    (1, 4, 2, 512, 4, 64, True, 2),         # zigzag
+    (1, 2, 1, 300, 3, 100, True, False),    # D = 100 in the 128 variant; Sb = 100
+    (1, 1, 1, 96, 2, 4, True, True),        # D = 4, smallest
 ])
 def test_simt_f32_grid(ra, B, Hq, Hkv, S, N, D, causal, striped):
     q, k, v = inputs(11 + S + D, B, Hq, Hkv, S, D, "f32")
