@@ -87,3 +87,43 @@ def test_pipelined_forward_host_equals_device_forward(ra, B, Hq, Hkv, S, N, D, d
         assert torch.equal(out_h, ref.cpu())
         if with_lse:
             assert torch.equal(lse_h, lse0.cpu())
+
+
+def test_pipelined_calls_on_two_streams_reuse_staging_safely(ra):
+    """Three calls with different inputs alternate between two caller streams
+    and two staging sets, with no host synchronisation between them: call 3
+    reuses call 1's staging set, so its uploads must wait for call 1's
+    downloads (the call is ordered on its caller's stream).  Every output is
+    the device forward of its own inputs."""
+    import torch
+    B, Hq, Hkv, S, N, D = 1, 8, 4, 1024, 4, 128
+    P = ra._ptr
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    stages = [[torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((B, Hkv, S, D), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((B, Hkv, S, D), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")] for _ in range(2)]
+    calls = []
+    for n in range(3):
+        q, k, v = inputs(8400 + n, B, Hq, Hkv, S, D, "bf16")
+        host = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+                for x in (q, k, v)]
+        out_h = torch.zeros((B, Hq, S, D), dtype=torch.int16).pin_memory()
+        lse_h = torch.zeros((B, Hq, S), dtype=torch.float32).pin_memory()
+        calls.append((q, k, v, host, out_h, lse_h))
+    torch.cuda.synchronize()
+    for n, (q, k, v, host, out_h, lse_h) in enumerate(calls):
+        st = streams[n % 2]
+        rc = ra.ra_forward_host(*[P(x) for x in host], P(out_h), P(lse_h),
+                                *[P(x) for x in stages[n % 2]], B, Hq, Hkv, S, D, N, 1, 1, 0.0,
+                                ra.RA_BF16, ra._stream_handle(st))
+        assert rc == ra.RA_OK, ra.ra_strerror(rc)
+    for st in streams:
+        assert ra.ra_check(ra._stream_handle(st)) == ra.RA_OK
+    for q, k, v, host, out_h, lse_h in calls:
+        tq, tk, tv = (to_device(x, "bf16") for x in (q, k, v))
+        out0, lse0 = ra.forward(tq, tk, tv, N, causal=True, striped=1)
+        ra.check()
+        assert torch.equal(out_h, out0.view(torch.int16).cpu())
+        assert torch.equal(lse_h, lse0.cpu())
