@@ -261,6 +261,332 @@ __global__ void __launch_bounds__(kRows) dkdv_kernel(const T* __restrict__ q,
         }
 }
 
+// ---------------------------------------------------------------- tiled kernels (D % 4 == 0, D <= 128)
+// Register-blocked versions of the two kernels above, for D % 4 == 0 and
+// D <= 128 (DMAX = 32, 64 or 128, D padded by zeros); the fold orders are
+// the same.  A block holds 64 rows of its own side (query rows for dq, key
+// rows for dk/dv) transposed in shared memory and streams the other side in
+// chunks of 32 rows, stored row-major in rows padded to DMAX + 4 floats.
+// Thread (rg, kg) = (tid / 8, tid % 8) computes the 4 x 4 products of its
+// rows 4rg..4rg+3 with chunk rows kg, kg+8, kg+16, kg+24 (the padding puts
+// the eight kg lanes on different bank groups), and accumulates its rows'
+// gradients on dims {32t + 4kg + e}.
+constexpr int kTR = 64;       // rows of the block's own side
+constexpr int kTK = 32;       // rows per chunk of the other side
+constexpr int kTThreads = 128;
+
+__device__ __forceinline__ void load4_f(const float* p, float* x) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+}
+__device__ __forceinline__ void load4_f(const __nv_bfloat16* p, float* x) {
+    const uint2 t = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(t.x << 16); x[1] = __uint_as_float(t.x & 0xffff0000u);
+    x[2] = __uint_as_float(t.y << 16); x[3] = __uint_as_float(t.y & 0xffff0000u);
+}
+__device__ __forceinline__ void store4_f(float* p, const float* x) {
+    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+}
+__device__ __forceinline__ void store4_f(__nv_bfloat16* p, const float* x) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 t;
+    t.x = *reinterpret_cast<const uint32_t*>(&a);
+    t.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(p) = t;
+}
+
+// rows [r0, r0 + 64) of a [rows, D] matrix, transposed into dst[DMAX][64]
+// and multiplied by mul; rows at or past `valid` and dims past D are zero
+template <typename T, int DMAX>
+__device__ __forceinline__ void stage_transposed(float (*dst)[kTR], const T* src, int64_t r0,
+                                                 int64_t valid, int D, float mul) {
+    for (int e = threadIdx.x; e < kTR * (DMAX / 4); e += kTThreads) {
+        const int r = e % kTR, d4 = e / kTR;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r0 + r < valid && 4 * d4 < D) load4_f(src + (r0 + r) * D + 4 * d4, x);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) dst[4 * d4 + a][r] = x[a] * mul;
+    }
+}
+// rows [c0, c0 + n) of a [rows, D] matrix into dst[32][DMAX + 4]; the rest zero
+template <typename T, int DMAX>
+__device__ __forceinline__ void stage_rows(float (*dst)[DMAX + 4], const T* src, int64_t c0, int n,
+                                           int D) {
+    for (int e = threadIdx.x; e < kTK * (DMAX / 4); e += kTThreads) {
+        const int d4 = e % (DMAX / 4), r = e / (DMAX / 4);
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < n && 4 * d4 < D) load4_f(src + (c0 + r) * D + 4 * d4, x);
+        store4_f(&dst[r][4 * d4], x);
+    }
+}
+// acc[a][c] += sum_d A[d][4rg + a] * Brows[kg + 8c][d]
+template <int DMAX>
+__device__ __forceinline__ void block_products(float (&acc)[4][4], const float (*A)[kTR],
+                                               const float (*Brows)[DMAX + 4], int rg, int kg) {
+#pragma unroll 2
+    for (int d4 = 0; d4 < DMAX / 4; ++d4) {
+        float av[4][4], bv[4][4];  // [dim][row], [chunk row][dim]
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 t = *reinterpret_cast<const float4*>(&A[4 * d4 + e][4 * rg]);
+            av[e][0] = t.x; av[e][1] = t.y; av[e][2] = t.z; av[e][3] = t.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float4 t = *reinterpret_cast<const float4*>(&Brows[kg + 8 * c][4 * d4]);
+            bv[c][0] = t.x; bv[c][1] = t.y; bv[c][2] = t.z; bv[c][3] = t.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(av[e][a], bv[c][e], acc[a][c]);
+    }
+}
+
+template <int DMAX>
+struct DqSmem {
+    float qt[DMAX][kTR];        // scale * q, transposed
+    float gt[DMAX][kTR];        // dout, transposed
+    float ks[kTK][DMAX + 4];    // k rows of the chunk
+    float vs[kTK][DMAX + 4];    // v rows of the chunk
+    float ps[kTR][kTK + 1];     // dS of the chunk
+};
+
+template <typename T, int DMAX>
+__global__ void __launch_bounds__(kTThreads)
+    dq_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                    const T* __restrict__ dout, const float* __restrict__ lse,
+                    const float* __restrict__ delta, T* __restrict__ dq, const Params p) {
+    constexpr int DPT = DMAX / 8;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    DqSmem<DMAX>& sm = *reinterpret_cast<DqSmem<DMAX>*>(smem_raw);
+    const int tid = threadIdx.x, rg = tid >> 3, kg = tid & 7;
+    const int i = blockIdx.y;   // query shard
+    const int bh = blockIdx.z;  // b * Hq + h
+    const int b = bh / p.Hq, h = bh % p.Hq, kvh = h / p.g;
+    const int64_t r0 = (int64_t)blockIdx.x * kTR;
+    const int64_t N = p.N, Sb = p.Sb;
+    const int D = p.D;
+    const int64_t r_last = (r0 + kTR - 1 < Sb) ? r0 + kTR - 1 : Sb - 1;
+    const int64_t qpos_last = token_pos(p, i, r_last);
+    const int64_t rowbase = (int64_t)bh * p.S + i * Sb;
+    int64_t qpos[4];
+    float L[4], dl[4];
+    bool rok[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int64_t r = r0 + 4 * rg + a;
+        qpos[a] = token_pos(p, i, r);
+        L[a] = (r < Sb) ? lse[rowbase + r] : -INFINITY;
+        dl[a] = (r < Sb) ? delta[rowbase + r] : 0.f;
+        rok[a] = r < Sb && L[a] > -INFINITY;
+    }
+    stage_transposed<T, DMAX>(sm.qt, q + rowbase * D, r0, Sb, D, p.scale);
+    stage_transposed<T, DMAX>(sm.gt, dout + rowbase * D, r0, Sb, D, 1.f);
+    float acc[4][DPT];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int d = 0; d < DPT; ++d) acc[a][d] = 0.f;
+    const T* kbase = k + ((int64_t)b * p.Hkv + kvh) * p.S * D;
+    const T* vbase = v + ((int64_t)b * p.Hkv + kvh) * p.S * D;
+
+    for (int s = 0; s < p.N; ++s) {
+        const int j = (int)((i - s + N) % N);
+        for (int64_t c0 = 0; c0 < Sb; c0 += kTK) {
+            if (p.causal && token_pos(p, j, c0) > qpos_last) break;  // keys ascend in a shard
+            const int nk = (int)((Sb - c0 < kTK) ? Sb - c0 : kTK);
+            __syncthreads();  // the previous chunk's reads are done
+            stage_rows<T, DMAX>(sm.ks, kbase + j * Sb * D, c0, nk, D);
+            stage_rows<T, DMAX>(sm.vs, vbase + j * Sb * D, c0, nk, D);
+            __syncthreads();
+            float sc[4][4], dp[4][4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc[a][c] = dp[a][c] = 0.f;
+            block_products<DMAX>(sc, sm.qt, sm.ks, rg, kg);
+            block_products<DMAX>(dp, sm.gt, sm.vs, rg, kg);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int key = kg + 8 * c;
+                const int64_t kpos = token_pos(p, j, c0 + key);
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const bool vis = rok[a] && key < nk && !(p.causal && kpos > qpos[a]);
+                    sm.ps[4 * rg + a][key] = vis ? expf(sc[a][c] - L[a]) * (dp[a][c] - dl[a]) : 0.f;
+                }
+            }
+            __syncthreads();
+            // dq += dS k on dims {32t + 4kg + e}
+#pragma unroll 4
+            for (int key = 0; key < kTK; ++key) {
+                float dsr[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) dsr[a] = sm.ps[4 * rg + a][key];
+#pragma unroll
+                for (int t = 0; t < DPT / 4; ++t) {
+                    const float4 kk = *reinterpret_cast<const float4*>(&sm.ks[key][32 * t + 4 * kg]);
+                    const float kx[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+                    for (int a = 0; a < 4; ++a)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            acc[a][4 * t + e] = fmaf(dsr[a], kx[e], acc[a][4 * t + e]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int64_t r = r0 + 4 * rg + a;
+        if (r >= Sb) continue;
+#pragma unroll
+        for (int t = 0; t < DPT / 4; ++t) {
+            const int d0 = 32 * t + 4 * kg;
+            if (d0 >= D) continue;
+            float x[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[e] = rok[a] ? acc[a][4 * t + e] * p.scale : 0.f;
+            store4_f(dq + (rowbase + r) * D + d0, x);
+        }
+    }
+}
+
+template <int DMAX>
+struct DkvSmem {
+    float kt[DMAX][kTR];        // scale * k, transposed (the block's keys)
+    float vt[DMAX][kTR];        // v, transposed
+    float qs[kTK][DMAX + 4];    // q rows of the chunk
+    float gs[kTK][DMAX + 4];    // dout rows of the chunk
+    float pt[kTR][kTK + 1];     // P^T of the chunk
+    float dst[kTR][kTK + 1];    // dS^T of the chunk
+    float ls[kTK], dls[kTK];    // lse and delta of the chunk's query rows
+};
+
+template <typename T, int DMAX>
+__global__ void __launch_bounds__(kTThreads)
+    dkdv_tiled_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                      const T* __restrict__ dout, const float* __restrict__ lse,
+                      const float* __restrict__ delta, T* __restrict__ dk, T* __restrict__ dv,
+                      const Params p) {
+    constexpr int DPT = DMAX / 8;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    DkvSmem<DMAX>& sm = *reinterpret_cast<DkvSmem<DMAX>*>(smem_raw);
+    const int tid = threadIdx.x, rg = tid >> 3, kg = tid & 7;
+    const int j = blockIdx.y;   // key/value shard
+    const int bk = blockIdx.z;  // b * Hkv + kv head
+    const int b = bk / p.Hkv, kvh = bk % p.Hkv;
+    const int64_t u0 = (int64_t)blockIdx.x * kTR;
+    const int64_t N = p.N, Sb = p.Sb;
+    const int D = p.D;
+    const int64_t kpos_first = token_pos(p, j, u0);  // smallest key position of the block
+    const int64_t keybase = (int64_t)bk * p.S + j * Sb;
+    int64_t kpos[4];
+    bool kok[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int64_t u = u0 + 4 * rg + a;
+        kpos[a] = token_pos(p, j, u);
+        kok[a] = u < Sb;
+    }
+    stage_transposed<T, DMAX>(sm.kt, k + keybase * D, u0, Sb, D, p.scale);
+    stage_transposed<T, DMAX>(sm.vt, v + keybase * D, u0, Sb, D, 1.f);
+    float dka[4][DPT], dva[4][DPT];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int d = 0; d < DPT; ++d) dka[a][d] = dva[a][d] = 0.f;
+
+    for (int s = 0; s < p.N; ++s) {
+        const int i = (int)((j + s) % N);  // query shard the block visits at step s
+        for (int gi = 0; gi < p.g; ++gi) {
+            const int64_t bh = (int64_t)b * p.Hq + (int64_t)kvh * p.g + gi;
+            const int64_t qbase = bh * p.S + i * Sb;
+            for (int64_t c0 = 0; c0 < Sb; c0 += kTK) {
+                const int nq = (int)((Sb - c0 < kTK) ? Sb - c0 : kTK);
+                // query positions ascend within a shard: a chunk whose last
+                // row precedes every key of the block has no visible pair
+                if (p.causal && token_pos(p, i, c0 + nq - 1) < kpos_first) continue;
+                __syncthreads();  // the previous chunk's reads are done
+                stage_rows<T, DMAX>(sm.qs, q + qbase * D, c0, nq, D);
+                stage_rows<T, DMAX>(sm.gs, dout + qbase * D, c0, nq, D);
+                if (tid < kTK) {
+                    sm.ls[tid] = (tid < nq) ? lse[qbase + c0 + tid] : -INFINITY;
+                    sm.dls[tid] = (tid < nq) ? delta[qbase + c0 + tid] : 0.f;
+                }
+                __syncthreads();
+                float sc[4][4], dp[4][4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) sc[a][c] = dp[a][c] = 0.f;
+                block_products<DMAX>(sc, sm.kt, sm.qs, rg, kg);
+                block_products<DMAX>(dp, sm.vt, sm.gs, rg, kg);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int qq = kg + 8 * c;
+                    const int64_t qpos = token_pos(p, i, c0 + qq);
+                    const float Lq = sm.ls[qq], dq_ = sm.dls[qq];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        const bool vis = kok[a] && qq < nq && Lq > -INFINITY &&
+                                         !(p.causal && qpos < kpos[a]);
+                        const float pe = vis ? expf(sc[a][c] - Lq) : 0.f;
+                        sm.pt[4 * rg + a][qq] = pe;
+                        sm.dst[4 * rg + a][qq] = pe * (dp[a][c] - dq_);
+                    }
+                }
+                __syncthreads();
+                // dv += P^T dout, dk += dS^T q on dims {32t + 4kg + e}
+#pragma unroll 2
+                for (int qq = 0; qq < kTK; ++qq) {
+                    float pr[4], dr[4];
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        pr[a] = sm.pt[4 * rg + a][qq];
+                        dr[a] = sm.dst[4 * rg + a][qq];
+                    }
+#pragma unroll
+                    for (int t = 0; t < DPT / 4; ++t) {
+                        const float4 gg = *reinterpret_cast<const float4*>(&sm.gs[qq][32 * t + 4 * kg]);
+                        const float4 q4 = *reinterpret_cast<const float4*>(&sm.qs[qq][32 * t + 4 * kg]);
+                        const float gx[4] = {gg.x, gg.y, gg.z, gg.w}, qx[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                        for (int a = 0; a < 4; ++a)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                dva[a][4 * t + e] = fmaf(pr[a], gx[e], dva[a][4 * t + e]);
+                                dka[a][4 * t + e] = fmaf(dr[a], qx[e], dka[a][4 * t + e]);
+                            }
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        const int64_t u = u0 + 4 * rg + a;
+        if (u >= Sb) continue;
+#pragma unroll
+        for (int t = 0; t < DPT / 4; ++t) {
+            const int d0 = 32 * t + 4 * kg;
+            if (d0 >= D) continue;
+            float x[4], y[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[e] = dka[a][4 * t + e] * p.scale;
+                y[e] = dva[a][4 * t + e];
+            }
+            store4_f(dk + (keybase + u) * D + d0, x);
+            store4_f(dv + (keybase + u) * D + d0, y);
+        }
+    }
+}
+
 Params make_params(const BwdProblem& pr) {
     Params P;
     P.B = pr.B; P.Hq = pr.Hq; P.Hkv = pr.Hkv; P.g = pr.Hq / pr.Hkv; P.N = pr.N; P.D = pr.D;
@@ -298,8 +624,36 @@ int launch_dkdv_t(const BwdProblem& pr, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
+template <typename T, int DMAX>
+int launch_tiled_t(const BwdProblem& pr, cudaStream_t stream) {
+    const Params P = make_params(pr);
+    const unsigned bx = (unsigned)((P.Sb + kTR - 1) / kTR);
+    const size_t s1 = sizeof(DqSmem<DMAX>), s2 = sizeof(DkvSmem<DMAX>);
+    auto k1 = dq_tiled_kernel<T, DMAX>;
+    auto k2 = dkdv_tiled_kernel<T, DMAX>;
+    if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2) !=
+            cudaSuccess)
+        return RA_ERR_CUDA;
+    k1<<<dim3(bx, pr.N, pr.B * pr.Hq), kTThreads, s1, stream>>>(
+        static_cast<const T*>(pr.q), static_cast<const T*>(pr.k), static_cast<const T*>(pr.v),
+        static_cast<const T*>(pr.dout), pr.lse, pr.delta, static_cast<T*>(pr.dq), P);
+    if (cudaGetLastError() != cudaSuccess) return RA_ERR_CUDA;
+    k2<<<dim3(bx, pr.N, pr.B * pr.Hkv), kTThreads, s2, stream>>>(
+        static_cast<const T*>(pr.q), static_cast<const T*>(pr.k), static_cast<const T*>(pr.v),
+        static_cast<const T*>(pr.dout), pr.lse, pr.delta, static_cast<T*>(pr.dk),
+        static_cast<T*>(pr.dv), P);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
 template <typename T>
 int launch_simt_d(const BwdProblem& pr, cudaStream_t stream) {
+    if (pr.D % 4 == 0) {  // the register-blocked kernels
+        if (pr.D <= 32) return launch_tiled_t<T, 32>(pr, stream);
+        if (pr.D <= 64) return launch_tiled_t<T, 64>(pr, stream);
+        return launch_tiled_t<T, 128>(pr, stream);
+    }
     if (pr.D <= 32) return launch_simt_t<T, 32>(pr, stream);
     if (pr.D <= 64) return launch_simt_t<T, 64>(pr, stream);
     return launch_simt_t<T, 128>(pr, stream);
@@ -314,7 +668,7 @@ bool bwd_delta_supported(const BwdProblem& p) {
 bool simt_bwd_supported(const BwdProblem& p) {
     // grids (row blocks, N, B*Hq) and (row blocks, N, B*Hkv)
     return p.D <= 128 && (int64_t)p.B * p.Hq <= 65535 && (int64_t)p.B * p.Hkv <= 65535 &&
-           p.N <= 65535 && (p.S / p.N + 127) / 128 <= 0x7fffffff;
+           p.N <= 65535 && (p.S / p.N + bwd::kTR - 1) / bwd::kTR <= 0x7fffffff;
 }
 
 int launch_bwd_delta(const BwdProblem& p, cudaStream_t stream) {

@@ -48,6 +48,10 @@ SIMT_F32 = [
     (1, 2, 1, 256, 4, 32, True, 2),
     (1, 1, 1, 7, 1, 5, True, 0),
     (1, 1, 1, 1, 1, 8, True, 1),
+    # register-blocked kernels: several 64-row blocks, ragged shards, zigzag
+    (1, 2, 1, 1000, 4, 128, True, 1),   # Sb = 250
+    (2, 4, 2, 640, 5, 64, False, 0),    # Sb = 128
+    (1, 2, 2, 512, 4, 32, True, 2),     # zigzag
 ]
 
 
