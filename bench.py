@@ -48,6 +48,9 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-configs", action="store_true",
+                    help="time the float64 oracle in full on configs 0-2 on all host cores, "
+                         "comparing every row with the library's output; one JSON line each")
     ap.add_argument("--op", default="forward",
                     choices=["forward", "backward", "merge", "stripe", "f32", "ulysses"],
                     help="forward: the ring-attention step (default); backward: ra_backward "
@@ -204,6 +207,7 @@ def cpu_oracle_sample(wl, seconds):
     t_total = 0.0
     kv_cache = {}
     scale = 1.0 / math.sqrt(D)
+    kept_rows, kept_o, kept_l = [], [], []
     for c0 in range(0, len(rows), 32):
         if t_total >= seconds:
             break
@@ -225,12 +229,42 @@ def cpu_oracle_sample(wl, seconds):
             qq = oracle.bf16_bits_to_f64(ragen.normal_bf16_rows(wl.seed, ragen.TENSOR_Q, qidx, D))
             qpos = pos[[pp for (_, _, pp) in rr]]
             t0 = time.perf_counter()
-            oracle.attend_rows(qq, qpos, kk, vv, pos, wl.causal, scale)
+            o, l = oracle.attend_rows(qq, qpos, kk, vv, pos, wl.causal, scale)
             t_total += time.perf_counter() - t0
+            kept_rows += rr
+            kept_o.append(o)
+            kept_l.append(l)
             vis = (qpos + 1) if wl.causal else np.full(len(rr), S)
             flops += float(4.0 * D * vis.sum())
             done += len(rr)
-    return {"flops": flops, "seconds": t_total, "rows": done, "threads": threads}
+    return {"flops": flops, "seconds": t_total, "rows": done, "threads": threads,
+            "sample_rows": kept_rows,
+            "o": np.concatenate(kept_o) if kept_o else np.zeros((0, D)),
+            "lse": np.concatenate(kept_l) if kept_l else np.zeros(0)}
+
+
+def parity_block(r, out, lse, wl):
+    """Compares the device output on the rows the CPU-baseline sample
+    computed with the oracle (outside the timed region)."""
+    import torch
+    rows = r["sample_rows"]
+    if not rows:
+        return None
+    idx = torch.tensor([(b * wl.Hq + h) * wl.S + p for (b, h, p) in rows], device=out.device)
+    got_o = out.view(-1, wl.D)[idx].double().cpu().numpy()
+    got_l = lse.view(-1)[idx].double().cpu().numpy()
+    d = np.abs(got_o - r["o"])
+    return {"max_abs": float(d.max()), "mean_abs": float(d.mean()),
+            "lse_max_abs": float(np.abs(got_l - r["lse"]).max()), "rows": len(rows),
+            "tol": {"max_abs": 2e-2, "mean_abs": 2e-3, "lse_max_abs": 2e-3},
+            "rows_from": "the cpu_baseline sample (stratified over heads and shards)"}
+
+
+def main_config(wl, world):
+    """The `config` object of the forward bench line (both arms)."""
+    return dict(wl.describe(), parallelism=f"replicas{world}",
+                l2="inputs larger than L2 (no flush)",
+                flops_per_step=wl.flops(), flops_exact_per_step=wl.flops_exact())
 
 
 def reference_arm(args, wl):
@@ -253,7 +287,7 @@ def reference_arm(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(wl.describe(), parallelism=f"replicas{args.gpus}"),
+        "config": main_config(wl, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"float64 NumPy oracle (plain softmax attention per row) on "
                                    f"{rows} stratified query rows per step of {wl.name}, each "
@@ -264,6 +298,114 @@ def reference_arm(args, wl):
     print(json.dumps(line), flush=True)
     return 0
 
+
+
+# ---------------------------------------------------------------- full oracle on configs 0-2
+CPU_CONFIGS = ("toy_f32", "noncausal_8k", "causal_32k_contig", "causal_32k_striped")
+
+
+def _oracle_slice(task):
+    """One (batch, query head) slice of a workload through the float64 oracle
+    (plain full attention, every row), in a spawned worker with one BLAS
+    thread, compared with the device's output for that slice.  Returns
+    (oracle seconds, max-abs, sum-abs, elements, lse max-abs)."""
+    name, b, h, got_o, got_l = task
+    import oracle
+    import ragen
+    wl = ragen.WORKLOADS[name]
+    S, D, N = wl.S, wl.D, wl.N
+    g = wl.Hq // wl.Hkv
+
+    def slab(tid, H, hh):
+        n, start = S * D, (b * H + hh) * S * D
+        if wl.dtype == "bf16":
+            x = oracle.bf16_bits_to_f64(ragen.normal_bf16(wl.seed, tid, n, start=start))
+        else:
+            x = ragen.normal_f32(wl.seed, tid, n, start=start).astype(np.float64)
+        return oracle.to_token_order(x.reshape(S, D), N, wl.striped)[None, None]
+
+    q = slab(ragen.TENSOR_Q, wl.Hq, h)
+    k = slab(ragen.TENSOR_K, wl.Hkv, h // g)
+    v = slab(ragen.TENSOR_V, wl.Hkv, h // g)
+    t0 = time.perf_counter()
+    o, lse = oracle.full_attention(q, k, v, wl.causal)
+    dt = time.perf_counter() - t0
+    o = oracle.to_shard_major(o[0, 0], N, wl.striped)
+    lse = oracle.to_shard_major(lse[0, 0][:, None], N, wl.striped)[:, 0]
+    if wl.dtype == "bf16":
+        got = oracle.bf16_bits_to_f64(got_o.view(np.uint16))
+    else:
+        got = got_o.astype(np.float64)
+    d = np.abs(got - o)
+    return dt, float(d.max()), float(d.sum()), int(d.size), float(np.abs(got_l - lse).max())
+
+
+def cpu_configs_arm(args):
+    """The float64 oracle in full (every query row) on configs 0-2, on all
+    host cores (one spawned worker per core, each over whole (batch, head)
+    slices), each compared row by row with the library's output for the same
+    inputs.  Prints one JSON line per workload."""
+    import multiprocessing as mp
+
+    import torch
+
+    import exact_long_context_order_b300 as ra
+    import ragen
+    if not torch.cuda.is_available():
+        raise SystemExit("--cpu-configs compares with the GPU output and needs a CUDA device")
+    torch.cuda.set_device(0)
+    ra.lib()
+    cores = len(os.sched_getaffinity(0))
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"  # the workers' BLAS: one thread each, one worker per core
+    ctx = mp.get_context("spawn")
+    cpu_model = ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                cpu_model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    with ctx.Pool(cores) as pool:
+        pool.map(abs, range(cores))  # start every worker before timing
+        for name in CPU_CONFIGS:
+            wl = ragen.WORKLOADS[name]
+            qs, kvs = wl.shapes()
+            dev = []
+            for tid, shape in ((ragen.TENSOR_Q, qs), (ragen.TENSOR_K, kvs),
+                               (ragen.TENSOR_V, kvs)):
+                if wl.dtype == "bf16":
+                    x = ragen.normal_bf16(wl.seed, tid, int(np.prod(shape))).reshape(shape)
+                    dev.append(torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16))
+                else:
+                    x = ragen.normal_f32(wl.seed, tid, int(np.prod(shape))).reshape(shape)
+                    dev.append(torch.from_numpy(x).cuda())
+            out, lse = ra.forward(*dev, wl.N, causal=wl.causal, striped=wl.striped)
+            ra.check()
+            o_h = (out.view(torch.int16) if wl.dtype == "bf16" else out).cpu().numpy()
+            l_h = lse.double().cpu().numpy()
+            tasks = [(name, b, h, o_h[b, h], l_h[b, h]) for b in range(wl.B)
+                     for h in range(wl.Hq)]
+            t0 = time.perf_counter()
+            res = pool.map(_oracle_slice, tasks, chunksize=1)
+            wall = time.perf_counter() - t0
+            n_el = sum(r[3] for r in res)
+            line = {
+                "cpu_oracle_full": wl.name, "value": wl.flops() / wall / 1e12, "unit": "TFLOP/s",
+                "cores": cores, "cpu_model": cpu_model, "wall_s": wall,
+                "oracle_cpu_s": sum(r[0] for r in res), "config": wl.describe(),
+                "how": "float64 NumPy oracle (oracle.full_attention, every row) per (batch, "
+                       "head) slice in spawned workers, one per core, one BLAS thread each; "
+                       "value = the metric's FLOPs (4*B*Hq*S^2*D, halved if causal) / wall "
+                       "time of all slices",
+                "parity": {"rows": wl.B * wl.Hq * wl.S, "max_abs": max(r[1] for r in res),
+                           "mean_abs": sum(r[2] for r in res) / n_el,
+                           "lse_max_abs": max(r[4] for r in res),
+                           "against": "the library's forward (ra_forward) on the same inputs"},
+            }
+            print(json.dumps(line), flush=True)
+    return 0
 
 
 # ---------------------------------------------------------------- helper kernels
@@ -448,6 +590,8 @@ def main():
     args = parse()
     import ragen
     wl = ragen.WORKLOADS[args.workload]
+    if args.cpu_configs:
+        return cpu_configs_arm(args)
     if args.impl == "reference":
         return reference_arm(args, wl)
     if args.op == "backward":
@@ -600,9 +744,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": dict(wl.describe(), parallelism=f"replicas{world}",
-                       l2="inputs larger than L2 (no flush)",
-                       flops_per_step=flops, flops_exact_per_step=wl.flops_exact()),
+        "config": main_config(wl, world),
         "tokens_per_s": tok_s,
         "frac_of_bf16_peak": value / world / peak,
         "gpu_launches": args.steps,
@@ -621,6 +763,7 @@ def main():
     }
     if world == 1 and not args.no_cpu_baseline:
         r = cpu_oracle_sample(wl, args.cpu_seconds)
+        line["parity"] = parity_block(r, out, lse, wl)
         line["cpu_baseline"] = {
             "value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["threads"],
             "kind": "oracle",

@@ -37,7 +37,9 @@ _SIGNATURES = {
     "ra_stripe": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _vp], _i32),
     "ra_relayout": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _i32, _vp], _i32),
     "ra_ulysses_exchange": ([_vp, _vp, _i32, _i32, _i64, _i32, _i64, _i32, _vp], _i32),
-    "ra_plan": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)], _i32),
+    "ra_plan": ([_i64, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)], _i32),
+    "ra_plan_tile": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)],
+                     _i32),
     "ra_plan_backward": ([_i64, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _i64, _c.POINTER(_i64)],
                          _i32),
     "ra_fold_log": ([_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
@@ -121,8 +123,12 @@ def ra_ulysses_exchange(src, dst, B, H, S, N, row_bytes, inverse, stream):
     return lib().ra_ulysses_exchange(src, dst, B, H, S, N, row_bytes, inverse, stream)
 
 
-def ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items):
-    return lib().ra_plan(S, N, causal, striped, tile, i, qt, items, cap, n_items)
+def ra_plan(S, N, causal, striped, tile, items, cap, n_items):
+    return lib().ra_plan(S, N, causal, striped, tile, items, cap, n_items)
+
+
+def ra_plan_tile(S, N, causal, striped, tile, i, qt, items, cap, n_items):
+    return lib().ra_plan_tile(S, N, causal, striped, tile, i, qt, items, cap, n_items)
 
 
 def ra_plan_backward(S, N, causal, striped, tile, j, kt, items, cap, n_items):
@@ -369,12 +375,22 @@ def ulysses_exchange(x, N: int, inverse: bool = False, out=None, stream=None):
 def plan(S: int, N: int, causal: bool, striped: bool, i: int, qt: int, tile: int = 128):
     """Host-side fold list of query tile (i, qt): list of (s, j, kt, kind)."""
     n = _i64()
-    _check(ra_plan(S, N, int(causal), int(striped), tile, i, qt, None, 0, ctypes.byref(n)),
-           "ra_plan")
+    _check(ra_plan_tile(S, N, int(causal), int(striped), tile, i, qt, None, 0, ctypes.byref(n)),
+           "ra_plan_tile")
     buf = (ctypes.c_int32 * (4 * max(1, n.value)))()
-    _check(ra_plan(S, N, int(causal), int(striped), tile, i, qt, buf, n.value, ctypes.byref(n)),
-           "ra_plan")
+    _check(ra_plan_tile(S, N, int(causal), int(striped), tile, i, qt, buf, n.value,
+                        ctypes.byref(n)), "ra_plan_tile")
     return [tuple(buf[4 * e:4 * e + 4]) for e in range(n.value)]
+
+
+def plan_schedule(S: int, N: int, causal: bool, striped, tile: int = 128):
+    """The whole fold schedule: list of (i, qt, s, j, kt, kind) in order."""
+    n = _i64()
+    _check(ra_plan(S, N, int(causal), int(striped), tile, None, 0, ctypes.byref(n)), "ra_plan")
+    buf = (ctypes.c_int32 * (6 * max(1, n.value)))()
+    _check(ra_plan(S, N, int(causal), int(striped), tile, buf, n.value, ctypes.byref(n)),
+           "ra_plan")
+    return [tuple(buf[6 * e:6 * e + 6]) for e in range(n.value)]
 
 
 def plan_backward(S: int, N: int, causal: bool, striped, j: int, kt: int, tile: int = 128):

@@ -41,6 +41,11 @@ int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, un
 bool tc_supported(const FwdProblem& p);
 // Device address of the current device's status word (read by ra_check).
 int device_status_word(unsigned int** status);
+// The current device's status word address and SM count, resolved once per
+// device (RA_ERR_UNSUPPORTED unless the device is sm_103).
+int device_info(unsigned int** status, int* sm_count);
+// Keeps the text of a CUDA error for ra_strerror(RA_ERR_CUDA) (per thread).
+void note_cuda_error(cudaError_t e);
 int launch_simt(const FwdProblem& p, unsigned int* status, cudaStream_t stream);
 // Host-only envelope checks, made before any CUDA call.
 bool simt_supported(const FwdProblem& p);

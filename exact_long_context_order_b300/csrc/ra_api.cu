@@ -167,6 +167,8 @@ struct HostPipe {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr, comp[2] = {nullptr, nullptr};
     cudaEvent_t fork = nullptr, join = nullptr, in[kHostChunks] = {}, done[kHostChunks] = {};
+    // one event per side stream, recorded only when a call fails part-way
+    cudaEvent_t unwind[4] = {};
 };
 std::mutex g_pipe_mu;
 HostPipe g_pipe[kMaxDevices];
@@ -186,10 +188,11 @@ int host_pipe(HostPipe** out) {
                 note_cuda(e);
                 return RA_ERR_CUDA;
             }
-        cudaEvent_t* events[2 + 2 * kHostChunks];
+        cudaEvent_t* events[6 + 2 * kHostChunks];
         int n = 0;
         events[n++] = &hp.fork;
         events[n++] = &hp.join;
+        for (cudaEvent_t& u : hp.unwind) events[n++] = &u;
         for (int c = 0; c < kHostChunks; ++c) {
             events[n++] = &hp.in[c];
             events[n++] = &hp.done[c];
@@ -208,6 +211,8 @@ int host_pipe(HostPipe** out) {
 }  // namespace
 
 int ra::device_status_word(unsigned int** status) { return device_state(status, nullptr); }
+int ra::device_info(unsigned int** status, int* sm_count) { return device_state(status, sm_count); }
+void ra::note_cuda_error(cudaError_t e) { note_cuda(e); }
 
 extern "C" {
 
@@ -340,7 +345,18 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
     if (!q_host || !k_host || !v_host || !out_host) return RA_ERR_INVALID_ARG;
     const int64_t esz = (dtype == RA_F32) ? 4 : 2;
     const int64_t G = (int64_t)B * Hkv;  // (batch, KV head) groups
-    const int nch = (G >= 4 && G <= 0x7fffffff) ? (int)std::min<int64_t>(G, kHostChunks) : 1;
+    int nch = (G >= 4 && G <= 0x7fffffff) ? (int)std::min<int64_t>(G, kHostChunks) : 1;
+    const int g = Hq / Hkv;
+    const int64_t qg = (int64_t)g * S * D * esz, kvg = S * D * esz, lg = (int64_t)g * S;
+    // Every chunk is a sub-problem whose device pointers must meet ra_forward's
+    // 16-byte rule; if one chunk's offset would not, run the call in order.
+    for (int c = 1; c < nch; ++c) {
+        const int64_t g0 = G * c / nch;
+        if ((g0 * qg) % 16 || (g0 * kvg) % 16 || (lse_dev && (g0 * lg * 4) % 16)) {
+            nch = 1;
+            break;
+        }
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     auto fail = [](cudaError_t err) {
@@ -379,10 +395,28 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
     HostPipe* hp = nullptr;
     if ((rc = host_pipe(&hp))) return rc;
     if ((e = cudaEventRecord(hp->fork, st))) return fail(e);
-    for (cudaStream_t s2 : {hp->h2d, hp->d2h, hp->comp[0], hp->comp[1]})
-        if ((e = cudaStreamWaitEvent(s2, hp->fork, 0))) return fail(e);
-    const int g = Hq / Hkv;
-    const int64_t qg = (int64_t)g * S * D * esz, kvg = S * D * esz, lg = (int64_t)g * S;
+    const cudaStream_t side[4] = {hp->h2d, hp->d2h, hp->comp[0], hp->comp[1]};
+    for (int x = 0; x < 4; ++x)
+        if ((e = cudaStreamWaitEvent(side[x], hp->fork, 0))) {
+            // the streams forked so far hold no work yet; join them anyway
+            for (int y = 0; y < x; ++y)
+                if (cudaEventRecord(hp->unwind[y], side[y]) == cudaSuccess)
+                    cudaStreamWaitEvent(st, hp->unwind[y], 0);
+            return fail(e);
+        }
+    // After the fork, a failure part-way must still make the caller's stream
+    // wait for whatever was enqueued on the side streams (copies and kernels
+    // that use the caller's buffers), so `stream` keeps ordering the call.
+    auto unwind = [&](int code) {
+        for (int y = 0; y < 4; ++y)
+            if (cudaEventRecord(hp->unwind[y], side[y]) == cudaSuccess)
+                cudaStreamWaitEvent(st, hp->unwind[y], 0);
+        return code;
+    };
+    auto fail_joined = [&](cudaError_t err) {
+        note_cuda(err);
+        return unwind(RA_ERR_CUDA);
+    };
     char* qd = static_cast<char*>(q_dev);
     char* kd = static_cast<char*>(k_dev);
     char* vd = static_cast<char*>(v_dev);
@@ -400,25 +434,25 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
             (e = cudaMemcpyAsync(vd + g0 * kvg, vh + g0 * kvg, m * kvg, cudaMemcpyHostToDevice,
                                  hp->h2d)) ||
             (e = cudaEventRecord(hp->in[c], hp->h2d)))
-            return fail(e);
+            return fail_joined(e);
         cudaStream_t cs = hp->comp[c & 1];
-        if ((e = cudaStreamWaitEvent(cs, hp->in[c], 0))) return fail(e);
+        if ((e = cudaStreamWaitEvent(cs, hp->in[c], 0))) return fail_joined(e);
         if ((rc = ra_forward_ex(qd + g0 * qg, kd + g0 * kvg, vd + g0 * kvg, od + g0 * qg,
                                 lse_dev ? lse_dev + g0 * lg : nullptr, (int)m, g, 1, S, D, N,
                                 causal, striped, scale, dtype, RA_KERNEL_AUTO, cs)))
-            return rc;
+            return unwind(rc);
         if ((e = cudaEventRecord(hp->done[c], cs)) ||
             (e = cudaStreamWaitEvent(hp->d2h, hp->done[c], 0)) ||
             (e = cudaMemcpyAsync(oh + g0 * qg, od + g0 * qg, m * qg, cudaMemcpyDeviceToHost,
                                  hp->d2h)))
-            return fail(e);
+            return fail_joined(e);
         if (lse_host && (e = cudaMemcpyAsync(lse_host + g0 * lg, lse_dev + g0 * lg, m * lg * 4,
                                              cudaMemcpyDeviceToHost, hp->d2h)))
-            return fail(e);
+            return fail_joined(e);
     }
     // every compute launch precedes a copy out, so the d2h stream's end joins all
     if ((e = cudaEventRecord(hp->join, hp->d2h)) || (e = cudaStreamWaitEvent(st, hp->join, 0)))
-        return fail(e);
+        return fail_joined(e);
     return RA_OK;
 }
 
@@ -525,8 +559,8 @@ int ra_ulysses_exchange(const void* src, void* dst, int B, int H, int64_t S, int
     return rc;
 }
 
-int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, int32_t* items,
-            int64_t cap, int64_t* n_items) {
+int ra_plan_tile(int64_t S, int N, int causal, int striped, int tile, int i, int qt,
+                 int32_t* items, int64_t cap, int64_t* n_items) {
     if (!n_items || S <= 0 || N <= 0 || tile < 2 || S % N) return RA_ERR_INVALID_ARG;
     if (striped < RA_LAYOUT_CONTIGUOUS || striped > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
     const int64_t Sb = S / N;
@@ -552,6 +586,39 @@ int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, 
             ++n;
         }
     }
+    *n_items = n;
+    return (items && n > cap) ? RA_ERR_CAPACITY : RA_OK;
+}
+
+int ra_plan(int64_t S, int N, int causal, int striped, int tile, int32_t* items, int64_t cap,
+            int64_t* n_items) {
+    if (!n_items || S <= 0 || N <= 0 || tile < 2 || S % N) return RA_ERR_INVALID_ARG;
+    if (striped < RA_LAYOUT_CONTIGUOUS || striped > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
+    const int64_t Sb = S / N;
+    if (striped == RA_LAYOUT_ZIGZAG && Sb % (2 * tile)) return RA_ERR_INVALID_ARG;
+    const int64_t nt = (Sb + tile - 1) / tile;
+    if (nt > 0x7fffffff) return RA_ERR_INVALID_ARG;
+    ra::RingGeom g{N, (int)nt, causal ? 1 : 0, striped};
+    int64_t n = 0;
+    for (int i = 0; i < N; ++i)
+        for (int qt = 0; qt < (int)nt; ++qt)
+            for (int s = 0; s < N; ++s) {
+                const int j = ((i - s) % N + N) % N;
+                int nk = 0, dk = 0;
+                ra::shard_span(g, i, j, qt, &nk, &dk);
+                for (int kt = 0; kt < nk; ++kt) {
+                    if (items && n < cap) {
+                        int32_t* e = items + n * 6;
+                        e[0] = i;
+                        e[1] = qt;
+                        e[2] = s;
+                        e[3] = j;
+                        e[4] = kt;
+                        e[5] = ra::fold_kind(g, i, j, qt, kt);
+                    }
+                    ++n;
+                }
+            }
     *n_items = n;
     return (items && n > cap) ? RA_ERR_CAPACITY : RA_OK;
 }

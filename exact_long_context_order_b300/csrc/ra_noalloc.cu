@@ -39,7 +39,11 @@ int scratch_address(int dev, unsigned int** addr) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return RA_ERR_CUDA;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            ra::note_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+            return RA_ERR_CUDA;
+        }
         g_scratch_addr[dev] = static_cast<unsigned int*>(p);
     }
     *addr = g_scratch_addr[dev];
@@ -78,21 +82,23 @@ extern "C" int ra_forward_noalloc(const void* q, const void* k, const void* v, v
     if (need_bytes > kNoAllocScratchBytes || items_bound >= (int64_t)1 << 31)
         return RA_ERR_CAPACITY;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return RA_ERR_CUDA;
-    if (major != 10 || minor != 3) return RA_ERR_UNSUPPORTED;
-    unsigned int* scratch = nullptr;
-    int rc = scratch_address(dev, &scratch);
-    if (rc) return rc;
+    // status word, SM count and architecture (sm_103 only), resolved once per device
     unsigned int* status = nullptr;
-    if ((rc = ra::device_status_word(&status))) return rc;
+    int sms = 0;
+    int rc = ra::device_info(&status, &sms);
+    if (rc) return rc;
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        ra::note_cuda_error(e);
+        return RA_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return RA_ERR_UNSUPPORTED;
+    unsigned int* scratch = nullptr;
+    if ((rc = scratch_address(dev, &scratch))) return rc;
     // launch_tc zeroes the counter on `stream` before the kernel starts, so the
     // previous call's final count never leaks into this one.
-    return ra::launch_tc(p, nullptr, status, scratch, sms, static_cast<cudaStream_t>(stream));
+    rc = ra::launch_tc(p, nullptr, status, scratch, sms, static_cast<cudaStream_t>(stream));
+    if (rc == RA_ERR_CUDA) ra::note_cuda_error(cudaGetLastError());
+    return rc;
 }

@@ -120,12 +120,16 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
  * copies of out (and lse, when lse_host is not NULL) back to the host.
  * With at least four (batch, KV head) groups (B*Hkv >= 4) the call pipelines
  * up to eight chunks of consecutive groups: chunk c+1's copies in overlap
- * chunk c's forward, and chunk c's copies out overlap later chunks'.  That
+ * chunk c's forward, and chunk c's copies out overlap later chunks'.  (A
+ * chunk starts at an offset of whole groups into each staging buffer; if one
+ * such offset is not a multiple of 16 bytes the call runs in order instead.)
+ * That
  * work runs on streams the library creates for the device on first use (one
  * copy stream per direction, two compute streams, kept until the process
  * exits), forked from `stream` at the start of the call and joined back into
- * it at the end, so `stream` orders the whole call as if it ran there; the
- * outputs are the bits ra_forward computes.  Concurrent calls from several
+ * it at the end, so `stream` orders the whole call as if it ran there (also
+ * when an error stops the call part-way: what was enqueued is joined before
+ * the error is returned); the outputs are the bits ra_forward computes.  Concurrent calls from several
  * host threads are serialised while they enqueue.  Fewer groups run in order
  * on `stream` itself.  Asynchronous: the host buffers must stay valid until
  * `stream` reaches the end of the call; page-locked (pinned) host memory
@@ -219,23 +223,41 @@ int ra_ulysses_exchange(const void* src, void* dst, int B, int H, int64_t S, int
                         int64_t row_bytes, int inverse, void* stream);
 
 /*
- * ra_plan (host only, no GPU): the fold list of one query tile.
- * For query shard i and query tile qt (rows [qt*tile, (qt+1)*tile) of the
- * shard), writes n_items entries of 4 int32 each, (s, j, kt, kind), in fold
- * order: ring steps s ascending (j = (i - s) mod N), key tiles kt of shard j
- * ascending, only tiles that hold at least one visible (query, key) pair;
- * kind is RA_FOLD_FULL (every pair visible), RA_FOLD_INCL (pairs with local
- * key row <= local query row) or RA_FOLD_STRICT (local key row < local query
- * row).  This is the exact order the tensor-core kernel folds the tile in.
- *   items: int32[cap][4] or NULL (then only *n_items is set).
+ * ra_plan (host only, no GPU): the whole fold schedule of the ring, the
+ * ordered work list the kernels follow.  Writes n_items entries of 6 int32
+ * each, (i, qt, s, j, kt, kind): query shards i ascending, their query tiles
+ * qt ascending (rows [qt*tile, (qt+1)*tile) of the shard), and for each query
+ * tile its folds in order -- ring steps s ascending with j = (i - s) mod N
+ * (glossary page, "Como funciona a atencao em anel": device i holds block
+ * (i - step) mod N, received from the previous device), key tiles kt of
+ * shard j ascending -- listing only tiles that hold at least one visible
+ * (query, key) pair, so the causal block and tile skips are the entries
+ * that are absent.  kind is RA_FOLD_FULL (every pair visible), RA_FOLD_INCL
+ * (pairs with local key row <= local query row) or RA_FOLD_STRICT (local
+ * key row < local query row).  The tensor-core kernel folds every query
+ * tile in exactly this order (ra_fold_log records it).
+ *   items: int32[cap][6] or NULL (then only *n_items is set).
  *   striped is the layout (RA_LAYOUT_*).  Requires tile >= 2; a shard's last
  *   tile may be partial (ceil(Sb/tile) tiles), except under zigzag, which
  *   needs Sb % (2*tile) == 0.
  * Errors: RA_ERR_INVALID_ARG, RA_ERR_CAPACITY (cap too small; *n_items is
  * still set).
  */
-int ra_plan(int64_t S, int N, int causal, int striped, int tile, int i, int qt, int32_t* items,
-            int64_t cap, int64_t* n_items);
+int ra_plan(int64_t S, int N, int causal, int striped, int tile, int32_t* items, int64_t cap,
+            int64_t* n_items);
+
+/*
+ * ra_plan_tile (host only, no GPU): the fold list of one query tile, the
+ * entries of ra_plan whose (i, qt) are given.  For query shard i and query
+ * tile qt writes n_items entries of 4 int32 each, (s, j, kt, kind), in fold
+ * order.
+ *   items: int32[cap][4] or NULL (then only *n_items is set).  Same size
+ *   rules as ra_plan; 0 <= i < N, 0 <= qt < ceil(Sb/tile).
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_CAPACITY (cap too small; *n_items is
+ * still set).
+ */
+int ra_plan_tile(int64_t S, int N, int causal, int striped, int tile, int i, int qt,
+                 int32_t* items, int64_t cap, int64_t* n_items);
 
 /*
  * ra_plan_backward (host only, no GPU): the visiting order of one key tile in

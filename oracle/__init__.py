@@ -47,6 +47,7 @@ from .attention import (  # noqa: F401
     ulysses_exchange,
     attention_backward,
     attention_backward_rows,
+    attention_backward_key_rows,
     backward_uniform_scores,
     ring_attention_backward,
 )

@@ -309,6 +309,51 @@ def attention_backward_rows(qrows, qpos, dorows, k, v, kpos, causal: bool, scale
     return scale * (dS @ k)
 
 
+def attention_backward_key_rows(qrows, qpos, dorows, k, v, kpos, keys, causal: bool,
+                                scale: float, chunk: int = 256):
+    """dk and dv of chosen key rows of one head, from the plain definition.
+
+    qrows [T, D] with positions qpos and dL/dout rows dorows [T, D] must hold
+    every query row that sees any chosen key (under the causal mask, every
+    query at or after the earliest chosen key's position); k, v [Sk, D] are
+    all keys and values of the head with positions kpos; ``keys`` indexes the
+    chosen rows of k.  For each query row t (taken ``chunk`` rows at a time
+    only to bound memory), over its visible keys u:
+        P_tu  = softmax_u(scale q_t . k_u)
+        dP_tu = dO_t . v_u
+        dS_tu = P_tu (dP_tu - sum_u' P_tu' dP_tu')     (softmax Jacobian)
+    and for each chosen key c
+        dK_c = scale sum_t dS_tc q_t,    dV_c = sum_t P_tc dO_t
+    -- the rows ``keys`` of ``attention_backward``'s dk and dv for one query
+    head (a key/value head's gradient is the sum over its query heads).
+    Returns dk [len(keys), D], dv [len(keys), D].
+    """
+    qrows = np.asarray(qrows, np.float64)
+    dorows = np.asarray(dorows, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    qpos = np.asarray(qpos)
+    kpos = np.asarray(kpos)
+    keys = np.asarray(keys, np.int64)
+    dk = np.zeros((len(keys), k.shape[1]))
+    dv = np.zeros((len(keys), v.shape[1]))
+    for r0 in range(0, len(qrows), chunk):
+        q, do, qp = qrows[r0:r0 + chunk], dorows[r0:r0 + chunk], qpos[r0:r0 + chunk]
+        s = (q @ k.T) * scale
+        if causal:
+            s = np.where(kpos[None, :] <= qp[:, None], s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        m = np.where(np.isfinite(m), m, 0.0)
+        e = np.exp(s - m)
+        den = e.sum(axis=1, keepdims=True)
+        P = e / np.where(den > 0, den, 1.0)
+        dP = do @ v.T
+        dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+        dk += scale * (dS[:, keys].T @ q)
+        dv += P[:, keys].T @ do
+    return dk, dv
+
+
 def backward_uniform_scores(q, v, dout, causal: bool, scale=None, dk_rows=None):
     """dk and dv of the plain definition when every score is zero (K = 0),
     token order, float64, by prefix sums.

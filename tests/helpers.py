@@ -117,10 +117,27 @@ def sample_rows(seed, B, Hq, S, N, n_rows):
     return sorted(set(picks))
 
 
-def sampled_reference(seed, wl_shapes, rows, causal, striped, N, scale=None):
+def _kv_token_order(seed, S, D, N, layout, Hkv, b, kvh):
+    """k and v of one (batch, KV head) slice, regenerated and put in token
+    order (float64, [S, D] each)."""
+    base = (b * Hkv + kvh) * S * D
+    kk = oracle.bf16_bits_to_f64(ragen.normal_bf16(seed, ragen.TENSOR_K, S * D, start=base))
+    vv = oracle.bf16_bits_to_f64(ragen.normal_bf16(seed, ragen.TENSOR_V, S * D, start=base))
+    return (oracle.to_token_order(kk.reshape(S, D), N, layout),
+            oracle.to_token_order(vv.reshape(S, D), N, layout))
+
+
+def sampled_reference(seed, wl_shapes, rows, causal, striped, N, scale=None,
+                      max_elems=1 << 25):
     """Oracle O, lse for sampled shard-major query rows of a bf16 workload,
     regenerating only what is needed (the sampled q rows, full k/v of the
-    kv heads involved) from the counter-based generator."""
+    kv heads involved) from the counter-based generator.
+
+    Each row is the plain definition (``oracle.attend_rows``) against the keys
+    of its KV head in token order.  Rows are taken in order of position, so
+    under the causal mask a group of rows needs only the keys up to its
+    largest position (the others are invisible to all of them); groups are
+    sized to keep the score block under ``max_elems`` entries."""
     (B, Hq, S, D), (_, Hkv, _, _) = wl_shapes
     g = Hq // Hkv
     sc = 1.0 / math.sqrt(D) if not scale else scale
@@ -131,19 +148,40 @@ def sampled_reference(seed, wl_shapes, rows, causal, striped, N, scale=None):
     for n, (b, h, p) in enumerate(rows):
         by_kv.setdefault((b, h // g), []).append(n)
     for (b, kvh), idxs in by_kv.items():
-        base = (b * Hkv + kvh) * S * D
-        kk = oracle.bf16_bits_to_f64(ragen.normal_bf16(seed, ragen.TENSOR_K, S * D, start=base))
-        vv = oracle.bf16_bits_to_f64(ragen.normal_bf16(seed, ragen.TENSOR_V, S * D, start=base))
-        kk, vv = kk.reshape(S, D), vv.reshape(S, D)
+        kk, vv = _kv_token_order(seed, S, D, N, striped, Hkv, b, kvh)
+        idxs = np.array(sorted(idxs, key=lambda n: pos[rows[n][2]]))
         qrows = [(rows[n][0] * Hq + rows[n][1]) * S + rows[n][2] for n in idxs]
         qq = oracle.bf16_bits_to_f64(ragen.normal_bf16_rows(seed, ragen.TENSOR_Q, qrows, D))
         qpos = pos[[rows[n][2] for n in idxs]]
-        for c0 in range(0, len(idxs), 32):  # bounds the [rows, S] score matrix
-            sl = slice(c0, c0 + 32)
-            o, l = oracle.attend_rows(qq[sl], qpos[sl], kk, vv, pos, causal, sc)
-            out_o[idxs[sl]] = o
-            out_l[idxs[sl]] = l
+        c0 = 0
+        while c0 < len(idxs):
+            # rows in this group: as many as fit the score block
+            c1 = c0 + 1
+            while c1 < len(idxs) and (c1 + 1 - c0) * (
+                    (int(qpos[c1]) + 1) if causal else S) <= max_elems:
+                c1 += 1
+            hi = int(qpos[c1 - 1]) + 1 if causal else S
+            o, l = oracle.attend_rows(qq[c0:c1], qpos[c0:c1], kk[:hi], vv[:hi],
+                                      np.arange(hi), causal, sc)
+            out_o[idxs[c0:c1]] = o
+            out_l[idxs[c0:c1]] = l
+            c0 = c1
     return out_o, out_l
+
+
+def slice_reference(seed, wl, b, h):
+    """Oracle O [S, D] and lse [S] of every row of one (batch, query head)
+    slice of a bf16 workload, shard-major, from regenerated inputs: the plain
+    definition (``oracle.full_attention``) in token order."""
+    S, D, N = wl.S, wl.D, wl.N
+    g = wl.Hq // wl.Hkv
+    base = (b * wl.Hq + h) * S * D
+    qq = oracle.bf16_bits_to_f64(ragen.normal_bf16(seed, ragen.TENSOR_Q, S * D, start=base))
+    qq = oracle.to_token_order(qq.reshape(S, D), N, wl.striped)
+    kk, vv = _kv_token_order(seed, S, D, N, wl.striped, wl.Hkv, b, h // g)
+    o, lse = oracle.full_attention(qq[None, None], kk[None, None], vv[None, None], wl.causal)
+    return (oracle.to_shard_major(o[0, 0], N, wl.striped),
+            oracle.to_shard_major(lse[0, 0][:, None], N, wl.striped)[:, 0])
 
 
 def grad_inputs(seed, B, Hq, S, D, dtype):
@@ -222,3 +260,37 @@ def assert_grad_close(got, ref, dtype, what="", extra=None):
     assert total <= tol["fro"] * float(np.linalg.norm(ref)) + float(np.linalg.norm(ext)) + \
         tol["floor"], f"{what}: normwise error {fro:.3e} > {tol['fro']:.3e}"
     return fro, float((err / np.maximum(nrm, 1e-300)).max())
+
+
+def slice_token_order(seed, tensor_id, shape, b, h, N, layout):
+    """One (batch, head) slice [S, D] of a generated bf16 tensor of shape
+    [B, H, S, D], as float64 in token order."""
+    _, H, S, D = shape
+    x = oracle.bf16_bits_to_f64(ragen.normal_bf16(seed, tensor_id, S * D,
+                                                  start=(b * H + h) * S * D))
+    return oracle.to_token_order(x.reshape(S, D), N, layout)
+
+
+def key_rows_delta_bound(qw, qpos, dow, k, v, kpos, keys, causal, scale, lam=8.0,
+                         u=2.0 ** -9, chunk=256):
+    """Per chosen key row, the squared delta term of ``delta_error_bounds``
+    for one query head: sum over the query rows t that see key c of
+    (scale P_tc |d delta_t| |q_t|)^2, with |d delta_t| <=
+    lam u sqrt(sum_d dO_td^2 (O_td^2 + sum_u P_tu^2 v_ud^2)).  qw, dow hold
+    every query row that sees a chosen key (token order)."""
+    keys = np.asarray(keys, np.int64)
+    out = np.zeros(len(keys))
+    for r0 in range(0, len(qw), chunk):
+        q, do, qp = qw[r0:r0 + chunk], dow[r0:r0 + chunk], qpos[r0:r0 + chunk]
+        s = (q @ k.T) * scale
+        if causal:
+            s = np.where(np.asarray(kpos)[None, :] <= qp[:, None], s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        P = e / e.sum(axis=1, keepdims=True)
+        o = P @ v
+        var_o = o ** 2 + (P ** 2) @ (v ** 2)
+        dd = lam * u * np.sqrt((do ** 2 * var_o).sum(axis=1))
+        w = scale * dd * np.linalg.norm(q, axis=1)
+        out += ((P[:, keys] * w[:, None]) ** 2).sum(axis=0)
+    return out

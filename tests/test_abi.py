@@ -85,15 +85,25 @@ def test_host_validation_rejects_before_any_device_work(lib):
 
 def test_plan_errors(lib):
     n = ctypes.c_int64()
-    assert ra.ra_plan(256, 2, 1, 0, 128, 0, 0, None, 0, None) == ra.RA_ERR_INVALID_ARG
-    assert ra.ra_plan(256, 2, 1, 2, 96, 0, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
-    assert ra.ra_plan(256, 2, 1, 0, 128, 2, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
-    assert ra.ra_plan(256, 2, 1, 0, 128, 0, 1, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
-    assert ra.ra_plan(256, 2, 1, 0, 128, 1, 0, None, 0, ctypes.byref(n)) == ra.RA_OK
+    T = ra.ra_plan_tile
+    assert T(256, 2, 1, 0, 128, 0, 0, None, 0, None) == ra.RA_ERR_INVALID_ARG
+    assert T(256, 2, 1, 2, 96, 0, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert T(256, 2, 1, 0, 128, 2, 0, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert T(256, 2, 1, 0, 128, 0, 1, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert T(256, 2, 1, 0, 128, 1, 0, None, 0, ctypes.byref(n)) == ra.RA_OK
     assert n.value == 2  # shard 1 of 2, contiguous causal: shard 0 full, own diagonal
     buf = (ctypes.c_int32 * 4)()
-    assert ra.ra_plan(256, 2, 1, 0, 128, 1, 0, buf, 1, ctypes.byref(n)) == ra.RA_ERR_CAPACITY
+    assert T(256, 2, 1, 0, 128, 1, 0, buf, 1, ctypes.byref(n)) == ra.RA_ERR_CAPACITY
     assert n.value == 2
+    # the whole schedule
+    assert ra.ra_plan(256, 2, 1, 0, 128, None, 0, None) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(256, 2, 1, 2, 96, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(255, 2, 1, 0, 128, None, 0, ctypes.byref(n)) == ra.RA_ERR_INVALID_ARG
+    assert ra.ra_plan(256, 2, 1, 0, 128, None, 0, ctypes.byref(n)) == ra.RA_OK
+    assert n.value == 3  # shard 0: its diagonal; shard 1: shard 0 full and its diagonal
+    buf = (ctypes.c_int32 * 12)()
+    assert ra.ra_plan(256, 2, 1, 0, 128, buf, 2, ctypes.byref(n)) == ra.RA_ERR_CAPACITY
+    assert n.value == 3
 
 
 @pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True),
@@ -111,6 +121,18 @@ def test_plan_equals_bruteforce_schedule(lib, causal, striped, S, N, T):
         for qt in range(nt):
             assert ra.plan(S, N, causal, striped, i, qt, tile=T) == by_tile.get((i, qt), []), \
                 (i, qt)
+
+
+@pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True),
+                                            (True, 2)])
+@pytest.mark.parametrize("S,N,T", [(512, 4, 32), (600, 3, 60), (256, 1, 128), (7 * 44, 7, 22)])
+def test_whole_schedule_equals_bruteforce_schedule(lib, causal, striped, S, N, T):
+    """Bit-exact: ra_plan's ordered work list == the oracle's brute-force
+    schedule, entry by entry (shards, tiles, ring steps, key tiles, kinds)."""
+    if striped == 2 and (S // N) % (2 * T):
+        pytest.skip("zigzag chunks must be whole tiles")
+    want = [tuple(int(x) for x in e) for e in oracle.fold_schedule(S, N, causal, striped, T, T)]
+    assert ra.plan_schedule(S, N, causal, striped, tile=T) == want
 
 
 @pytest.mark.parametrize("causal,striped", [(False, False), (True, False), (True, True)])

@@ -52,6 +52,11 @@ SIMT_F32 = [
     (1, 2, 1, 1000, 4, 128, True, 1),   # Sb = 250
     (2, 4, 2, 640, 5, 64, False, 0),    # Sb = 128
     (1, 2, 2, 512, 4, 32, True, 2),     # zigzag
+    # head dimensions padded up to the tiled kernels' 128 / 32 variants: the
+    # partial-vector staging and the padded columns of the epilogue
+    (1, 2, 1, 300, 3, 100, True, 0),    # D = 100 in the 128 variant, GQA
+    (1, 4, 2, 256, 2, 20, True, 1),     # D = 20 in the 32 variant, GQA
+    (1, 2, 2, 192, 3, 4, False, 0),     # D = 4, the smallest
 ]
 
 

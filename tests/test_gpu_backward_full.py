@@ -5,7 +5,9 @@
   against the oracle's gradient.
 * gqa_128k (the bench workload: 32 query heads on 8 KV heads, S=131072 in
   16 striped shards, causal):
-  - random inputs: stratified sampled rows of dq against the per-row oracle;
+  - random inputs: stratified sampled rows of dq against the per-row oracle,
+    and dk, dv of sampled key rows (among the last 1024 tokens, whose
+    gradients need at most 1024 query rows per head) against the oracle;
   - uniform scores (K = 0, random q, v, dout): every row of dv and sampled
     rows of dk against the oracle's prefix-sum closed form, and dq exactly 0.
     All tiles, masks and ring steps run; only the score values are trivial.
@@ -21,7 +23,8 @@ import ragen
 from ragen import WORKLOADS
 
 from helpers import (TOL_BWD, assert_grad_close, backward_reference, delta_error_bounds,
-                     from_device, grad_inputs, inputs, sample_rows, to_device)
+                     from_device, grad_inputs, inputs, key_rows_delta_bound, sample_rows,
+                     to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +61,10 @@ def _host_inputs(wl, tensors):
             for t in tensors]
 
 
-def test_backward_gqa_128k_sampled_dq_rows(ra):
+@pytest.fixture(scope="module")
+def gqa_128k_grads(ra):
+    """The bench workload's forward and backward on random inputs (host
+    arrays of the inputs, device gradients)."""
     wl = WORKLOADS["gqa_128k"]
     q, k, v, dout = _host_inputs(wl, (ragen.TENSOR_Q, ragen.TENSOR_K, ragen.TENSOR_V,
                                       ragen.TENSOR_DO))
@@ -67,6 +73,56 @@ def test_backward_gqa_128k_sampled_dq_rows(ra):
     dq, dk, dv = ra.backward(tq, tk, tv, out, lse, tg, wl.N, causal=wl.causal,
                              striped=wl.striped)
     ra.check()
+    del tq, tk, tv, tg, out, lse
+    return wl, (q, k, v, dout), (dq, dk, dv)
+
+
+def test_backward_gqa_128k_sampled_dk_dv_rows(gqa_128k_grads):
+    """Random inputs: dk and dv of sampled key rows against the oracle.  A
+    key's gradient needs every query row that sees it, each with its full
+    softmax, so the sample is taken among the last 1024 tokens (seen by at
+    most 1024 queries per head): they lie in the last key tile of every one
+    of the 16 shards, visited by query tiles of every shard.  Two KV heads,
+    each summing its four query heads."""
+    wl, (q, k, v, dout), (dq, dk, dv) = gqa_128k_grads
+    S, N, D = wl.S, wl.N, wl.D
+    g = wl.Hq // wl.Hkv
+    sc = 1.0 / math.sqrt(D)
+    pos = oracle.positions(S, N, wl.striped)
+    inv = np.empty(S, dtype=np.int64)
+    inv[pos] = np.arange(S)            # token t sits at shard-major row inv[t]
+    rng = np.random.default_rng(wl.seed + 5)
+    keys = sorted({S - 1024, S - 1} | set(rng.integers(S - 1024, S, 30).tolist()))
+    t0 = keys[0]
+    tok = np.arange(S)
+    qs, _ = wl.shapes()
+    for kvh in (0, wl.Hkv - 1):
+        K = oracle.to_token_order(oracle.bf16_bits_to_f64(k[0, kvh]), N, wl.striped)
+        V = oracle.to_token_order(oracle.bf16_bits_to_f64(v[0, kvh]), N, wl.striped)
+        dk_ref = np.zeros((len(keys), D))
+        dv_ref = np.zeros((len(keys), D))
+        extra = np.zeros(len(keys))
+        for h in range(kvh * g, (kvh + 1) * g):
+            Qw = oracle.to_token_order(oracle.bf16_bits_to_f64(q[0, h]), N, wl.striped)[t0:]
+            dOw = oracle.to_token_order(oracle.bf16_bits_to_f64(dout[0, h]), N, wl.striped)[t0:]
+            a, b = oracle.attention_backward_key_rows(Qw, tok[t0:], dOw, K, V, tok, keys,
+                                                      wl.causal, sc)
+            dk_ref += a
+            dv_ref += b
+            extra += key_rows_delta_bound(Qw, tok[t0:], dOw, K, V, tok, keys, wl.causal, sc)
+        rows = torch_rows(dk, 0, kvh, inv[keys])
+        assert_grad_close(rows, dk_ref, "bf16", f"dk kv head {kvh}", np.sqrt(extra))
+        assert_grad_close(torch_rows(dv, 0, kvh, inv[keys]), dv_ref, "bf16",
+                          f"dv kv head {kvh}")
+
+
+def torch_rows(t, b, h, rows):
+    import torch
+    return t[b, h][torch.as_tensor(np.asarray(rows), device=t.device)].double().cpu().numpy()
+
+
+def test_backward_gqa_128k_sampled_dq_rows(gqa_128k_grads):
+    wl, (q, k, v, dout), (dq, dk, dv) = gqa_128k_grads
     rows = sample_rows(wl.seed + 1, wl.B, wl.Hq, wl.S, wl.N, 96)
     g = wl.Hq // wl.Hkv
     sc = 1.0 / math.sqrt(wl.D)

@@ -56,6 +56,10 @@ def test_forward_host_equals_device_forward(ra):
     (2, 10, 5, 512, 2, 64, "bf16"),     # 10 groups over 8 chunks: uneven chunks
     (1, 12, 4, 1000, 4, 128, "bf16"),   # ragged shards (Sb = 250), 4 groups
     (1, 4, 4, 256, 2, 32, "f32"),       # the SIMT kernel, 4 groups
+    # chunk offsets that are not 16-byte multiples (lse: 24 bytes per group;
+    # q: 24 bytes per group): the call must run in order, not pipelined
+    (1, 4, 4, 6, 2, 16, "bf16"),
+    (1, 4, 4, 3, 1, 4, "bf16"),
 ])
 def test_pipelined_forward_host_equals_device_forward(ra, B, Hq, Hkv, S, N, D, dt):
     """With at least four (batch, KV head) groups the call pipelines chunks of

@@ -304,22 +304,53 @@ def test_noncausal_8k_every_row(ra):
     assert_close(out, lse, ro, rl, "bf16", wl.name)
 
 
-@pytest.mark.parametrize("name,n_rows", [("causal_32k_contig", 768), ("causal_32k_striped", 768),
-                                         ("causal_32k_zigzag", 768), ("gqa_128k", 768),
-                                         ("gqa_128k_ragged", 768), ("long_1m", 384)])
-def test_full_size_sampled_rows(ra, name, n_rows):
+# Full-size workloads, launched as the bench launches them: a stratified row
+# sample (every head and shard, each shard's first and last row), plus every
+# row of chosen (batch, head) slices, or of a slice's first shards.
+FULL_SIZE = [
+    # name, sampled rows, whole (b, h) slices, (heads, shards) checked on every row
+    ("causal_32k_contig", 768, [(b, h) for b in (0, 1) for h in (0, 31)], None),
+    ("causal_32k_striped", 768, [(b, h) for b in (0, 1) for h in (0, 31)], None),
+    ("causal_32k_zigzag", 768, [(0, 0), (1, 31)], None),
+    ("gqa_128k", 4096, [], ((0, 31), (0, 1))),
+    ("gqa_128k_ragged", 768, [], None),
+    ("long_1m", 4096, [], None),
+]
+
+
+@pytest.mark.parametrize("name,n_rows,slices,shard_rows", FULL_SIZE)
+def test_full_size_rows(ra, name, n_rows, slices, shard_rows):
     import torch
+    from helpers import slice_reference
     wl = WORKLOADS[name]
     tq, tk, tv = _device_inputs(wl)
     out, lse = ra.forward(tq, tk, tv, wl.N, causal=wl.causal, striped=wl.striped)
     ra.check()
-    rows = sample_rows(wl.seed + 1, wl.B, wl.Hq, wl.S, wl.N, n_rows)
-    idx = torch.tensor([(b * wl.Hq + h) * wl.S + p for (b, h, p) in rows], device="cuda")
-    got_o = out.view(-1, wl.D)[idx].double().cpu().numpy()
-    got_l = lse.view(-1)[idx].double().cpu().numpy()
+    del tq, tk, tv
     assert torch.isfinite(out.view(-1, wl.D)[:: max(1, wl.S // 3)].float()).all()
+
+    def gather(rows):
+        idx = torch.tensor([(b * wl.Hq + h) * wl.S + p for (b, h, p) in rows], device="cuda")
+        return (out.view(-1, wl.D)[idx].double().cpu().numpy(),
+                lse.view(-1)[idx].double().cpu().numpy())
+
+    rows = sample_rows(wl.seed + 1, wl.B, wl.Hq, wl.S, wl.N, n_rows)
     ro, rl = sampled_reference(wl.seed, wl.shapes(), rows, wl.causal, wl.striped, wl.N)
-    assert_close(got_o, got_l, ro, rl, "bf16", wl.name)
+    mx, mean = assert_close(*gather(rows), ro, rl, "bf16", f"{wl.name} sampled")
+    print(f"{wl.name}: {len(rows)} sampled rows max-abs {mx:.2e} mean-abs {mean:.2e}")
+    for (b, h) in slices:
+        ro, rl = slice_reference(wl.seed, wl, b, h)
+        got_o = out[b, h].double().cpu().numpy()
+        got_l = lse[b, h].double().cpu().numpy()
+        mx, mean = assert_close(got_o, got_l, ro, rl, "bf16", f"{wl.name} b={b} h={h}")
+        print(f"{wl.name}: every row of b={b} h={h} max-abs {mx:.2e} mean-abs {mean:.2e}")
+    if shard_rows:
+        heads, shards = shard_rows
+        rows = [(0, h, i * wl.Sb + r) for h in heads for i in shards for r in range(wl.Sb)]
+        ro, rl = sampled_reference(wl.seed, wl.shapes(), rows, wl.causal, wl.striped, wl.N)
+        mx, mean = assert_close(*gather(rows), ro, rl, "bf16", f"{wl.name} shards {shards}")
+        print(f"{wl.name}: every row of heads {heads} in shards {shards} ({len(rows)} rows) "
+              f"max-abs {mx:.2e} mean-abs {mean:.2e}")
 
 
 def test_empty_problems_leave_the_stream_usable(ra):

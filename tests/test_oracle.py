@@ -346,3 +346,20 @@ def test_ulysses_pipeline_equals_full_attention(causal):
     o = back.transpose(1, 2, 0, 3, 4).reshape(B, H, S, D)
     o_f, _ = oracle.full_attention(q, k, v, causal)
     np.testing.assert_allclose(o, o_f, atol=1e-12)
+
+
+def test_bf16_upcast_known_words():
+    """bfloat16 is the top half of an IEEE binary32 word: sign, 8 exponent
+    bits (bias 127), 7 fraction bits.  Known words decoded by hand."""
+    words = np.array([0x3F80, 0xC000, 0x3FC0, 0x4049, 0x0000, 0x8000, 0x7F80, 0xFF80,
+                      0x0001, 0x0080, 0x7F7F, 0xBE80, 0x4300], dtype=np.uint16)
+    want = [1.0, -2.0, 1.5, 3.140625, 0.0, -0.0, math.inf, -math.inf,
+            2.0 ** -133,                      # smallest subnormal: 2^-126 * 2^-7
+            2.0 ** -126,                      # smallest normal
+            (2 - 2.0 ** -7) * 2.0 ** 127,     # largest finite
+            -0.25, 128.0]
+    got = oracle.bf16_bits_to_f64(words)
+    assert got.dtype == np.float64
+    for w, g, e in zip(words, got, want):
+        assert g == e and math.copysign(1, g) == math.copysign(1, e), (hex(int(w)), g, e)
+    assert np.isnan(oracle.bf16_bits_to_f64(np.array([0x7FC0], dtype=np.uint16)))[0]

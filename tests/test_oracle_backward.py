@@ -175,3 +175,34 @@ def test_uniform_score_closed_form_equals_the_full_gradient(causal):
     np.testing.assert_allclose(dk_cf, dk[:, :, rows], rtol=0, atol=1e-12)
     dk_all, _ = oracle.backward_uniform_scores(q, v, dout, causal)
     np.testing.assert_allclose(dk_all, dk, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_rows_match_torch_autograd(causal):
+    """dk, dv of chosen key rows (used on sampled key rows at full size),
+    summed over the query heads of a GQA group, against torch autograd of the
+    whole problem.  Under the causal mask only the queries at or after the
+    earliest chosen key are passed, which must be enough."""
+    torch = pytest.importorskip("torch")
+    B, Hq, Hkv, S, D = 1, 4, 2, 40, 16
+    q, k, v = rnd((B, Hq, S, D), 31), rnd((B, Hkv, S, D), 32), rnd((B, Hkv, S, D), 33)
+    dout = rnd((B, Hq, S, D), 34)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    g = Hq // Hkv
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk.repeat_interleave(g, dim=1), tv.repeat_interleave(g, dim=1), is_causal=causal)
+    o.backward(torch.tensor(dout, dtype=torch.float64))
+    keys = [25, 26, 31, 39] if causal else [0, 7, 25, 39]
+    t0 = keys[0] if causal else 0
+    pos = np.arange(S)
+    for kvh in range(Hkv):
+        dk = np.zeros((len(keys), D))
+        dv = np.zeros((len(keys), D))
+        for h in range(kvh * g, (kvh + 1) * g):
+            a, b = oracle.attention_backward_key_rows(
+                q[0, h, t0:], pos[t0:], dout[0, h, t0:], k[0, kvh], v[0, kvh], pos, keys,
+                causal, 1 / math.sqrt(D), chunk=7)
+            dk += a
+            dv += b
+        np.testing.assert_allclose(dk, tk.grad[0, kvh, keys].numpy(), rtol=0, atol=1e-11)
+        np.testing.assert_allclose(dv, tv.grad[0, kvh, keys].numpy(), rtol=0, atol=1e-11)
