@@ -48,6 +48,9 @@ def parse():
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ring", action="store_true",
+                    help="run the workload as a real ring over the job's ranks (shard r on "
+                         "rank r, K/V blocks passed between ranks); strong scaling")
     ap.add_argument("--cpu-configs", action="store_true",
                     help="time the float64 oracle in full on configs 0-2 on all host cores, "
                          "comparing every row with the library's output; one JSON line each")
@@ -585,6 +588,92 @@ def backward_arm(args, wl):
     return 0
 
 
+# ---------------------------------------------------------------- true ring across ranks
+def ring_arm(args, wl):
+    """The workload as a real ring over the ranks of this job (--ring): rank r
+    holds shard r of N = world size (the workload's layout), and each step is
+    ring_attention -- N calls of ra_ring_step, with each K/V block passed to
+    the next rank (NCCL send/recv between GPUs) while the current one is
+    folded.  The total problem is fixed as ranks are added (strong scaling);
+    value = the workload's FLOPs / the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    import exact_long_context_order_b300 as ra
+    import ragen
+    from exact_long_context_order_b300.ring import ring_attention
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if not dist.is_initialized():
+        dist.init_process_group("nccl" if world > 1 else "gloo",
+                                device_id=torch.device("cuda", local) if world > 1 else None,
+                                init_method=None if world > 1 else "tcp://127.0.0.1:" +
+                                str(os.environ.get("MASTER_PORT", "29512")),
+                                rank=rank, world_size=world)
+    ra.lib()
+    if wl.dtype != "bf16" or wl.S % world:
+        raise SystemExit("--ring runs bf16 workloads whose S is a multiple of the rank count")
+    Sb = wl.S // world
+    # this rank's shard of q, k, v: i.i.d. N(0, 1) from the generator, drawn at
+    # the shard's own counter range of each (batch, head) slice
+    def shard(tid, H):
+        h = torch.empty((wl.B, H, Sb, wl.D), dtype=torch.int16, pin_memory=True)
+        flat = h.numpy().reshape(wl.B * H, Sb * wl.D)
+        for bh in range(wl.B * H):
+            ragen.normal_bf16(wl.seed, tid, Sb * wl.D, start=(bh * wl.S + rank * Sb) * wl.D,
+                              out=flat[bh].view(np.uint16))
+        return h.to("cuda").view(torch.bfloat16)
+    q, k, v = shard(ragen.TENSOR_Q, wl.Hq), shard(ragen.TENSOR_K, wl.Hkv), shard(ragen.TENSOR_V,
+                                                                                  wl.Hkv)
+    out = torch.empty_like(q)
+    lse = torch.empty((wl.B, wl.Hq, Sb), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ring_attention(q, k, v, causal=wl.causal, layout=int(wl.striped), out=out, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    ra.check(stream)
+    clocks = ClockSampler(local)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    rc = ra.ra_check(ra._stream_handle(stream))
+    if rc != ra.RA_OK:
+        raise SystemExit(f"device status after timed region: {ra.ra_strerror(rc)}")
+    t_max = max_over_ranks(a.elapsed_time(b), device="cuda")
+    value = wl.flops() * args.steps / (t_max * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": dict(wl.describe(), parallelism=f"ring{world}", ring_devices=world,
+                           tokens_per_rank=Sb, l2="inputs larger than L2 (no flush)",
+                           flops_per_step=wl.flops()),
+            "tokens_per_s": wl.B * wl.S * args.steps / (t_max * 1e-3),
+            "frac_of_bf16_peak": value / world / float(peaks["bf16_tflops"]),
+            "gpu_launches": args.steps * world,
+            "clocks": clk, "e2e": None,
+            "how": "ring_attention per step: N ra_ring_step calls per rank, K/V blocks sent to "
+                   "the next rank while the current block is folded",
+        }
+        print(json.dumps(line), flush=True)
+    dist.destroy_process_group()
+    return 0
+
+
 # ---------------------------------------------------------------- our arm
 def main():
     args = parse()
@@ -594,6 +683,8 @@ def main():
         return cpu_configs_arm(args)
     if args.impl == "reference":
         return reference_arm(args, wl)
+    if args.ring:
+        return ring_arm(args, wl)
     if args.op == "backward":
         return backward_arm(args, wl)
     if args.op != "forward":

@@ -23,6 +23,7 @@ RA_BF16, RA_F32 = 0, 1
 RA_KERNEL_AUTO, RA_KERNEL_TC, RA_KERNEL_SIMT = 0, 1, 2
 RA_FOLD_FULL, RA_FOLD_INCL, RA_FOLD_STRICT = 0, 1, 2
 RA_LAYOUT_CONTIGUOUS, RA_LAYOUT_STRIPED, RA_LAYOUT_ZIGZAG = 0, 1, 2
+RA_STEP_FIRST, RA_STEP_LAST = 1, 2
 
 _c = ctypes
 _vp, _i32, _i64, _f32 = _c.c_void_p, _c.c_int, _c.c_int64, _c.c_float
@@ -34,6 +35,8 @@ _SIGNATURES = {
     "ra_forward_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
                          _i64, _i32, _i32, _i32, _i32, _f32, _i32, _vp], _i32),
     "ra_merge": ([_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp], _i32),
+    "ra_ring_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32,
+                      _i32, _i32, _i32, _i32, _f32, _i32, _vp], _i32),
     "ra_stripe": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _vp], _i32),
     "ra_relayout": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _i32, _vp], _i32),
     "ra_ulysses_exchange": ([_vp, _vp, _i32, _i32, _i64, _i32, _i64, _i32, _vp], _i32),
@@ -109,6 +112,12 @@ def ra_forward_host(q_h, k_h, v_h, out_h, lse_h, q_d, k_d, v_d, out_d, lse_d, B,
 
 def ra_merge(out_a, lse_a, out_b, lse_b, rows, D, dtype, stream):
     return lib().ra_merge(out_a, lse_a, out_b, lse_b, rows, D, dtype, stream)
+
+
+def ra_ring_step(q, k, v, state_o, state_lse, out, lse, B, Hq, Hkv, Sb, D, N, i, j, causal,
+                 layout, scale, flags, stream):
+    return lib().ra_ring_step(q, k, v, state_o, state_lse, out, lse, B, Hq, Hkv, Sb, D, N, i, j,
+                              causal, layout, scale, flags, stream)
 
 
 def ra_stripe(src, dst, BH, S, N, row_bytes, inverse, stream):
@@ -251,6 +260,42 @@ def forward(q, k, v, N: int, causal: bool = False, striped: bool = False, scale=
                        _stream_handle(stream))
     _check(rc, "ra_forward")
     return out, lse
+
+
+def ring_step(q, k, v, N: int, i: int, j: int, state_o=None, state_lse=None, out=None, lse=None,
+              first: bool = False, last: bool = False, causal: bool = False, layout=0,
+              scale=None, stream=None):
+    """One ring step over torch CUDA tensors: query shard i (q [B, Hq, Sb, D]
+    bf16) folds key/value block j (k, v [B, Hkv, Sb, D]) into its running
+    state (state_o float32 like q, state_lse float32 [B, Hq, Sb]).  With
+    ``last`` the result goes to out (bf16, allocated when None) and lse
+    instead.  Returns (state_o, state_lse, out, lse)."""
+    import torch
+    B, Hq, Sb, D = q.shape
+    Hkv = k.shape[1]
+    if q.dtype != torch.bfloat16 or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("ring_step takes bf16 q, k, v")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k and v must be contiguous")
+    if k.shape != (B, Hkv, Sb, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Hkv, Sb, D] with q's Sb and D")
+    if not (first and last):
+        if state_o is None:
+            state_o = torch.empty((B, Hq, Sb, D), dtype=torch.float32, device=q.device)
+        if state_lse is None:
+            state_lse = torch.empty((B, Hq, Sb), dtype=torch.float32, device=q.device)
+    if last:
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, Hq, Sb), dtype=torch.float32, device=q.device)
+    flags = (RA_STEP_FIRST if first else 0) | (RA_STEP_LAST if last else 0)
+    rc = ra_ring_step(_ptr(q), _ptr(k), _ptr(v), _ptr(state_o), _ptr(state_lse), _ptr(out),
+                      _ptr(lse), B, Hq, Hkv, Sb, D, N, i, j, int(causal), int(layout),
+                      float(scale or 0.0), flags, _stream_handle(stream))
+    _check(rc, "ra_ring_step")
+    return state_o, state_lse, out, lse
 
 
 def backward(q, k, v, out, lse, dout, N: int, causal: bool = False, striped: bool = False,

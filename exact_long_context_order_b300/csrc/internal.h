@@ -55,6 +55,29 @@ int launch_merge(void* out_a, float* lse_a, const void* out_b, const float* lse_
 int launch_stripe(const void* src, void* dst, int64_t BH, int64_t S, int N, int64_t row_bytes,
                   int layout, int inverse, cudaStream_t stream);
 
+// One step of a ring whose devices are separate processes: query shard i
+// ([B, Hq, Sb, D]) folds key/value block j ([B, Hkv, Sb, D]) of a ring of N
+// devices into its running state (state_o fp32 [B, Hq, Sb, D], state_lse
+// [B, Hq, Sb]); on the last step the folded result goes to out (bf16) and lse
+// instead of the state.
+struct StepProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    float* state_o;
+    float* state_lse;
+    void* out;
+    float* lse;
+    int B, Hq, Hkv;
+    int64_t Sb;
+    int D, N, i, j, causal, layout;
+    float scale;  // resolved (> 0)
+    int first, last;
+};
+bool tc_step_supported(const StepProblem& p);
+int launch_tc_step(const StepProblem& p, unsigned int* status, unsigned int* work, int sm_count,
+                   cudaStream_t stream);
+
 // Backward problem: the forward's tensors plus dout, the gradients and the
 // per-row terms delta (float32 [B*Hq*S], in the caller's workspace).
 struct BwdProblem {

@@ -99,11 +99,49 @@ struct Params {
     int max_entries;
     unsigned int* work;  // item counter, zero at launch: CTAs take items in order
     long long timeout_cycles;  // self test only: limit of every bounded wait
+    // Ring step only (STEP kernels): the buffers hold query shard step_i and
+    // key/value block step_j alone (S = Sb rows per (b, h) slice); the items
+    // cover the shard's query tiles, `ring` is the real ring whose masks apply,
+    // and the epilogue folds the block's partial into the running state.
+    RingGeom ring;
+    int step_i, step_j, step_s;
+    int step_first, step_last;
+    float* state_o;    // [B*Hq*Sb, D] running normalised output (fp32)
+    float* state_lse;  // [B*Hq*Sb] running log-sum-exp (natural log)
 };
+
+// The fold list of an item: every ring step (TileWalk), or in a ring step
+// only the key tiles of the block that step holds.
+template <bool STEP>
+__device__ __forceinline__ void walk_start(TileWalk& w, const ItemGeom& G, const Params& p,
+                                           const Item& it) {
+    if constexpr (STEP) {
+        w.s = p.step_s;
+        w.j = p.step_j;
+        w.kt = 0;
+        int nk0, nk1, d;
+        shard_span(p.ring, p.step_i, p.step_j, it.qt[0], &nk0, &d);
+        shard_span(p.ring, p.step_i, p.step_j, it.qt[1], &nk1, &d);
+        w.nk = nk0 > nk1 ? nk0 : nk1;
+    } else {
+        w.start(G.rg, it);
+    }
+}
+template <bool STEP>
+__device__ __forceinline__ bool walk_done(const TileWalk& w, const ItemGeom& G) {
+    if constexpr (STEP) return w.kt >= w.nk;
+    else return w.done(G.rg);
+}
+template <bool STEP>
+__device__ __forceinline__ void walk_next(TileWalk& w, const ItemGeom& G, const Item& it) {
+    if constexpr (STEP) ++w.kt;
+    else w.next(G.rg, it);
+}
 
 // RAGGED: the shard size is not a multiple of the tile, so each shard's last
 // query and key tile is partial (compiled out of the common case).
-template <int D, bool LOG, bool SELFTEST, bool RAGGED>
+// STEP: one step of a ring whose devices are separate processes (see Params).
+template <int D, bool LOG, bool SELFTEST, bool RAGGED, bool STEP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -205,8 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int64_t kvrow0 = (int64_t)(it.b * G.Hkv + it.kvh) * p.S;
                 TileWalk w;
-                for (w.start(G.rg, it); !w.done(G.rg) && ok; w.next(G.rg, it)) {
-                    const int row = (int)(kvrow0 + (int64_t)w.j * p.Sb + (int64_t)w.kt * kT);
+                for (walk_start<STEP>(w, G, p, it); !walk_done<STEP>(w, G) && ok;
+                     walk_next<STEP>(w, G, it)) {
+                    // a ring step's buffer holds only the block it folds
+                    const int64_t jrow = STEP ? 0 : (int64_t)w.j * p.Sb;
+                    const int row = (int)(kvrow0 + jrow + (int64_t)w.kt * kT);
                     for (int kv = 0; kv < 2; ++kv) {
                         if (SELFTEST && kv_pos == 0) {  // self test: nothing ever signals stage 0
                             ++kv_pos;
@@ -299,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status, wlim))) break;
                 TileWalk w;
                 uint32_t n = 0;
-                for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n) {
+                for (walk_start<STEP>(w, G, p, it); !walk_done<STEP>(w, G);
+                     walk_next<STEP>(w, G, it), ++n) {
                     const uint32_t stK = kv_pos % C::kStages;
                     if (!(ok = wait_bar(bar(C::bKVFull + stK), (kv_pos / C::kStages) & 1,
                                         abort_flag, p.status, wlim)))
@@ -333,6 +375,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++gt;
                 }
                 if (!ok) break;
+                if (STEP && n == 0) {
+                    // no tile of this block is visible to the item: no MMA reads
+                    // its Q tile or writes its O, so release both at once
+                    mbar_arrive(bar(C::bQEmpty));
+                    mbar_arrive(bar(C::bOFull + t));
+                    continue;
+                }
                 umma_commit(bar(C::bQEmpty));  // every S MMA of this slot and item is issued
                 const uint32_t vp = kv_pos - 1, stV = vp % C::kStages;
                 if (!(ok = wait_bar(bar(C::bKVFull + stV), (vp / C::kStages) & 1, abort_flag,
@@ -385,8 +434,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int n_logged = 0;
             TileWalk w;
             uint32_t n = 0;
-            for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n, ++gt) {
-                const int kind = fold_kind(G.rg, it.i, w.j, qt, w.kt);
+            for (walk_start<STEP>(w, G, p, it); !walk_done<STEP>(w, G);
+                 walk_next<STEP>(w, G, it), ++n, ++gt) {
+                const int kind = STEP ? fold_kind(p.ring, p.step_i, w.j, qt, w.kt)
+                                      : fold_kind(G.rg, it.i, w.j, qt, w.kt);
                 ok = wait_bar(bar(C::bSFull + t), gt & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
@@ -519,7 +570,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_bar(bar(C::bOFull + t), k & 1, abort_flag, p.status, wlim);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            if (valid) {
+            if (STEP && valid) {
+                // Fold this block's partial (O/l, lse_b) into the running state
+                // (O_s, lse_s) by the log-sum-exp weighting, in exp2 units:
+                //   lse = log2(2^a + 2^b),  O = 2^(a-lse) O_s + 2^(b-lse) O/l.
+                // Rows this block leaves empty (l = 0) keep the state.
+                const int64_t row = (int64_t)(it.b * G.Hq + hq) * p.S + (int64_t)qt * kT + r;
+                const bool row_ok = !RAGGED || qt < G.rg.nt - 1 || r < p.rem;
+                constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.69314718055994531f;
+                const float b2 = (l > 0.f) ? m_used * sl2 + lg2_approx(l) : -INFINITY;
+                const float a2 = (!p.step_first && row_ok) ? p.state_lse[row] * kLog2e : -INFINITY;
+                const float mx = fmaxf(a2, b2);
+                float cs = 0.f, cp = 0.f, lse_n = -INFINITY;
+                if (mx > -INFINITY) {
+                    const float ws = ex2_approx(a2 - mx), wp = ex2_approx(b2 - mx);
+                    const float den = ws + wp;
+                    cs = ws / den;
+                    cp = (l > 0.f) ? wp / den / l : 0.f;
+                    lse_n = (mx + lg2_approx(den)) * kLn2;
+                }
+                const bool use_o = l > 0.f;
+                float4* srow = reinterpret_cast<float4*>(p.state_o + row * D);
+                uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(o_tm + c * 32, o);  // warp-collective: every lane loads
+                    tmem_wait_ld();
+                    reg_fence(o);
+                    float nv[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) nv[e] = use_o ? cp * __uint_as_float(o[e]) : 0.f;
+                    if (!p.step_first && row_ok) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 sv = srow[c * 8 + e];
+                            nv[4 * e] = fmaf(cs, sv.x, nv[4 * e]);
+                            nv[4 * e + 1] = fmaf(cs, sv.y, nv[4 * e + 1]);
+                            nv[4 * e + 2] = fmaf(cs, sv.z, nv[4 * e + 2]);
+                            nv[4 * e + 3] = fmaf(cs, sv.w, nv[4 * e + 3]);
+                        }
+                    }
+                    if (row_ok) {
+                        if (p.step_last) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                orow[c * 4 + e] = make_uint4(
+                                    pack_bf16x2(nv[8 * e], nv[8 * e + 1]),
+                                    pack_bf16x2(nv[8 * e + 2], nv[8 * e + 3]),
+                                    pack_bf16x2(nv[8 * e + 4], nv[8 * e + 5]),
+                                    pack_bf16x2(nv[8 * e + 6], nv[8 * e + 7]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                srow[c * 8 + e] = make_float4(nv[4 * e], nv[4 * e + 1],
+                                                              nv[4 * e + 2], nv[4 * e + 3]);
+                        }
+                    }
+                }
+                if (row_ok) {
+                    if (!p.step_last) p.state_lse[row] = lse_n;
+                    else if (p.lse) p.lse[row] = lse_n;
+                }
+            } else if (valid) {
                 const int64_t row = (int64_t)(it.b * G.Hq + hq) * p.S + (int64_t)it.i * p.Sb +
                                     (int64_t)qt * kT + r;
                 // a shard's last tile may hold fewer than 128 real rows
@@ -581,7 +694,7 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     if (!encode_rows_bf16(&mq, pr.q, q_rows, D) || !encode_rows_bf16(&mk, pr.k, kv_rows, D) ||
         !encode_rows_bf16(&mv, pr.v, kv_rows, D))
         return RA_ERR_CUDA;
-    Params P;
+    Params P = {};
     const int Sb = (int)(pr.S / pr.N);
     const int nt = (Sb + kT - 1) / kT;
     P.G = make_item_geom(pr.B, pr.Hq, pr.Hkv, pr.N, nt, pr.causal, pr.striped);
@@ -609,7 +722,71 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
+template <int D, bool RAGGED>
+static int launch_step_impl(const StepProblem& pr, unsigned int* status, unsigned int* work,
+                            int sm_count, cudaStream_t stream) {
+    using C = Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.Sb, kv_rows = (int64_t)pr.B * pr.Hkv * pr.Sb;
+    if (!encode_rows_bf16(&mq, pr.q, q_rows, D) || !encode_rows_bf16(&mk, pr.k, kv_rows, D) ||
+        !encode_rows_bf16(&mv, pr.v, kv_rows, D))
+        return RA_ERR_CUDA;
+    Params P = {};
+    const int Sb = (int)pr.Sb;
+    const int nt = (Sb + kT - 1) / kT;
+    // items: the query tiles of the one local shard (a ring of one device);
+    // the masks come from the real ring
+    P.G = make_item_geom(pr.B, pr.Hq, pr.Hkv, 1, nt, pr.causal, pr.layout);
+    P.ring = RingGeom{pr.N, nt, pr.causal, pr.layout};
+    P.step_i = pr.i;
+    P.step_j = pr.j;
+    P.step_s = ((pr.i - pr.j) % pr.N + pr.N) % pr.N;
+    P.step_first = pr.first;
+    P.step_last = pr.last;
+    P.state_o = pr.state_o;
+    P.state_lse = pr.state_lse;
+    P.S = Sb;
+    P.Sb = Sb;
+    P.rem = Sb - (nt - 1) * kT;
+    P.sl2 = (float)((double)pr.scale * 1.4426950408889634);
+    P.out = static_cast<__nv_bfloat16*>(pr.out);
+    P.lse = pr.lse;
+    P.status = status;
+    P.work = work;
+    P.timeout_cycles = kTimeoutCycles;
+    if (P.G.n_items <= 0) return RA_OK;
+    if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
+    auto kern = fwd_kernel<D, false, false, RAGGED, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return RA_ERR_CUDA;
+    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
+    kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, P);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
 }  // namespace tc
+
+bool tc_step_supported(const StepProblem& p) {
+    if (p.D != 64 && p.D != 128) return false;
+    if (p.Sb <= 0 || p.Sb > (1ll << 30)) return false;
+    if (p.layout == kZigzag && p.Sb % (2 * tc::kT)) return false;
+    if ((int64_t)p.B * p.Hq * p.Sb >= (1ll << 31) || (int64_t)p.B * p.Hkv * p.Sb >= (1ll << 31))
+        return false;
+    return true;
+}
+
+int launch_tc_step(const StepProblem& p, unsigned int* status, unsigned int* work, int sm_count,
+                   cudaStream_t stream) {
+    if (!tc_step_supported(p)) return RA_ERR_UNSUPPORTED;
+    if (!work) return RA_ERR_INVALID_ARG;
+    const bool ragged = p.Sb % tc::kT != 0;
+    if (p.D == 128)
+        return ragged ? tc::launch_step_impl<128, true>(p, status, work, sm_count, stream)
+                      : tc::launch_step_impl<128, false>(p, status, work, sm_count, stream);
+    return ragged ? tc::launch_step_impl<64, true>(p, status, work, sm_count, stream)
+                  : tc::launch_step_impl<64, false>(p, status, work, sm_count, stream);
+}
 
 bool tc_supported(const FwdProblem& p) {
     if (p.dtype != RA_BF16 || (p.D != 64 && p.D != 128)) return false;

@@ -88,6 +88,37 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tm, uint32_t a_tm, uint32_t b_
                 (acc || kk > 0) ? 1u : 0u);
 }
 
+// Half tiles of the dk/dv kernel: 64 of a query tile's 128 rows, starting
+// 64 rows (8 KiB of 128-byte rows) into each box of the smem slot.
+constexpr uint32_t kHalfBytes = 64 * 128;
+
+// D = A B^T for a K-major 128 x HD tile A and the 64 K-major rows of B at
+// b_smem (M = 128, N = 64, HD/16 K-steps of 16).
+template <int HD>
+__device__ __forceinline__ void mma_nt_n64(uint32_t d_tm, uint32_t a_smem, uint32_t b_smem) {
+    constexpr uint32_t idesc = make_idesc_bf16(128, 64, false, false);
+    const uint64_t da = make_sdesc(a_smem, 16, 1024, kLayoutSW128);
+    const uint64_t db = make_sdesc(b_smem, 16, 1024, kLayoutSW128);
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off16 = ((kk / 4) * kBoxBytes + (kk % 4) * 32) >> 4;
+        umma_ss(d_tm, da + off16, db + off16, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// D (+)= A B: A is 128 x 64 bf16 in TMEM (32 columns), B the 64 row-major
+// rows of HD columns at b_smem, read MN-major (4 K-steps of 16 rows).
+template <int HD>
+__device__ __forceinline__ void mma_tn_k64(uint32_t d_tm, uint32_t a_tm, uint32_t b_smem,
+                                           bool acc) {
+    constexpr uint32_t idesc = make_idesc_bf16(128, HD, false, true);
+    const uint64_t db = make_sdesc(b_smem, kBoxBytes, 1024, kLayoutSW128);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        umma_ts(d_tm, a_tm + kk * 8, db + (uint64_t)((kk * 2048) >> 4), idesc,
+                (acc || kk > 0) ? 1u : 0u);
+}
+
 struct Params {
     TileGeom G;
     int64_t S;
@@ -500,10 +531,14 @@ constexpr int kBarOff = kVecOff + 2 * kVecBytes;
 enum {
     bKVFull = 0, bKVEmpty, bQFull, bQEmpty = bQFull + kQStages, bDOFull = bQEmpty + kQStages,
     bDOEmpty = bDOFull + kDOStages, bVecFull = bDOEmpty + kDOStages, bVecEmpty = bVecFull + 2,
-    bSFull = bVecEmpty + 2, bSRead, bPFull, bDPFull, bDPRead, bDsFull, bAccFull, bAccEmpty,
+    // per query half h of the tile: S^T(h) done, P^T(h) written, dP^T(h) done, dS^T(h) written
+    bSFull = bVecEmpty + 2, bPFull = bSFull + 2, bDPFull = bPFull + 2, bDsFull = bDPFull + 2,
+    bAccFull = bDsFull + 2, bAccEmpty,
     bDrain, bItemFull = bDrain + 2, bItemEmpty = bItemFull + 2, kNumBars = bItemEmpty + 2
 };
 constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 32 + 1024;
+// S^T of query half h in columns [64h, 64h + 64) (P^T written over the first
+// 32 of them), dP^T of half h at 128 + 64h (dS^T over its first 32), then dV, dK.
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 // readers of a published item: two MMA issuers, the row-vector warp, eight softmax warps
 constexpr uint32_t kItemReaders = 11;
@@ -546,12 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bVecFull + s), 32);
             mbar_init(bar(bVecEmpty + s), 8);
         }
-        mbar_init(bar(bSFull), 1);
-        mbar_init(bar(bSRead), 8);
-        mbar_init(bar(bPFull), 8);
-        mbar_init(bar(bDPFull), 1);
-        mbar_init(bar(bDPRead), 8);
-        mbar_init(bar(bDsFull), 8);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(bar(bSFull + h), 1);
+            mbar_init(bar(bPFull + h), 4);  // the four warps of half h's warpgroup
+            mbar_init(bar(bDPFull + h), 1);
+            mbar_init(bar(bDsFull + h), 4);
+        }
         mbar_init(bar(bAccFull), 2);
         mbar_init(bar(bAccEmpty), 8);
         mbar_init(bar(bDrain), 1);
@@ -662,29 +697,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuers
         // Two issuer threads on disjoint tensor memory, so that one's waits on
         // the softmax overlap the other's GEMMs in the pipe:
-        //   lane 0 of warp 1: S^T(n) into S, then dV += P^T(n) dO(n) reading S;
-        //   lane 0 of warp 2: dP^T(n) into dP, then dK += dS^T(n) Q(n) reading dP.
-        // Each keeps its own in-order reuse (S(n+1) after dV(n), dP(n+1) after
-        // dK(n)); stages and accumulators both read complete on two commits.
+        //   lane 0 of warp 1: S^T(n, h) = K Q(n, h)^T for the two query halves h
+        //   of tile n, then dV += P^T(n, h) dO(n, h) reading S^T's columns;
+        //   lane 0 of warp 2: dP^T(n, h) = V dO(n, h)^T, then dK += dS^T(n, h)
+        //   Q(n, h) reading dP^T's columns.
+        // Each half has its own columns and its own softmax warpgroup, so the
+        // next tile's S^T(n+1, h) is issued right behind dV(n, h) (in-order
+        // pipe) without waiting for the other half's softmax.  Stages and
+        // accumulators read by both issuers complete on two commits.
         if (lane == 0) {
             const bool is_s = (warp == 1);
+            const uint32_t sc_col = tmem + (is_s ? kColS : kColDP);
+            const uint32_t acc_col = tmem + (is_s ? kColDV : kColDK);
+            const uint32_t a_kv = base + (is_s ? kKOff : kVOff);
+            const int full_in = is_s ? bQFull : bDOFull;      // B of the score GEMM
+            const uint32_t off_in = is_s ? kQOff : kDOOff;
+            const uint32_t off_acc = is_s ? kDOOff : kQOff;   // B of the accumulation GEMM
+            const int sig_full = is_s ? bSFull : bDPFull;
+            const int sig_ready = is_s ? bPFull : bDsFull;
             uint32_t g = 0;
             int k = 0;
             bool ok = true;
-            // S^T(gg) = K Q(gg)^T or dP^T(gg) = V dO(gg)^T
-            auto issue_first = [&](uint32_t gg) -> bool {
-                const int full = is_s ? bQFull : bDOFull;
-                if (!wait_bar(bar(full + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status,
-                              wlim))
+            auto wait_in = [&](uint32_t gg) -> bool {
+                if (!wait_bar(bar(full_in + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status, wlim))
                     return false;
                 tc_fence_after();
-                if (is_s)
-                    mma_nt<D>(tmem + kColS, base + kKOff, base + kQOff + (gg & 1) * kTileBytes, false);
-                else
-                    mma_nt<D>(tmem + kColDP, base + kVOff, base + kDOOff + (gg & 1) * kTileBytes,
-                           false);
-                umma_commit(bar(is_s ? bSFull : bDPFull));
                 return true;
+            };
+            // S^T(gg, h) = K Q(gg, h)^T resp. dP^T(gg, h) = V dO(gg, h)^T
+            auto issue_score = [&](uint32_t gg, int h) {
+                mma_nt_n64<D>(sc_col + 64 * h, a_kv,
+                              base + off_in + (gg & 1) * kTileBytes + h * kHalfBytes);
+                umma_commit(bar(sig_full + h));
             };
             for (;; ++k) {
                 const long long item = read_item(k, ok);
@@ -695,32 +739,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 KeyWalk w;
                 w.start(G.rg, t.j, t.kt, heads);
-                if (!(ok = issue_first(g))) break;
+                if (!(ok = wait_in(g))) break;
+                issue_score(g, 0);
+                issue_score(g, 1);
                 for (uint32_t n = 0; !w.done(G.rg); ++n, ++g) {
                     KeyWalk nx = w;
                     nx.next(G.rg, t.j, t.kt, heads);
                     const bool more = !nx.done(G.rg);
-                    // P^T(n) resp. dS^T(n) written by the softmax
-                    if (!(ok = wait_bar(bar(is_s ? bPFull : bDsFull), g & 1, abort_flag, p.status,
-                                        wlim)))
-                        break;
-                    if (n == 0 && k > 0 &&
-                        !(ok = wait_bar(bar(bAccEmpty), (k - 1) & 1, abort_flag, p.status,
-                                        wlim)))
-                        break;
-                    tc_fence_after();
-                    if (is_s) {
-                        mma_tn<D>(tmem + kColDV, tmem + kColS, base + kDOOff + (g & 1) * kTileBytes,
-                               n > 0);
-                        umma_commit(bar(bDOEmpty + (g & 1)));
-                        umma_commit(bar(bQEmpty + (g & 1)));  // S(n) read Q(n)
-                    } else {
-                        mma_tn<D>(tmem + kColDK, tmem + kColDP, base + kQOff + (g & 1) * kTileBytes,
-                               n > 0);
-                        umma_commit(bar(bQEmpty + (g & 1)));
-                        umma_commit(bar(bDOEmpty + (g & 1)));  // dP(n) read dO(n)
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        // P^T(n, h) resp. dS^T(n, h) written by half h's warpgroup
+                        if (!(ok = wait_bar(bar(sig_ready + h), g & 1, abort_flag, p.status,
+                                            wlim)))
+                            break;
+                        if (n == 0 && h == 0 && k > 0 &&
+                            !(ok = wait_bar(bar(bAccEmpty), (k - 1) & 1, abort_flag, p.status,
+                                            wlim)))
+                            break;
+                        tc_fence_after();
+                        mma_tn_k64<D>(acc_col, sc_col + 64 * h,
+                                      base + off_acc + (g & 1) * kTileBytes + h * kHalfBytes,
+                                      n > 0 || h > 0);
+                        if (h == 1) {  // every MMA of this tile reading Q(n) and dO(n) is issued
+                            umma_commit(bar(bDOEmpty + (g & 1)));
+                            umma_commit(bar(bQEmpty + (g & 1)));
+                        }
+                        if (more) {
+                            if (h == 0 && !(ok = wait_in(g + 1))) break;
+                            issue_score(g + 1, h);
+                        }
                     }
-                    if (more && !(ok = issue_first(g + 1))) break;
+                    if (!ok) break;
                     w = nx;
                 }
                 if (!ok) break;
@@ -796,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!key_ok || kind == kNone) lo = kT;
                 const float* vs = vec + (g & 1) * (2 * kT);
                 // ---- P^T = exp2(S^T scale log2e - lse log2e), over S^T
-                ok = wait_bar(bar(bSFull), g & 1, abort_flag, p.status, wlim);
+                ok = wait_bar(bar(bSFull + wg), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sr[2][32];
@@ -805,9 +853,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 reg_fence(sr[0]);
                 reg_fence(sr[1]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bSRead));
                 ok = wait_bar(bar(bVecFull + (g & 1)), (g >> 1) & 1, abort_flag, p.status,
                               wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -852,15 +897,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[cc * 16 + e / 2 + 1] = pack_bf16x2(pf[cc][e + 2], pf[cc][e + 3]);
                         }
                 }
-                ok = wait_bar(bar(bSRead), g & 1, abort_flag, p.status, wlim);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tmem_st32(tmem + lane_off + kColS + 32 * wg, pk);
+                // this warpgroup alone reads and writes its half's columns
+                tmem_st32(tmem + lane_off + kColS + q0, pk);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bPFull));
+                if (lane == 0) mbar_arrive(bar(bPFull + wg));
                 // ---- dS^T = P^T (dP^T - delta), over dP^T
-                ok = wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, wlim);
+                ok = wait_bar(bar(bDPFull + wg), g & 1, abort_flag, p.status, wlim);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t dp[2][32];
@@ -869,9 +913,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 reg_fence(dp[0]);
                 reg_fence(dp[1]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bDPRead));
                 const float4* dl4 = reinterpret_cast<const float4*>(vs + kT + q0);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
@@ -891,14 +932,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[cc * 16 + e / 2 + 1] = pack_bf16x2(d[2], d[3]);
                     }
                 }
-                ok = wait_bar(bar(bDPRead), g & 1, abort_flag, p.status, wlim);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tmem_st32(tmem + lane_off + kColDP + 32 * wg, pk);
+                tmem_st32(tmem + lane_off + kColDP + q0, pk);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(bDsFull));
+                    mbar_arrive(bar(bDsFull + wg));
                     mbar_arrive(bar(bVecEmpty + (g & 1)));
                 }
             }

@@ -86,6 +86,9 @@ enum {
     RA_KERNEL_SIMT = 2  /* fp32 SIMT kernel (any D <= 256, any Sb); f32 or bf16 */
 };
 
+/* Flags of ra_ring_step. */
+enum { RA_STEP_FIRST = 1, RA_STEP_LAST = 2 };
+
 /* Fold kinds reported by ra_plan / ra_fold_log. */
 enum { RA_FOLD_FULL = 0, RA_FOLD_INCL = 1, RA_FOLD_STRICT = 2 };
 
@@ -153,6 +156,49 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
 int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                   int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
                   int dtype, int kernel, void* stream);
+
+/*
+ * ra_ring_step: one step of a ring whose devices are separate processes (or
+ * GPUs): query shard i folds the key/value block j it holds at this step into
+ * its running online-softmax state.  This is the per-device step of the
+ * method: device i keeps its query block, at ring step s it holds block
+ * j = (i - s) mod N received from the previous device, computes the scores
+ * of its queries against that block and folds them into a running maximum,
+ * normaliser and rescaled numerator (glossary page, "Como funciona a atencao
+ * em anel"; aiunderstanding.org, "Immersione profonda": only K and V travel
+ * round the ring, the transfer hidden behind the block's compute, and
+ * "Approfondimento tecnico": the online-softmax fold).  Moving the block
+ * between devices is the caller's (the package's ring driver uses
+ * torch.distributed send/recv); this call only computes.
+ *   q        [B, Hq, Sb, D] bf16 (read): query shard i.
+ *   k, v     [B, Hkv, Sb, D] bf16 (read): key/value block j.
+ *   state_o  [B, Hq, Sb, D] float32, state_lse [B, Hq, Sb] float32: the
+ *            running state, the normalised output and natural-log
+ *            log-sum-exp of the blocks folded so far (-inf, output 0, for a
+ *            row that has seen no visible key).  Read unless RA_STEP_FIRST,
+ *            written unless RA_STEP_LAST; may be NULL when both flags are set.
+ *   out      [B, Hq, Sb, D] bf16, lse [B, Hq, Sb] float32: written only with
+ *            RA_STEP_LAST (the state after this fold, as ra_forward's outputs
+ *            for shard i); out must then be given, lse may be NULL.
+ *   Sb: tokens per shard (any Sb >= 0 for contiguous and striped shards;
+ *   zigzag needs Sb % 256 == 0).  N: ring devices; 0 <= i, j < N.  causal,
+ *   layout (RA_LAYOUT_*), scale: as ra_forward, applied to the global token
+ *   positions of shard i's queries and block j's keys, so folding blocks
+ *   j = i, i-1, ..., i-N+1 (mod N) with the first flagged RA_STEP_FIRST and
+ *   the last RA_STEP_LAST gives ra_forward's result for shard i.  A block
+ *   with no visible pair leaves the state as it was.
+ *   flags: RA_STEP_FIRST | RA_STEP_LAST (both for N = 1).
+ * The fold of a block's partial (O_b, lse_b) into the state (O_s, lse_s) is
+ * the log-sum-exp weighting of ra_merge, in fp32:
+ *   lse = ln(e^lse_s + e^lse_b),  O = e^(lse_s-lse) O_s + e^(lse_b-lse) O_b.
+ * Runs the tcgen05 tensor-core kernel (bf16, D in {64, 128}).
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_ALIGN (any pointer not 16-byte
+ * aligned), RA_ERR_UNSUPPORTED (D, device, or B*Hq*Sb >= 2^31 rows),
+ * RA_ERR_CUDA.  An empty problem (B == 0 or Sb == 0) is a no-op.
+ */
+int ra_ring_step(const void* q, const void* k, const void* v, float* state_o, float* state_lse,
+                 void* out, float* lse, int B, int Hq, int Hkv, int64_t Sb, int D, int N, int i,
+                 int j, int causal, int layout, float scale, int flags, void* stream);
 
 /*
  * ra_merge: fold partial result b into partial result a, in place.

@@ -259,3 +259,32 @@ def test_size_limits_are_rejected_before_any_device_work(lib):
     assert bwd(1, 1 << 14, 1, 1 << 17, 128, 16, ra.RA_KERNEL_TC) == ra.RA_ERR_UNSUPPORTED
     assert bwd(1, 1 << 16, 1, 1 << 15, 128, 8, ra.RA_KERNEL_AUTO) == ra.RA_ERR_UNSUPPORTED
     assert bwd(1, 2, 1, 256, 32, 2, ra.RA_KERNEL_TC) == ra.RA_ERR_UNSUPPORTED  # D = 32
+
+
+def test_ring_step_host_validation(lib):
+    """ra_ring_step refuses bad arguments on the host, before any CUDA call."""
+    p = ctypes.c_void_p(16 * 1024)  # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(16 * 1024 + 8)
+
+    def call(q=p, st_o=p, st_l=p, out=p, lse=p, B=1, Hq=2, Hkv=1, Sb=256, D=128, N=4, i=1,
+             j=0, layout=1, flags=0):
+        return ra.ra_ring_step(q, p, p, st_o, st_l, out, lse, B, Hq, Hkv, Sb, D, N, i, j, 1,
+                               layout, 0.0, flags, None)
+
+    F, L = ra.RA_STEP_FIRST, ra.RA_STEP_LAST
+    assert call(i=4) == ra.RA_ERR_INVALID_ARG            # shard outside the ring
+    assert call(j=-1) == ra.RA_ERR_INVALID_ARG
+    assert call(Hq=3, Hkv=2) == ra.RA_ERR_INVALID_ARG    # Hq % Hkv
+    assert call(flags=4) == ra.RA_ERR_INVALID_ARG        # unknown flag
+    assert call(layout=3) == ra.RA_ERR_INVALID_ARG
+    assert call(layout=2, Sb=255) == ra.RA_ERR_INVALID_ARG
+    assert call(q=None) == ra.RA_ERR_INVALID_ARG
+    assert call(st_o=None) == ra.RA_ERR_INVALID_ARG      # the state is read and written
+    assert call(st_l=None, flags=F) == ra.RA_ERR_INVALID_ARG
+    assert call(out=None, flags=L) == ra.RA_ERR_INVALID_ARG
+    assert call(st_o=odd) == ra.RA_ERR_ALIGN
+    assert call(lse=odd, flags=L) == ra.RA_ERR_ALIGN
+    assert call(D=96) == ra.RA_ERR_UNSUPPORTED           # tensor-core head dimensions only
+    assert call(layout=2, Sb=384) == ra.RA_ERR_UNSUPPORTED  # zigzag chunks must be whole tiles
+    assert call(B=0) == ra.RA_OK                         # empty: nothing to do
+    assert call(Sb=0, q=None) == ra.RA_OK
