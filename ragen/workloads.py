@@ -79,6 +79,9 @@ WORKLOADS = {
     # profiling case: same kernel shape as gqa_128k, inputs larger than L2 but under 1 GB
     "prof_64k": Workload(5, "bf16_causal_gqa_B1_Hq16_Hkv4_S65536_N8_D128_striped", "bf16",
                          1, 16, 4, 65536, 8, 128, True, True),
+    # the 128K GQA shape at head dimension 64 (a tensor-core kernel variant)
+    "gqa_128k_d64": Workload(7, "bf16_causal_gqa_B1_Hq32_Hkv8_S131072_N16_D64_striped", "bf16",
+                             1, 32, 8, 131072, 16, 64, True, 1),
     "long_1m": Workload(4, "bf16_causal_gqa_B1_Hq8_Hkv1_S1048576_N64_D128_striped", "bf16",
                         1, 8, 1, 1048576, 64, 128, True, True),
 }
