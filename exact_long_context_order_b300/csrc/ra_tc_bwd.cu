@@ -18,9 +18,12 @@
 //    accumulators travel with the block round the ring in its cyclic order,
 //    entering it at device 0 (query shards i = 0..N-1, so that blocks running
 //    together read the same query tiles from L2), and in each shard the
-//    query tiles that see it, for every query head of its GQA group.  Per query tile: S^T = K Q^T and
-//    dP^T = V dO^T; P^T and dS^T (bf16) are written over them; dV += P^T dO
-//    and dK += dS^T Q (A from TMEM, dO and Q read MN-major).
+//    query tiles that see it, for every query head of its GQA group.  Each
+//    query tile is taken as two halves of 64 rows with their own TMEM
+//    columns: S^T = K Q^T and dP^T = V dO^T per half; P^T and dS^T (bf16) are
+//    written over them; dV += P^T dO and dK += dS^T Q (A from TMEM, dO and Q
+//    read MN-major).  Each half is its own dependency chain, so the next
+//    tile's half follows this tile's same half without waiting for the other.
 // Both kernels recompute S and dP, so a tile pair costs 7 tile GEMMs where a
 // single kernel reducing dQ across key tiles would cost 5.
 //
@@ -29,7 +32,8 @@
 // signal, the other's GEMMs keep the tensor core busy): warps 1 and 3 in
 // dq_kernel, warps 1 and 2 in dkv_kernel, where warp 3 stages the per-row lse
 // and delta of each query tile; warp 2 owns TMEM; warps 4-11 are two
-// warpgroups that split the 128 columns of each score tile.  Every mbarrier
+// warpgroups that split the 128 columns of each score tile (in dkv_kernel,
+// one query half each).  Every mbarrier
 // wait is bounded; on time-out a kernel records kStatusTimeout, drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
