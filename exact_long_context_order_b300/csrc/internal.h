@@ -35,9 +35,15 @@ struct FoldLog {
 // SM cycles) bounds every wait of the kernel; withhold_first_k = 1 is the
 // failure-detection self test (each CTA's first K-tile copy is never issued,
 // so its waits run out and the kernel reports kStatusTimeout).
+// split_mode 1 lets a non-causal problem with one to two items per SM run
+// as stream-K (fixed contiguous work ranges per CTA; an item cut between two
+// CTAs is combined from the tail's partial, scratch taken from a library
+// memory pool on `stream`); 0 always uses the dynamic queue.
 int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, unsigned int* work,
               int sm_count, cudaStream_t stream, long long timeout_cycles = 0,
-              int withhold_first_k = 0);
+              int withhold_first_k = 0, int split_mode = 0);
+// Whether launch_tc with split_mode 1 runs p as stream-K (host only).
+bool tc_uses_streamk(const FwdProblem& p, int sm_count);
 bool tc_supported(const FwdProblem& p);
 // Device address of the current device's status word (read by ra_check).
 int device_status_word(unsigned int** status);

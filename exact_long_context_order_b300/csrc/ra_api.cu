@@ -238,7 +238,8 @@ int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float*
     if (use_tc) {
         unsigned int* work = nullptr;
         if ((rc = work_slot(&work))) return rc;
-        rc = ra::launch_tc(p, nullptr, status, work, sms, st);
+        rc = ra::launch_tc(p, nullptr, status, work, sms, st, 0, 0,
+                           kernel == RA_KERNEL_AUTO ? 1 : 0);
     } else
         rc = ra::launch_simt(p, status, st);
     if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
@@ -346,6 +347,15 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
     const int64_t esz = (dtype == RA_F32) ? 4 : 2;
     const int64_t G = (int64_t)B * Hkv;  // (batch, KV head) groups
     int nch = (G >= 4 && G <= 0x7fffffff) ? (int)std::min<int64_t>(G, kHostChunks) : 1;
+    {
+        // A problem ra_forward runs as stream-K cuts items at places a chunk
+        // would not: run it whole, so the outputs stay the same bits.
+        int sms = 0;
+        if ((rc = device_state(nullptr, &sms))) return rc;
+        const ra::FwdProblem whole = make_problem(q_dev, k_dev, v_dev, out_dev, lse_dev, B, Hq,
+                                                  Hkv, S, D, N, causal, striped, scale, dtype);
+        if (ra::tc_uses_streamk(whole, sms)) nch = 1;
+    }
     const int g = Hq / Hkv;
     const int64_t qg = (int64_t)g * S * D * esz, kvg = S * D * esz, lg = (int64_t)g * S;
     // Every chunk is a sub-problem whose device pointers must meet ra_forward's

@@ -36,6 +36,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -108,14 +109,38 @@ struct Params {
     int step_first, step_last;
     float* state_o;    // [B*Hq*Sb, D] running normalised output (fp32)
     float* state_lse;  // [B*Hq*Sb] running log-sum-exp (natural log)
+    // Stream-K launches only (non-causal problems with one to two items per
+    // SM, every item folding fold_len key tiles): CTA c takes the c-th equal,
+    // contiguous range of the flattened (item, fold position) space instead of
+    // items from the queue, so the last wave leaves no SM idle.  An item cut
+    // between CTAs c and c+1 runs as a head segment [0, p) at the end of c's
+    // range and a tail segment [p, fold_len) at the start of c+1's.  The tail
+    // writes its partial (O/l and lse, fp32) to part_o / part_lse and raises
+    // its warp's flag; the head, which finishes later, waits for the flag and
+    // combines the partial with its own O and l by the log-sum-exp weighting.
+    long long n_work;          // work values >= n_work end a CTA's loop
+    int fold_len;
+    float* part_o;             // [n_items][2 slots][D/4 chunks][128 rows] float4
+    float* part_lse;           // [n_items][2 slots][128 rows]
+    unsigned int* part_flag;   // [n_items][2 slots][4 warps], zero at launch
 };
 
-// The fold list of an item: every ring step (TileWalk), or in a ring step
-// only the key tiles of the block that step holds.
-template <bool STEP>
+enum Mode : int { kModeRing = 0, kModeStep = 1, kModeStreamK = 2 };
+
+// A work value: an item index, or in stream-K launches an item and the range
+// [b, e) of its fold positions, packed as item << 32 | b << 16 | e.
+struct Work {
+    long long item;
+    int b, e;
+};
+
+// The fold list of an item: every ring step (TileWalk), the key tiles of
+// the one block a ring step holds, or fold positions [b, e) of a stream-K
+// segment (non-causal: position s*nt + kt is key tile kt of shard (i - s)).
+template <int MODE>
 __device__ __forceinline__ void walk_start(TileWalk& w, const ItemGeom& G, const Params& p,
-                                           const Item& it) {
-    if constexpr (STEP) {
+                                           const Item& it, const Work& wk) {
+    if constexpr (MODE == kModeStep) {
         w.s = p.step_s;
         w.j = p.step_j;
         w.kt = 0;
@@ -123,25 +148,57 @@ __device__ __forceinline__ void walk_start(TileWalk& w, const ItemGeom& G, const
         shard_span(p.ring, p.step_i, p.step_j, it.qt[0], &nk0, &d);
         shard_span(p.ring, p.step_i, p.step_j, it.qt[1], &nk1, &d);
         w.nk = nk0 > nk1 ? nk0 : nk1;
+    } else if constexpr (MODE == kModeStreamK) {
+        const int nt = G.rg.nt;
+        w.s = wk.b / nt;
+        w.kt = wk.b % nt;
+        w.nk = wk.e;  // the end position
+        w.j = it.i - w.s;
+        if (w.j < 0) w.j += G.rg.N;
     } else {
+        (void)wk;
         w.start(G.rg, it);
     }
 }
-template <bool STEP>
+template <int MODE>
 __device__ __forceinline__ bool walk_done(const TileWalk& w, const ItemGeom& G) {
-    if constexpr (STEP) return w.kt >= w.nk;
+    if constexpr (MODE == kModeStep) return w.kt >= w.nk;
+    else if constexpr (MODE == kModeStreamK) return w.s * G.rg.nt + w.kt >= w.nk;
     else return w.done(G.rg);
 }
-template <bool STEP>
+template <int MODE>
 __device__ __forceinline__ void walk_next(TileWalk& w, const ItemGeom& G, const Item& it) {
-    if constexpr (STEP) ++w.kt;
-    else w.next(G.rg, it);
+    if constexpr (MODE == kModeStep) {
+        ++w.kt;
+    } else if constexpr (MODE == kModeStreamK) {
+        if (++w.kt >= G.rg.nt) {
+            w.kt = 0;
+            ++w.s;
+            w.j = it.i - w.s;
+            if (w.j < 0) w.j += G.rg.N;
+        }
+    } else {
+        w.next(G.rg, it);
+    }
+}
+template <int MODE>
+__device__ __forceinline__ Work decode_work(long long v) {
+    Work wk;
+    if constexpr (MODE == kModeStreamK) {
+        wk.item = v >> 32;
+        wk.b = (int)((v >> 16) & 0xffff);
+        wk.e = (int)(v & 0xffff);
+    } else {
+        wk.item = v;
+        wk.b = wk.e = 0;
+    }
+    return wk;
 }
 
-// RAGGED: the shard size is not a multiple of the tile, so each shard's last
-// query and key tile is partial (compiled out of the common case).
-// STEP: one step of a ring whose devices are separate processes (see Params).
-template <int D, bool LOG, bool SELFTEST, bool RAGGED, bool STEP = false>
+// MODE: kModeRing (the whole ring, items from the dynamic queue), kModeStep
+// (one step of a ring whose devices are separate processes) or kModeStreamK
+// (fixed contiguous work ranges per CTA; see Params).
+template <int D, bool LOG, bool SELFTEST, bool RAGGED, int MODE = kModeRing>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -202,9 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // producer takes the next index from the global counter one item ahead and
     // publishes it in a two-entry shared ring; every role reads it from there.
     // An index >= n_items ends the CTA's loop.
+    constexpr bool STEP = MODE == kModeStep, STREAMK = MODE == kModeStreamK;
     auto read_item = [&](int k, bool& ok) -> long long {
         ok = wait_bar(bar(C::bItemFull + (k & 1)), (k >> 1) & 1, abort_flag, p.status, wlim);
-        return ok ? item_slot[k & 1] : G.n_items;
+        return ok ? item_slot[k & 1] : p.n_work;
     };
     if (warp < 4) regs_dec<kRegsOther>();
     if (warp == 0) {
@@ -223,12 +281,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(C::bItemFull + (kk & 1)));
                 return true;
             };
-            long long item = (long long)atomicAdd(p.work, 1u);
+            // stream-K: this CTA's contiguous range of (item, fold position)
+            const long long total = STREAMK ? G.n_items * (long long)p.fold_len : 0;
+            long long sk_cur = STREAMK ? total * blockIdx.x / gridDim.x : 0;
+            const long long sk_end = STREAMK ? total * (blockIdx.x + 1) / gridDim.x : 0;
+            auto next_work = [&]() -> long long {
+                if constexpr (STREAMK) {
+                    if (sk_cur >= sk_end) return p.n_work;
+                    const long long itm = sk_cur / p.fold_len;
+                    const int b = (int)(sk_cur % p.fold_len);
+                    const long long left = sk_end - sk_cur;
+                    const int e = (left < p.fold_len - b) ? b + (int)left : p.fold_len;
+                    sk_cur += e - b;
+                    return (itm << 32) | ((long long)b << 16) | e;
+                } else {
+                    return (long long)atomicAdd(p.work, 1u);
+                }
+            };
+            long long item = next_work();
             ok = publish(0, item);
-            for (; ok && item < G.n_items; ++k) {
-                const long long next = (long long)atomicAdd(p.work, 1u);
+            for (; ok && item < p.n_work; ++k) {
+                const long long next = next_work();
                 if (!(ok = publish(k + 1, next))) break;
-                const Item it = decode_item(G, item);
+                const Work wk = decode_work<MODE>(item);
+                const Item it = decode_item(G, wk.item);
                 item = next;
                 if (k > 0 && !(ok = wait_bar(bar(C::bQEmpty), (k - 1) & 1, abort_flag, p.status, wlim)))
                     break;
@@ -243,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int64_t kvrow0 = (int64_t)(it.b * G.Hkv + it.kvh) * p.S;
                 TileWalk w;
-                for (walk_start<STEP>(w, G, p, it); !walk_done<STEP>(w, G) && ok;
-                     walk_next<STEP>(w, G, it)) {
+                for (walk_start<MODE>(w, G, p, it, wk); !walk_done<MODE>(w, G) && ok;
+                     walk_next<MODE>(w, G, it)) {
                     // a ring step's buffer holds only the block it folds
                     const int64_t jrow = STEP ? 0 : (int64_t)w.j * p.Sb;
                     const int row = (int)(kvrow0 + jrow + (int64_t)w.kt * kT);
@@ -335,13 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (;; ++k) {
                 const long long item = read_item(k, ok);
                 if (ok) mbar_arrive(bar(C::bItemEmpty + (k & 1)));
-                if (!ok || item >= G.n_items) break;
-                const Item it = decode_item(G, item);
+                if (!ok || item >= p.n_work) break;
+                const Work wk = decode_work<MODE>(item);
+                const Item it = decode_item(G, wk.item);
                 if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status, wlim))) break;
                 TileWalk w;
                 uint32_t n = 0;
-                for (walk_start<STEP>(w, G, p, it); !walk_done<STEP>(w, G);
-                     walk_next<STEP>(w, G, it), ++n) {
+                for (walk_start<MODE>(w, G, p, it, wk); !walk_done<MODE>(w, G);
+                     walk_next<MODE>(w, G, it), ++n) {
                     const uint32_t stK = kv_pos % C::kStages;
                     if (!(ok = wait_bar(bar(C::bKVFull + stK), (kv_pos / C::kStages) & 1,
                                         abort_flag, p.status, wlim)))
@@ -425,8 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::bItemEmpty + (k & 1)));
-            if (item >= G.n_items) break;
-            const Item it = decode_item(G, item);
+            if (item >= p.n_work) break;
+            const Work wk = decode_work<MODE>(item);
+            const Item it = decode_item(G, wk.item);
             const int qt = t ? it.qt[1] : it.qt[0];
             const int hq = t ? it.h[1] : it.h[0];  // query head of this slot
             const bool valid = (t == 0) || it.valid1;
@@ -434,8 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int n_logged = 0;
             TileWalk w;
             uint32_t n = 0;
-            for (walk_start<STEP>(w, G, p, it); !walk_done<STEP>(w, G);
-                 walk_next<STEP>(w, G, it), ++n, ++gt) {
+            for (walk_start<MODE>(w, G, p, it, wk); !walk_done<MODE>(w, G);
+                 walk_next<MODE>(w, G, it), ++n, ++gt) {
                 const int kind = STEP ? fold_kind(p.ring, p.step_i, w.j, qt, w.kt)
                                       : fold_kind(G.rg, it.i, w.j, qt, w.kt);
                 ok = wait_bar(bar(C::bSFull + t), gt & 1, abort_flag, p.status, wlim);
@@ -632,6 +710,99 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!p.step_last) p.state_lse[row] = lse_n;
                     else if (p.lse) p.lse[row] = lse_n;
                 }
+            } else if (STREAMK && valid && !(wk.b == 0 && wk.e == p.fold_len)) {
+                // A segment of an item cut between two CTAs (see Params).
+                const int64_t row = (int64_t)(it.b * G.Hq + hq) * p.S + (int64_t)it.i * p.Sb +
+                                    (int64_t)qt * kT + r;
+                const bool row_ok = !RAGGED || qt < G.rg.nt - 1 || r < p.rem;
+                constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.69314718055994531f;
+                const int64_t blk = wk.item * 2 + t;  // the tail's partial of this slot
+                // column-chunk-major: float4 chunk cc of row r at [blk][cc][r], so
+                // a warp's 32 rows move 512 contiguous bytes per chunk
+                float4* pblk = reinterpret_cast<float4*>(p.part_o) + blk * (D / 4) * kT + r;
+                unsigned int* flag = p.part_flag + blk * 4 + (warp & 3);
+                const bool use_o = l > 0.f;
+                const float lse_own = use_o ? (m_used * sl2 + lg2_approx(l)) * kLn2 : -INFINITY;
+                if (wk.b > 0) {
+                    // tail segment: write the partial (O/l, lse), then raise the flag
+                    const float inv_l = use_o ? 1.f / l : 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(o_tm + c * 32, o);  // warp-collective: every lane loads
+                        tmem_wait_ld();
+                        reg_fence(o);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            pblk[(c * 8 + e) * kT] =
+                                make_float4(__uint_as_float(o[4 * e]) * inv_l,
+                                            __uint_as_float(o[4 * e + 1]) * inv_l,
+                                            __uint_as_float(o[4 * e + 2]) * inv_l,
+                                            __uint_as_float(o[4 * e + 3]) * inv_l);
+                    }
+                    p.part_lse[blk * kT + r] = lse_own;
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicExch(flag, 1u);
+                } else {
+                    // head segment, at the end of the previous CTA's range: the
+                    // tail ran at the start of the next CTA's, so its flag is
+                    // normally up already.  The wait is bounded all the same.
+                    bool have = true;
+                    if (lane == 0) {
+                        const long long t0 = clock64();
+                        while (atomicAdd(flag, 0u) == 0u) {
+                            if (clock64() - t0 > wlim) {
+                                atomicOr(p.status, kStatusTimeout);
+                                have = false;
+                                break;
+                            }
+                        }
+                    }
+                    have = __shfl_sync(0xffffffffu, have ? 1 : 0, 0) != 0;
+                    __threadfence();
+                    const float lse_tail = have ? __ldcg(p.part_lse + blk * kT + r) : -INFINITY;
+                    const float mx = fmaxf(lse_own, lse_tail);
+                    float w_own = 0.f, w_tail = 0.f, lse_n = -INFINITY;
+                    if (mx > -INFINITY) {
+                        const float e0 = ex2_approx((lse_own - mx) * kLog2e);
+                        const float e1 = ex2_approx((lse_tail - mx) * kLog2e);
+                        const float den = e0 + e1;
+                        w_own = use_o ? e0 / den / l : 0.f;  // applied to the unnormalised O
+                        w_tail = e1 / den;
+                        lse_n = mx + lg2_approx(den) * kLn2;
+                    }
+                    uint4* orow = reinterpret_cast<uint4*>(p.out + row * D);
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(o_tm + c * 32, o);  // warp-collective: every lane loads
+                        tmem_wait_ld();
+                        reg_fence(o);
+                        float4 tv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            tv[e] = have ? __ldcg(pblk + (c * 8 + e) * kT)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (row_ok) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 x = tv[2 * e], y = tv[2 * e + 1];
+                                const float* oo = reinterpret_cast<const float*>(&o[8 * e]);
+                                orow[c * 4 + e] = make_uint4(
+                                    pack_bf16x2(fmaf(w_own, oo[0], w_tail * x.x),
+                                                fmaf(w_own, oo[1], w_tail * x.y)),
+                                    pack_bf16x2(fmaf(w_own, oo[2], w_tail * x.z),
+                                                fmaf(w_own, oo[3], w_tail * x.w)),
+                                    pack_bf16x2(fmaf(w_own, oo[4], w_tail * y.x),
+                                                fmaf(w_own, oo[5], w_tail * y.y)),
+                                    pack_bf16x2(fmaf(w_own, oo[6], w_tail * y.z),
+                                                fmaf(w_own, oo[7], w_tail * y.w)));
+                            }
+                        }
+                    }
+                    if (row_ok && p.lse) p.lse[row] = lse_n;
+                }
             } else if (valid) {
                 const int64_t row = (int64_t)(it.b * G.Hq + hq) * p.S + (int64_t)it.i * p.Sb +
                                     (int64_t)qt * kT + r;
@@ -684,10 +855,87 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
+// Stream-K applies to non-causal problems with fewer than two items per SM
+// (the dynamic queue's last wave would leave SMs idle) and at least one item
+// per SM (so an item is cut between at most two CTAs, into a head and a
+// tail).  Every item then folds the same N * nt key tiles.
+static bool use_streamk(long long n_items, const FwdProblem& pr, int nt, int sm_count) {
+    const long long fold_len = (long long)pr.N * nt;
+    return !pr.causal && sm_count > 0 && n_items >= sm_count && n_items < 2ll * sm_count &&
+           fold_len <= 0xffff && n_items < (1ll << 31);
+}
+
+// The stream-K scratch (the tails' partials and flags) comes from a memory
+// pool the library owns per device, allocated and freed on the launch's
+// stream, so launches on different streams never share it; freed blocks stay
+// reserved in the pool (up to 1 GiB) for the next launch.  Under CUDA-graph
+// stream capture it is a graph allocation of the device's default pool.
+static std::mutex g_pool_mu;
+static cudaMemPool_t g_pool[64];
+
+static int scratch_alloc(void** ptr, int64_t bytes, cudaStream_t stream) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return RA_ERR_CUDA;
+    if (cap == cudaStreamCaptureStatusActive)
+        return cudaMallocAsync(ptr, bytes, stream) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RA_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return RA_ERR_UNSUPPORTED;
+    cudaMemPool_t pool = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_pool_mu);
+        if (!g_pool[dev]) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            cudaMemPool_t created = nullptr;
+            if (cudaMemPoolCreate(&created, &props) != cudaSuccess) return RA_ERR_CUDA;
+            uint64_t keep = 1ull << 30;
+            if (cudaMemPoolSetAttribute(created, cudaMemPoolAttrReleaseThreshold, &keep) !=
+                cudaSuccess)
+                return RA_ERR_CUDA;
+            g_pool[dev] = created;
+        }
+        pool = g_pool[dev];
+    }
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream) == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+template <int D, bool RAGGED>
+static int launch_streamk(Params P, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, int sm_count, cudaStream_t stream, int N) {
+    using C = Cfg<D>;
+    P.fold_len = N * P.G.rg.nt;
+    P.n_work = P.G.n_items << 32;
+    const int64_t rows = P.G.n_items * 2 * kT;  // [item][slot][row]
+    const int64_t o_bytes = rows * D * 4, l_bytes = (rows * 4 + 255) / 256 * 256;
+    const int64_t f_bytes = P.G.n_items * 8 * 4;
+    void* ws = nullptr;
+    int rc = scratch_alloc(&ws, o_bytes + l_bytes + f_bytes, stream);
+    if (rc) return rc;
+    P.part_o = static_cast<float*>(ws);
+    P.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+    P.part_flag = reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + o_bytes + l_bytes);
+    auto kern = fwd_kernel<D, false, false, RAGGED, kModeStreamK>;
+    if (cudaMemsetAsync(P.part_flag, 0, f_bytes, stream) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+            cudaSuccess) {
+        rc = RA_ERR_CUDA;
+    } else {
+        // one CTA per SM, every CTA resident: a head segment's wait for the
+        // next CTA's tail always ends
+        kern<<<(unsigned)sm_count, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, P);
+        if (cudaGetLastError() != cudaSuccess) rc = RA_ERR_CUDA;
+    }
+    if (cudaFreeAsync(ws, stream) != cudaSuccess) rc = RA_ERR_CUDA;
+    return rc;
+}
+
 template <int D, bool LOG, bool RAGGED>
 static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* status,
                        unsigned int* work, int sm_count, cudaStream_t stream,
-                       long long timeout_cycles, int withhold_first_k) {
+                       long long timeout_cycles, int withhold_first_k, int split_mode) {
     using C = Cfg<D>;
     CUtensorMap mq, mk, mv;
     const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.S, kv_rows = (int64_t)pr.B * pr.Hkv * pr.S;
@@ -710,7 +958,10 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     P.max_entries = flog ? flog->max_entries : 0;
     P.work = work;
     P.timeout_cycles = timeout_cycles > 0 ? timeout_cycles : kTimeoutCycles;
+    P.n_work = P.G.n_items;
     if (P.G.n_items <= 0) return RA_OK;
+    if (!LOG && !withhold_first_k && split_mode == 1 && use_streamk(P.G.n_items, pr, nt, sm_count))
+        return launch_streamk<D, RAGGED>(P, mq, mk, mv, sm_count, stream, pr.N);
     if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
     auto kern = withhold_first_k ? fwd_kernel<D, false, true, RAGGED>
                                  : fwd_kernel<D, LOG, false, RAGGED>;
@@ -754,9 +1005,10 @@ static int launch_step_impl(const StepProblem& pr, unsigned int* status, unsigne
     P.status = status;
     P.work = work;
     P.timeout_cycles = kTimeoutCycles;
+    P.n_work = P.G.n_items;
     if (P.G.n_items <= 0) return RA_OK;
     if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
-    auto kern = fwd_kernel<D, false, false, RAGGED, true>;
+    auto kern = fwd_kernel<D, false, false, RAGGED, kModeStep>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return RA_ERR_CUDA;
@@ -801,14 +1053,24 @@ bool tc_supported(const FwdProblem& p) {
     return true;
 }
 
+bool tc_uses_streamk(const FwdProblem& p, int sm_count) {
+    if (!tc_supported(p)) return false;
+    const int Sb = (int)(p.S / p.N);
+    const int nt = (Sb + tc::kT - 1) / tc::kT;
+    const ItemGeom G = make_item_geom(p.B, p.Hq, p.Hkv, p.N, nt, p.causal, p.striped);
+    return tc::use_streamk(G.n_items, p, nt, sm_count);
+}
+
 int launch_tc(const FwdProblem& p, const FoldLog* flog, unsigned int* status, unsigned int* work,
-              int sm_count, cudaStream_t stream, long long timeout_cycles, int withhold_first_k) {
+              int sm_count, cudaStream_t stream, long long timeout_cycles, int withhold_first_k,
+              int split_mode) {
     if (!tc_supported(p)) return RA_ERR_UNSUPPORTED;
     if (!work) return RA_ERR_INVALID_ARG;
     const bool ragged = (p.S / p.N) % tc::kT != 0;
     auto go = [&](auto d, auto lg, auto rg) {
         return tc::launch_impl<decltype(d)::value, decltype(lg)::value, decltype(rg)::value>(
-            p, flog, status, work, sm_count, stream, timeout_cycles, withhold_first_k);
+            p, flog, status, work, sm_count, stream, timeout_cycles, withhold_first_k,
+            split_mode);
     };
     using T = std::true_type;
     using F = std::false_type;

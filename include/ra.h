@@ -25,7 +25,9 @@
  *   allocates one 4 KiB block per device on the first tensor-core launch on
  *   that device (cudaMalloc, kept until exit): 64 work-queue counters, one
  *   per launch in flight, each zeroed on the launch's stream.  Make the first
- *   such call on a device outside CUDA-graph stream capture.
+ *   such call on a device outside CUDA-graph stream capture.  A forward run
+ *   as stream-K (see ra_forward_ex) also takes scratch, on its stream, from a
+ *   memory pool the library creates per device on first use.
  * - Layout is "shard-major": q and out are [B, Hq, S, D], k and v are
  *   [B, Hkv, S, D], lse is [B, Hq, S]; all row-major and contiguous.  Shard i
  *   owns rows [i*Sb, (i+1)*Sb) of every (b, h) slice, Sb = S / N.  The
@@ -125,7 +127,8 @@ int ra_forward(const void* q, const void* k, const void* v, void* out, float* ls
  * up to eight chunks of consecutive groups: chunk c+1's copies in overlap
  * chunk c's forward, and chunk c's copies out overlap later chunks'.  (A
  * chunk starts at an offset of whole groups into each staging buffer; if one
- * such offset is not a multiple of 16 bytes the call runs in order instead.)
+ * such offset is not a multiple of 16 bytes, or ra_forward would run the
+ * problem as stream-K (see ra_forward_ex), the call runs in order instead.)
  * That
  * work runs on streams the library creates for the device on first use (one
  * copy stream per direction, two compute streams, kept until the process
@@ -152,7 +155,23 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
                     int striped, float scale, int dtype, void* stream);
 
 /* ra_forward with an explicit kernel choice (RA_KERNEL_*).  RA_KERNEL_TC
- * returns RA_ERR_UNSUPPORTED when the shape is outside its envelope. */
+ * returns RA_ERR_UNSUPPORTED when the shape is outside its envelope.
+ * Stream-K.  The tensor-core kernel runs one persistent CTA per SM and hands
+ * out work items (pairs of 128-row query tiles, each folding its whole ring)
+ * from a queue.  A non-causal problem with between one and two items per SM
+ * would leave many SMs idle in the queue's last wave, so RA_KERNEL_AUTO then
+ * gives every CTA an equal, contiguous range of the items' key tiles
+ * instead.  An item cut between two CTAs is folded as a head and a tail
+ * segment; the tail writes its partial (O/l and lse, fp32) and the head,
+ * which finishes later, combines it with its own by the log-sum-exp
+ * weighting of ra_merge -- the same two halves in the same order on every
+ * call, so the result does not depend on timing.  The scratch (2*128 rows of
+ * D + 1 floats per item) is taken on `stream` from a memory pool the library
+ * owns per device (created on first use; freed blocks stay reserved, up to
+ * 1 GiB, for reuse); under CUDA-graph stream capture it is a graph
+ * allocation.  RA_KERNEL_TC always uses the queue.  A head's wait for its
+ * tail is bounded; if it ran out (possible only if the GPU could not keep
+ * every CTA resident) ra_check reports RA_ERR_TIMEOUT. */
 int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                   int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
                   int dtype, int kernel, void* stream);

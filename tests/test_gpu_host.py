@@ -131,3 +131,28 @@ def test_pipelined_calls_on_two_streams_reuse_staging_safely(ra):
         ra.check()
         assert torch.equal(out_h, out0.view(torch.int16).cpu())
         assert torch.equal(lse_h, lse0.cpu())
+
+
+def test_forward_host_of_a_stream_k_problem_equals_device_forward(ra):
+    """A non-causal problem that ra_forward runs as stream-K (256 items) is
+    run whole by ra_forward_host rather than in chunks, so the bits match."""
+    import torch
+    B, Hq, Hkv, S, N, D = 2, 8, 8, 4096, 2, 64
+    q, k, v = inputs(8500, B, Hq, Hkv, S, D, "bf16")
+    tq, tk, tv = (to_device(x, "bf16") for x in (q, k, v))
+    out0, lse0 = ra.forward(tq, tk, tv, N, causal=False)
+    ra.check()
+    hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).pin_memory()
+                  for x in (q, k, v))
+    out_h = torch.zeros(hq.shape, dtype=torch.int16).pin_memory()
+    lse_h = torch.zeros((B, Hq, S), dtype=torch.float32).pin_memory()
+    stage = [torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv),
+             torch.empty_like(tq), torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")]
+    P = ra._ptr
+    side = torch.cuda.Stream()
+    rc = ra.ra_forward_host(P(hq), P(hk), P(hv), P(out_h), P(lse_h), *[P(x) for x in stage], B,
+                            Hq, Hkv, S, D, N, 0, 0, 0.0, ra.RA_BF16, ra._stream_handle(side))
+    assert rc == ra.RA_OK, ra.ra_strerror(rc)
+    assert ra.ra_check(ra._stream_handle(side)) == ra.RA_OK
+    assert torch.equal(out_h, out0.view(torch.int16).cpu())
+    assert torch.equal(lse_h, lse0.cpu())

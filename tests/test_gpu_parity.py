@@ -108,6 +108,33 @@ def test_tc_bf16_grid(ra, B, Hq, Hkv, S, N, D, causal, striped):
     assert_close(out, lse, ro, rl, "bf16", "tc")
 
 
+# Non-causal problems with between one and two work items per SM run as
+# stream-K (fixed contiguous work ranges per CTA; an item cut between two CTAs
+# is combined from the tail's partial); these shapes have 256 items.
+STREAMK_GRID = [
+    (2, 8, 8, 4096, 2, 64),      # MHA: query-tile pairs
+    (1, 8, 2, 8192, 4, 128),     # GQA: head pairs
+    (2, 8, 8, 3800, 2, 128),     # ragged (Sb = 1900), odd tile count: a pair with one tile
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,N,D", STREAMK_GRID)
+def test_streamk_matches_oracle(ra, B, Hq, Hkv, S, N, D):
+    import torch
+    q, k, v = inputs(401 + S + N + D, B, Hq, Hkv, S, D, "bf16")
+    tq, tk, tv = (to_device(x, "bf16") for x in (q, k, v))
+    out, lse = ra.forward(tq, tk, tv, N, causal=False)
+    out2, lse2 = ra.forward(tq, tk, tv, N, causal=False)
+    whole_o, whole_l = ra.forward(tq, tk, tv, N, causal=False, kernel="tc")
+    ra.check()
+    # the cut items' halves are combined in a fixed order: the same bits on every call
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse, lse2)
+    ro, rl = reference(q, k, v, N, False, False, "bf16")
+    assert_close(from_device(out), from_device(lse), ro, rl, "bf16", "stream-K")
+    assert not torch.equal(out.view(torch.int16), whole_o.view(torch.int16)), \
+        "expected this few-item problem to run as stream-K"
+
+
 def test_tc_custom_scale_and_no_lse(ra):
     import torch
     B, Hq, Hkv, S, N, D = 1, 2, 1, 512, 2, 128
