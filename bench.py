@@ -52,7 +52,7 @@ def parse():
                     help="run the workload as a real ring over the job's ranks (shard r on "
                          "rank r, K/V blocks passed between ranks); strong scaling")
     ap.add_argument("--cpu-configs", action="store_true",
-                    help="time the float64 oracle in full on configs 0-2 on all host cores, "
+                    help="time the float64 oracle in full on the four smallest workloads on all host cores, "
                          "comparing every row with the library's output; one JSON line each")
     ap.add_argument("--op", default="forward",
                     choices=["forward", "backward", "merge", "stripe", "f32", "ulysses"],
@@ -303,7 +303,7 @@ def reference_arm(args, wl):
 
 
 
-# ---------------------------------------------------------------- full oracle on configs 0-2
+# ---------------------------------------------------------------- full oracle on the small workloads
 CPU_CONFIGS = ("toy_f32", "noncausal_8k", "causal_32k_contig", "causal_32k_striped")
 
 
@@ -344,7 +344,7 @@ def _oracle_slice(task):
 
 
 def cpu_configs_arm(args):
-    """The float64 oracle in full (every query row) on configs 0-2, on all
+    """The float64 oracle in full (every query row) on the four smallest workloads, on all
     host cores (one spawned worker per core, each over whole (batch, head)
     slices), each compared row by row with the library's output for the same
     inputs.  Prints one JSON line per workload."""

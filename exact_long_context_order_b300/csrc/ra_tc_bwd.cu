@@ -716,7 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a_kv = base + (is_s ? kKOff : kVOff);
             const int full_in = is_s ? bQFull : bDOFull;      // B of the score GEMM
             const uint32_t off_in = is_s ? kQOff : kDOOff;
-            const uint32_t off_acc = is_s ? kDOOff : kQOff;   // B of the accumulation GEMM
+            const int full_acc = is_s ? bDOFull : bQFull;     // B of the accumulation GEMM
+            const uint32_t off_acc = is_s ? kDOOff : kQOff;
             const int sig_full = is_s ? bSFull : bDPFull;
             const int sig_ready = is_s ? bPFull : bDsFull;
             uint32_t g = 0;
@@ -758,6 +759,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (n == 0 && h == 0 && k > 0 &&
                             !(ok = wait_bar(bar(bAccEmpty), (k - 1) & 1, abort_flag, p.status,
                                             wlim)))
+                            break;
+                        // the accumulation GEMM's B stage (dO resp. Q) was loaded for
+                        // the other issuer's score GEMM: wait for it here too
+                        if (h == 0 && !(ok = wait_bar(bar(full_acc + (g & 1)), (g >> 1) & 1,
+                                                      abort_flag, p.status, wlim)))
                             break;
                         tc_fence_after();
                         mma_tn_k64<D>(acc_col, sc_col + 64 * h,
