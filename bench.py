@@ -869,12 +869,17 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         r = cpu_oracle_sample(wl, args.cpu_seconds)
         line["parity"] = parity_block(r, out, lse, wl)
+        cpu_rate = r["flops"] / r["seconds"]
         line["cpu_baseline"] = {
-            "value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["threads"],
+            "value": cpu_rate / 1e12, "unit": "TFLOP/s", "cores": r["threads"],
             "kind": "oracle",
             "sample": f"float64 NumPy oracle (plain softmax attention per row) on {r['rows']} "
                       f"stratified query rows of {wl.name}, each against all keys it sees; "
-                      f"FLOPs = 4*D*visible keys; {r['seconds']:.1f} s of CPU time"}
+                      f"FLOPs = 4*D*visible keys; {r['seconds']:.1f} s of CPU time",
+            "seconds_per_row": r["seconds"] / max(1, r["rows"]),
+            # labelled extrapolation: the whole step's metric FLOPs at the
+            # sample's rate (rows differ in cost; the sample is stratified)
+            "extrapolated_step_s": flops / cpu_rate}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
