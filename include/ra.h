@@ -169,9 +169,12 @@ int ra_forward_host(const void* q_host, const void* k_host, const void* v_host, 
  * D + 1 floats per item) is taken on `stream` from a memory pool the library
  * owns per device (created on first use; freed blocks stay reserved, up to
  * 1 GiB, for reuse); under CUDA-graph stream capture it is a graph
- * allocation.  RA_KERNEL_TC always uses the queue.  A head's wait for its
- * tail is bounded; if it ran out (possible only if the GPU could not keep
- * every CTA resident) ra_check reports RA_ERR_TIMEOUT. */
+ * allocation.  RA_KERNEL_TC always uses the queue.  A head waits only for
+ * its successor CTA's first segment, and CTAs start in index order, so the
+ * kernel completes even when it shares the GPU with other work; the wait is
+ * bounded (4e9 SM cycles, about 2 s) and could run out only if other kernels
+ * kept the successor off every SM for that long: ra_check then reports
+ * RA_ERR_TIMEOUT. */
 int ra_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                   int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped, float scale,
                   int dtype, int kernel, void* stream);
