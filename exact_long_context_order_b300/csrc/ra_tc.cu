@@ -923,9 +923,8 @@ static int launch_streamk(Params P, const CUtensorMap& mq, const CUtensorMap& mk
             cudaSuccess) {
         rc = RA_ERR_CUDA;
     } else {
-        // one CTA per SM; a head segment waits only for the next CTA's
-        // first segment and CTAs start in index order, so some waiting CTA's
-        // successor is always running: the waits end
+        // one CTA per SM, every CTA resident: a head segment's wait for the
+        // next CTA's tail always ends
         kern<<<(unsigned)sm_count, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, P);
         if (cudaGetLastError() != cudaSuccess) rc = RA_ERR_CUDA;
     }
