@@ -452,3 +452,49 @@ def plan_backward(S: int, N: int, causal: bool, striped, j: int, kt: int, tile: 
 def check(stream=None):
     """Synchronise and raise if a kernel recorded a device-side failure."""
     _check(ra_check(_stream_handle(stream)), "ra_check")
+
+
+def attention(q, k, v, N: int, causal: bool = False, striped=False, scale=None):
+    """Ring attention with autograd: ``forward`` in the forward pass and
+    ``backward`` (dq, dk, dv from the saved q, k, v, out and lse) in the
+    backward pass.  Tensors as for ``forward``; returns out (like q).  For
+    training, the way the method is used (1M-token training on the pages)."""
+    return _AttentionFn.apply(q, k, v, N, causal, striped, scale)
+
+
+def _autograd_function():
+    import torch
+
+    class AttentionFn(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, N, causal, striped, scale):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            out, lse = forward(q, k, v, N, causal=causal, striped=striped, scale=scale)
+            ctx.save_for_backward(q, k, v, out, lse)
+            ctx.cfg = (N, causal, striped, scale)
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, out, lse = ctx.saved_tensors
+            N, causal, striped, scale = ctx.cfg
+            dq, dk, dv = backward(q, k, v, out, lse, dout.contiguous(), N, causal=causal,
+                                  striped=striped, scale=scale)
+            return dq, dk, dv, None, None, None, None
+
+    return AttentionFn
+
+
+class _LazyFn:
+    """Builds the autograd Function on first use (importing the package does
+    not import torch)."""
+    fn = None
+
+    @classmethod
+    def apply(cls, *args):
+        if cls.fn is None:
+            cls.fn = _autograd_function()
+        return cls.fn.apply(*args)
+
+
+_AttentionFn = _LazyFn
