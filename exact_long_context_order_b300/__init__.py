@@ -37,6 +37,8 @@ _SIGNATURES = {
     "ra_merge": ([_vp, _vp, _vp, _vp, _i64, _i32, _i32, _vp], _i32),
     "ra_ring_step": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _i32, _i32,
                       _i32, _i32, _i32, _i32, _f32, _i32, _vp], _i32),
+    "ra_ring_step_backward": ([_vp] * 13 + [_i32, _i32, _i32, _i64, _i32, _i32, _i32, _i32,
+                                           _i32, _i32, _f32, _i32, _vp], _i32),
     "ra_stripe": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _vp], _i32),
     "ra_relayout": ([_vp, _vp, _i64, _i64, _i32, _i64, _i32, _i32, _vp], _i32),
     "ra_ulysses_exchange": ([_vp, _vp, _i32, _i32, _i64, _i32, _i64, _i32, _vp], _i32),
@@ -118,6 +120,13 @@ def ra_ring_step(q, k, v, state_o, state_lse, out, lse, B, Hq, Hkv, Sb, D, N, i,
                  layout, scale, flags, stream):
     return lib().ra_ring_step(q, k, v, state_o, state_lse, out, lse, B, Hq, Hkv, Sb, D, N, i, j,
                               causal, layout, scale, flags, stream)
+
+
+def ra_ring_step_backward(q, k, v, out, lse, dout, delta, dq_state, dk_state, dv_state, dq, dk,
+                          dv, B, Hq, Hkv, Sb, D, N, i, j, causal, layout, scale, flags, stream):
+    return lib().ra_ring_step_backward(q, k, v, out, lse, dout, delta, dq_state, dk_state,
+                                       dv_state, dq, dk, dv, B, Hq, Hkv, Sb, D, N, i, j, causal,
+                                       layout, scale, flags, stream)
 
 
 def ra_stripe(src, dst, BH, S, N, row_bytes, inverse, stream):
@@ -296,6 +305,45 @@ def ring_step(q, k, v, N: int, i: int, j: int, state_o=None, state_lse=None, out
                       float(scale or 0.0), flags, _stream_handle(stream))
     _check(rc, "ra_ring_step")
     return state_o, state_lse, out, lse
+
+
+def ring_step_backward(q, k, v, out, lse, dout, N: int, i: int, j: int, delta=None,
+                       dq_state=None, dk_state=None, dv_state=None, first: bool = False,
+                       last: bool = False, causal: bool = False, layout=0, scale=None,
+                       stream=None):
+    """One backward ring step over torch CUDA tensors (ra_ring_step_backward):
+    query shard i (q, out, dout [B, Hq, Sb, D] bf16, lse float32) against
+    block j (k, v [B, Hkv, Sb, D]).  delta (float32 [B, Hq, Sb]) is computed
+    on the first step and must be passed back on the later ones, as must the
+    shard's dq_state and the block's dk_state / dv_state (float32, allocated
+    when None).  Returns (delta, dq_state, dk_state, dv_state, dq, dk, dv);
+    dq, dk, dv (bf16) are set on the last step only."""
+    import torch
+    B, Hq, Sb, D = q.shape
+    Hkv = k.shape[1]
+    for t in (q, k, v, out, dout):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v, out and dout must be contiguous bf16")
+    if k.shape != (B, Hkv, Sb, D) or v.shape != k.shape or dout.shape != q.shape:
+        raise ValueError("k and v must be [B, Hkv, Sb, D], dout like q")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    if delta is None:
+        delta = torch.empty((B, Hq, Sb), **f32)
+    if not (first and last):
+        dq_state = torch.empty((B, Hq, Sb, D), **f32) if dq_state is None else dq_state
+        dk_state = torch.empty((B, Hkv, Sb, D), **f32) if dk_state is None else dk_state
+        dv_state = torch.empty((B, Hkv, Sb, D), **f32) if dv_state is None else dv_state
+    dq = dk = dv = None
+    if last:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flags = (RA_STEP_FIRST if first else 0) | (RA_STEP_LAST if last else 0)
+    rc = ra_ring_step_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                               _ptr(delta), _ptr(dq_state), _ptr(dk_state), _ptr(dv_state),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sb, D, N, i, j,
+                               int(causal), int(layout), float(scale or 0.0), flags,
+                               _stream_handle(stream))
+    _check(rc, "ra_ring_step_backward")
+    return delta, dq_state, dk_state, dv_state, dq, dk, dv
 
 
 def backward(q, k, v, out, lse, dout, N: int, causal: bool = False, striped: bool = False,

@@ -104,6 +104,34 @@ struct BwdProblem {
     int dtype;
 };
 
+// One backward step of a ring whose devices are separate processes: query
+// shard i (q, out, dout, lse, delta) against the block j it holds (k, v);
+// dq_state for the shard, dk_state / dv_state for the block (fp32
+// accumulators); on the last step the totals go to dq, dk, dv (bf16).
+struct BwdStepProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* out;
+    const float* lse;
+    const void* dout;
+    float* delta;
+    float* dq_state;
+    float* dk_state;
+    float* dv_state;
+    void* dq;
+    void* dk;
+    void* dv;
+    int B, Hq, Hkv;
+    int64_t Sb;
+    int D, N, i, j, causal, layout;
+    float scale;  // resolved (> 0)
+    int first, last;
+};
+bool tc_bwd_step_supported(const BwdStepProblem& p);
+int launch_bwd_tc_step(const BwdStepProblem& p, unsigned int* status, unsigned int* work,
+                       int sm_count, cudaStream_t stream);
+
 int launch_bwd_delta(const BwdProblem& p, cudaStream_t stream);
 int launch_bwd_simt(const BwdProblem& p, cudaStream_t stream);
 int launch_bwd_dkdv_simt(const BwdProblem& p, cudaStream_t stream);

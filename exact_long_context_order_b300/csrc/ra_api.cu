@@ -527,6 +527,48 @@ int ra_ring_step(const void* q, const void* k, const void* v, float* state_o, fl
     return rc;
 }
 
+int ra_ring_step_backward(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* dout, float* delta, float* dq_state,
+                          float* dk_state, float* dv_state, void* dq, void* dk, void* dv, int B,
+                          int Hq, int Hkv, int64_t Sb, int D, int N, int i, int j, int causal,
+                          int layout, float scale, int flags, void* stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sb < 0 || D <= 0 || N <= 0) return RA_ERR_INVALID_ARG;
+    if (Hq % Hkv || i < 0 || i >= N || j < 0 || j >= N) return RA_ERR_INVALID_ARG;
+    if (layout < RA_LAYOUT_CONTIGUOUS || layout > RA_LAYOUT_ZIGZAG) return RA_ERR_INVALID_ARG;
+    if (layout == RA_LAYOUT_ZIGZAG && Sb % 2) return RA_ERR_INVALID_ARG;
+    if (flags & ~(RA_STEP_FIRST | RA_STEP_LAST)) return RA_ERR_INVALID_ARG;
+    const bool first = flags & RA_STEP_FIRST, last = flags & RA_STEP_LAST;
+    if (empty_problem(B, Sb)) return RA_OK;
+    if (!q || !k || !v || !lse || !dout || !delta) return RA_ERR_INVALID_ARG;
+    if (first && !out) return RA_ERR_INVALID_ARG;  // delta comes from out and dout
+    // the state is read unless this is the first step, written unless the last
+    if (!(first && last) && (!dq_state || !dk_state || !dv_state)) return RA_ERR_INVALID_ARG;
+    if (last && (!dq || !dk || !dv)) return RA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, out, lse, dout, delta, dq_state, dk_state, dv_state, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return RA_ERR_ALIGN;
+    ra::BwdStepProblem p;
+    p.q = q; p.k = k; p.v = v; p.out = out; p.lse = lse; p.dout = dout; p.delta = delta;
+    p.dq_state = dq_state; p.dk_state = dk_state; p.dv_state = dv_state;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sb = Sb; p.D = D; p.N = N; p.i = i; p.j = j;
+    p.causal = causal ? 1 : 0;
+    p.layout = layout;
+    p.scale = (scale > 0.f && std::isfinite(scale)) ? scale : (float)(1.0 / std::sqrt((double)D));
+    p.first = first ? 1 : 0;
+    p.last = last ? 1 : 0;
+    if (!ra::tc_bwd_step_supported(p)) return RA_ERR_UNSUPPORTED;
+    unsigned int* status = nullptr;
+    int sms = 0;
+    int rc = device_state(&status, &sms);
+    if (rc) return rc;
+    unsigned int* work = nullptr;
+    if ((rc = work_slot(&work))) return rc;
+    rc = ra::launch_bwd_tc_step(p, status, work, sms, static_cast<cudaStream_t>(stream));
+    if (rc == RA_ERR_CUDA) note_cuda(cudaGetLastError());
+    return rc;
+}
+
 int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out, float* lse,
                          int B, int Hq, int Hkv, int64_t S, int D, int N, int causal, int striped,
                          float scale, int64_t timeout_cycles, void* stream) {

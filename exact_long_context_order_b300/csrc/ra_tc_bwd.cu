@@ -138,7 +138,47 @@ struct Params {
     unsigned int* status;
     unsigned int* work;
     long long timeout_cycles;  // self test only: limit of every bounded wait
+    // Ring step only (STEP kernels): the buffers hold query shard step_i (q,
+    // dout, lse, delta) and key/value block step_j alone, S = Sb rows per
+    // (b, h) slice, so the item geometry is a ring of one device; `ring` is
+    // the real ring whose masks apply.  The step adds its terms into fp32
+    // state: dq_state for the shard's rows, dk_state / dv_state for the
+    // block's (the accumulators that travel with the block).  step_first:
+    // the state starts at zero; step_last: the totals go to dq, dk, dv in
+    // bf16 instead of back to the state.
+    RingGeom ring;
+    int step_i, step_j, step_first, step_last;
+    float* dq_state;
+    float* dk_state;
+    float* dv_state;
 };
+
+// The walks of the ring-step kernels (one block of the real ring).
+// dq: key tiles [0, nk) of block step_j that query tile qt of shard step_i
+// sees.
+RA_HD void step_key_walk(const Params& p, int qt, TileWalk& w) {
+    int d;
+    w.s = 0;
+    w.j = p.step_j;
+    w.kt = 0;
+    shard_span(p.ring, p.step_i, p.step_j, qt, &w.nk, &d);
+}
+// dk/dv: the query tiles of shard step_i (every query head of the group)
+// that key tile kt of block step_j sees; w.i is 0 (the buffers' only shard)
+// while the walk runs and 1 once it is done.
+RA_HD void step_query_walk(const Params& p, int kt, KeyWalk& w) {
+    key_span(p.ring, p.step_i, p.step_j, kt, &w.q_lo, &w.q_hi);
+    w.s = 0;
+    w.gi = 0;
+    w.qt = w.q_lo;
+    w.i = (w.q_lo < w.q_hi) ? 0 : 1;
+}
+RA_HD void step_query_next(KeyWalk& w, int heads) {
+    if (++w.qt < w.q_hi) return;
+    w.qt = w.q_lo;
+    if (++w.gi < heads) return;
+    w.i = 1;
+}
 
 // ============================================================== dq kernel
 namespace dqk {
@@ -160,8 +200,9 @@ constexpr uint32_t kItemReaders = 10;  // two MMA issuers and eight softmax warp
 }  // namespace dqk
 
 // SELFTEST: the failure-detection self test (the first K tile is never
-// loaded, every wait is bounded by p.timeout_cycles).
-template <int D, bool SELFTEST>
+// loaded, every wait is bounded by p.timeout_cycles).  STEP: one step of a
+// ring whose devices are separate processes (see Params).
+template <int D, bool SELFTEST, bool STEP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -238,6 +279,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         it.valid1 = 0;
         return it;
     };
+    // the item's key tiles: its fold list, or in a ring step block step_j's
+    auto wstart = [&](TileWalk& w, const Item& it) {
+        if constexpr (STEP) step_key_walk(p, it.qt[0], w);
+        else w.start(G.rg, it);
+    };
+    auto wdone = [&](const TileWalk& w) -> bool {
+        if constexpr (STEP) return w.kt >= w.nk;
+        else return w.done(G.rg);
+    };
+    auto wnext = [&](TileWalk& w, const Item& it) {
+        if constexpr (STEP) ++w.kt;
+        else w.next(G.rg, it);
+    };
 
     if (warp < 4) regs_dec<kRegsOther>();
     if (warp == 0) {
@@ -279,8 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int64_t kvrow0 = (int64_t)(t.b * G.Hkv + t.kvh) * p.S;
                 TileWalk w;
-                for (w.start(G.rg, it); !w.done(G.rg) && ok; w.next(G.rg, it), ++tiles) {
-                    const int row = (int)(kvrow0 + (int64_t)w.j * p.Sb + (int64_t)w.kt * kT);
+                for (wstart(w, it); !wdone(w) && ok; wnext(w, it), ++tiles) {
+                    const int64_t jrow = STEP ? 0 : (int64_t)w.j * p.Sb;
+                    const int row = (int)(kvrow0 + jrow + (int64_t)w.kt * kT);
                     const uint32_t sk = tiles % kKStages, uk = tiles / kKStages;
                     if (uk > 0 && !(ok = wait_bar(bar(bKEmpty + sk), (uk - 1) & 1, abort_flag,
                                                   p.status, wlim)))
@@ -350,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 TileWalk w;
                 uint32_t n = 0;
-                for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++n) {
+                for (wstart(w, it); !wdone(w); wnext(w, it), ++n) {
                     if (is_a) {
                         const uint32_t sk = g % kKStages;
                         if (!(ok = wait_bar(bar(bKFull + sk), (g / kKStages) & 1, abort_flag,
@@ -378,8 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 umma_commit(bar(bQEmpty));  // this issuer's MMAs reading Q (A) or dO (B) are issued
                 if (is_a) {
-                    if (!(ok = issue_dq(n, k))) break;
-                    umma_commit(bar(bDqFull));
+                    if (STEP && n == 0) {
+                        // the block holds no key this tile sees: no dQ MMA; the
+                        // epilogue folds nothing into the state
+                        mbar_arrive(bar(bDqFull));
+                    } else {
+                        if (!(ok = issue_dq(n, k))) break;
+                        umma_commit(bar(bDqFull));
+                    }
                 }
             }
             if (!ok) {
@@ -416,8 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float dl = row_ok ? p.delta[row] : 0.f;
             const uint64_t nl2x2 = f2_pack(nl2, nl2), ndl2 = f2_pack(-dl, -dl);
             TileWalk w;
-            for (w.start(G.rg, it); !w.done(G.rg); w.next(G.rg, it), ++g) {
-                const int kind = fold_kind(G.rg, t.i, w.j, t.qt, w.kt);
+            uint32_t n = 0;
+            for (wstart(w, it); !wdone(w); wnext(w, it), ++g, ++n) {
+                const int kind = STEP ? fold_kind(p.ring, p.step_i, p.step_j, t.qt, w.kt)
+                                      : fold_kind(G.rg, t.i, w.j, t.qt, w.kt);
                 ok = wait_bar(bar(bSFull + (g & 1)), (g >> 1) & 1, abort_flag, p.status,
                               wlim) &&
                      wait_bar(bar(bDPFull), g & 1, abort_flag, p.status, wlim);
@@ -489,6 +552,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t sc2 = f2_pack(p.scale, p.scale);
             const int e0 = (D / 2) * wg;  // dq columns of this warpgroup
             uint4* drow = reinterpret_cast<uint4*>(p.dq + row * D + e0);
+            if constexpr (STEP) {
+                // dq_state (+)= scale * this block's dQ; the last step writes dq
+                float4* srow = reinterpret_cast<float4*>(p.dq_state + row * D + e0);
+#pragma unroll 1
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    uint32_t o[32];
+                    if (n > 0) {
+                        tmem_ld32(tmem + lane_off + kColDQ + e0 + cc * 32, o);
+                        tmem_wait_ld();
+                        reg_fence(o);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = 0u;
+                    }
+                    float nv[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) nv[e] = p.scale * __uint_as_float(o[e]);
+                    if (!row_ok) continue;
+                    if (!p.step_first) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 sv = srow[cc * 8 + e];
+                            nv[4 * e] += sv.x;
+                            nv[4 * e + 1] += sv.y;
+                            nv[4 * e + 2] += sv.z;
+                            nv[4 * e + 3] += sv.w;
+                        }
+                    }
+                    if (p.step_last) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            drow[cc * 4 + e] = make_uint4(
+                                pack_bf16x2(nv[8 * e], nv[8 * e + 1]),
+                                pack_bf16x2(nv[8 * e + 2], nv[8 * e + 3]),
+                                pack_bf16x2(nv[8 * e + 4], nv[8 * e + 5]),
+                                pack_bf16x2(nv[8 * e + 6], nv[8 * e + 7]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            srow[cc * 8 + e] = make_float4(nv[4 * e], nv[4 * e + 1],
+                                                           nv[4 * e + 2], nv[4 * e + 3]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bDqEmpty));
+                continue;
+            }
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 uint32_t o[32];
@@ -549,8 +660,9 @@ constexpr uint32_t kItemReaders = 11;
 }  // namespace dkv
 
 // SELFTEST: the failure-detection self test (the first Q tile is never
-// loaded, every wait is bounded by p.timeout_cycles).
-template <int D, bool SELFTEST>
+// loaded, every wait is bounded by p.timeout_cycles).  STEP: one step of a
+// ring whose devices are separate processes (see Params).
+template <int D, bool SELFTEST, bool STEP = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -626,6 +738,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         return (int64_t)(t.b * G.Hq + t.kvh * heads + w.gi) * p.S + (int64_t)w.i * p.Sb +
                (int64_t)w.qt * kT;
     };
+    // the key tile's query tiles: in the whole ring, or in a ring step shard
+    // step_i's
+    auto wstart = [&](KeyWalk& w, const KTile& t) {
+        if constexpr (STEP) step_query_walk(p, t.kt, w);
+        else w.start(G.rg, t.j, t.kt, heads);
+    };
+    auto wnext = [&](KeyWalk& w, const KTile& t) {
+        if constexpr (STEP) step_query_next(w, heads);
+        else w.next(G.rg, t.j, t.kt, heads);
+    };
 
     if (warp < 4) regs_dec<kRegsOther>();
     if (warp == 0) {
@@ -679,8 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pol_kv);
                 }
                 KeyWalk w;
-                for (w.start(G.rg, t.j, t.kt, heads); !w.done(G.rg);
-                     w.next(G.rg, t.j, t.kt, heads), ++g) {
+                for (wstart(w, t); !w.done(G.rg); wnext(w, t), ++g) {
                     const int row = (int)qrow0(t, w);
                     if (!(ok = load_ring(bQFull, bQEmpty, kQOff, &tm_q, row))) break;
                     q_issued = g + 1;
@@ -743,13 +864,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = wait_bar(bar(bKVFull), k & 1, abort_flag, p.status, wlim)))
                     break;
                 KeyWalk w;
-                w.start(G.rg, t.j, t.kt, heads);
+                wstart(w, t);
+                if (STEP && w.done(G.rg)) {
+                    // no query tile of the shard sees this key tile: no MMA; the
+                    // epilogue passes the state on unchanged
+                    mbar_arrive(bar(bKVEmpty));
+                    mbar_arrive(bar(bAccFull));
+                    continue;
+                }
                 if (!(ok = wait_in(g))) break;
                 issue_score(g, 0);
                 issue_score(g, 1);
                 for (uint32_t n = 0; !w.done(G.rg); ++n, ++g) {
                     KeyWalk nx = w;
-                    nx.next(G.rg, t.j, t.kt, heads);
+                    wnext(nx, t);
                     const bool more = !nx.done(G.rg);
                     for (int h = 0; h < 2 && ok; ++h) {
                         // P^T(n, h) resp. dS^T(n, h) written by half h's warpgroup
@@ -806,8 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (item >= G.n_items) break;
             const KTile t = decode_ktile(G, item);
             KeyWalk w;
-            for (w.start(G.rg, t.j, t.kt, heads); !w.done(G.rg);
-                 w.next(G.rg, t.j, t.kt, heads), ++g) {
+            for (wstart(w, t); !w.done(G.rg); wnext(w, t), ++g) {
                 const uint32_t st = g & 1, use = g >> 1;
                 ok = use == 0 || wait_bar(bar(bVecEmpty + st), (use - 1) & 1, abort_flag, p.status,
                                           wlim);
@@ -845,9 +972,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const KTile t = decode_ktile(G, item);
             const bool key_ok = t.kt < nt - 1 || c < p.rem;
             KeyWalk w;
-            for (w.start(G.rg, t.j, t.kt, heads); !w.done(G.rg);
-                 w.next(G.rg, t.j, t.kt, heads), ++g) {
-                const int kind = fold_kind(G.rg, w.i, t.j, w.qt, t.kt);
+            uint32_t n_tiles = 0;
+            for (wstart(w, t); !w.done(G.rg); wnext(w, t), ++g, ++n_tiles) {
+                const int kind = STEP ? fold_kind(p.ring, p.step_i, p.step_j, w.qt, t.kt)
+                                      : fold_kind(G.rg, w.i, t.j, w.qt, t.kt);
                 // pair (query column q, key row c) visible iff lo <= q < hi
                 int lo = (kind == kIncl) ? c : (kind == kStrict) ? c + 1 : 0;
                 const int hi = (w.qt == nt - 1) ? p.rem : kT;
@@ -959,6 +1087,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t krow = (int64_t)(t.b * G.Hkv + t.kvh) * p.S + (int64_t)t.j * p.Sb +
                                  (int64_t)t.kt * kT + c;
             const uint64_t sc2 = f2_pack(p.scale, p.scale), one2 = f2_pack(1.f, 1.f);
+            if constexpr (STEP) {
+                // the block's accumulators (+)= this step's dV and scale * dK; the
+                // last step writes dk, dv
+#pragma unroll 1
+                for (int which = 0; which < 2; ++which) {
+                    const uint32_t col = which ? kColDK : kColDV;
+                    const float mul = which ? p.scale : 1.f;
+                    const int e0 = (D / 2) * wg;
+                    float4* srow = reinterpret_cast<float4*>((which ? p.dk_state : p.dv_state) +
+                                                             krow * D + e0);
+                    uint4* drow = reinterpret_cast<uint4*>((which ? p.dk : p.dv) + krow * D + e0);
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 64; ++cc) {
+                        uint32_t o[32];
+                        if (n_tiles > 0) {
+                            tmem_ld32(tmem + lane_off + col + e0 + cc * 32, o);
+                            tmem_wait_ld();
+                            reg_fence(o);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = 0u;
+                        }
+                        if (!key_ok) continue;
+                        float nv[32];
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) nv[e] = mul * __uint_as_float(o[e]);
+                        if (!p.step_first) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float4 sv = srow[cc * 8 + e];
+                                nv[4 * e] += sv.x;
+                                nv[4 * e + 1] += sv.y;
+                                nv[4 * e + 2] += sv.z;
+                                nv[4 * e + 3] += sv.w;
+                            }
+                        }
+                        if (p.step_last) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                drow[cc * 4 + e] = make_uint4(
+                                    pack_bf16x2(nv[8 * e], nv[8 * e + 1]),
+                                    pack_bf16x2(nv[8 * e + 2], nv[8 * e + 3]),
+                                    pack_bf16x2(nv[8 * e + 4], nv[8 * e + 5]),
+                                    pack_bf16x2(nv[8 * e + 6], nv[8 * e + 7]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                srow[cc * 8 + e] = make_float4(nv[4 * e], nv[4 * e + 1],
+                                                               nv[4 * e + 2], nv[4 * e + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bAccEmpty));
+                continue;
+            }
 #pragma unroll
             for (int which = 0; which < 2; ++which) {  // dV, then dK (times scale)
                 const uint32_t col = which ? kColDK : kColDV;
@@ -1045,7 +1230,95 @@ static int launch_one(const BwdProblem& pr, int which, unsigned int* status, uns
     return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
+// One ring step (see Params): the dq kernel over the shard's query tiles,
+// then the dk/dv kernel over the block's key tiles, both STEP variants.
+static int launch_step(const BwdStepProblem& pr, int which, unsigned int* status,
+                       unsigned int* work, int sm_count, cudaStream_t stream) {
+    CUtensorMap mq, mdo, mk, mv;
+    const int64_t q_rows = (int64_t)pr.B * pr.Hq * pr.Sb, kv_rows = (int64_t)pr.B * pr.Hkv * pr.Sb;
+    if (!encode_rows_bf16(&mq, pr.q, q_rows, pr.D) ||
+        !encode_rows_bf16(&mdo, pr.dout, q_rows, pr.D) ||
+        !encode_rows_bf16(&mk, pr.k, kv_rows, pr.D) || !encode_rows_bf16(&mv, pr.v, kv_rows, pr.D))
+        return RA_ERR_CUDA;
+    Params P = {};
+    const int Sb = (int)pr.Sb;
+    const int nt = (Sb + kT - 1) / kT;
+    // items: the buffers' one shard (query tiles, resp. key tiles of the block)
+    P.G = make_tile_geom(pr.B, pr.Hq, pr.Hkv, 1, nt, pr.causal, pr.layout, which == 1);
+    P.S = Sb;
+    P.Sb = Sb;
+    P.rem = Sb - (nt - 1) * kT;
+    P.sl2 = (float)((double)pr.scale * 1.4426950408889634);
+    P.scale = pr.scale;
+    P.lse = pr.lse;
+    P.delta = pr.delta;
+    P.dq = static_cast<__nv_bfloat16*>(pr.dq);
+    P.dk = static_cast<__nv_bfloat16*>(pr.dk);
+    P.dv = static_cast<__nv_bfloat16*>(pr.dv);
+    P.status = status;
+    P.work = work;
+    P.timeout_cycles = kTimeoutCycles;
+    P.ring.N = pr.N;
+    P.ring.nt = nt;
+    P.ring.causal = pr.causal;
+    P.ring.striped = pr.layout;
+    P.step_i = pr.i;
+    P.step_j = pr.j;
+    P.step_first = pr.first;
+    P.step_last = pr.last;
+    P.dq_state = pr.dq_state;
+    P.dk_state = pr.dk_state;
+    P.dv_state = pr.dv_state;
+    if (P.G.n_items <= 0) return RA_OK;
+    if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
+    auto kern = pr.D == 64 ? (which ? dkv_kernel<64, false, true> : dq_kernel<64, false, true>)
+                           : (which ? dkv_kernel<128, false, true> : dq_kernel<128, false, true>);
+    const int smem = which ? dkv::kSmemBytes : dqk::kSmemBytes;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return RA_ERR_CUDA;
+    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
+    kern<<<(unsigned)grid, kThreads, smem, stream>>>(mq, mdo, mk, mv, P);
+    return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
 }  // namespace tcb
+
+bool tc_bwd_step_supported(const BwdStepProblem& p) {
+    if (p.D != 64 && p.D != 128) return false;
+    if (p.Sb <= 0 || p.Sb > (1ll << 30)) return false;
+    if (p.layout == kZigzag && p.Sb % (2 * tcb::kT)) return false;
+    if ((int64_t)p.B * p.Hq * p.Sb >= (1ll << 31) || (int64_t)p.B * p.Hkv * p.Sb >= (1ll << 31))
+        return false;
+    return true;
+}
+
+int launch_bwd_tc_step(const BwdStepProblem& p, unsigned int* status, unsigned int* work,
+                       int sm_count, cudaStream_t stream) {
+    if (!tc_bwd_step_supported(p)) return RA_ERR_UNSUPPORTED;
+    if (!work) return RA_ERR_INVALID_ARG;
+    if (p.first) {
+        // delta = rowsum(dout * out) of the shard, kept by the caller for the
+        // later steps
+        BwdProblem d = {};
+        d.out = p.out;
+        d.dout = p.dout;
+        d.delta = p.delta;
+        d.B = p.B;
+        d.Hq = p.Hq;
+        d.Hkv = p.Hkv;
+        d.S = p.Sb;
+        d.D = p.D;
+        d.N = 1;
+        d.dtype = RA_BF16;
+        int rc = launch_bwd_delta(d, stream);
+        if (rc) return rc;
+    }
+    // both kernels take items from the same counter, zeroed before each launch
+    int rc = tcb::launch_step(p, 0, status, work, sm_count, stream);
+    if (rc) return rc;
+    return tcb::launch_step(p, 1, status, work, sm_count, stream);
+}
 
 bool tc_bwd_supported(const BwdProblem& p) {
     if (p.dtype != RA_BF16 || (p.D != 64 && p.D != 128)) return false;

@@ -1,5 +1,7 @@
 """Ring attention across processes: one query shard per process, K/V blocks
-passed round the ring, one ``ra_ring_step`` kernel call per ring step.
+passed round the ring, one ``ra_ring_step`` kernel call per ring step; and
+its backward, one ``ra_ring_step_backward`` call per step, with each block's
+gradient accumulators travelling with the block.
 
 The method as the pages describe it for several devices ("Ring Attention"
 glossary page, "Como funciona a atencao em anel"; aiunderstanding.org,
@@ -141,3 +143,117 @@ def _ring_loop(q, k, v, group, N, r, step, causal, layout, scale, out, lse, trac
             ex.finish(handle)
             cur, spare = spare, cur
     return out, lse
+
+
+def _library_step_backward(q, k, v, out, lse, dout, N, i, j, delta, dq_state, dk_state, dv_state,
+                           first, last, causal, layout, scale, stream):
+    from . import ring_step_backward
+    return ring_step_backward(q, k, v, out, lse, dout, N, i, j, delta=delta, dq_state=dq_state,
+                              dk_state=dk_state, dv_state=dv_state, first=first, last=last,
+                              causal=causal, layout=layout, scale=scale, stream=stream)
+
+
+def ring_attention_backward(q, k, v, out, lse, dout, group=None, causal: bool = False,
+                            layout=0, scale=None, step_fn: Optional[Callable] = None,
+                            stream=None, trace: Optional[list] = None):
+    """Gradients (dq, dk, dv) of ``ring_attention`` for this rank's shard.
+
+    q, out, dout [B, Hq, Sb, D], lse [B, Hq, Sb] (the forward's), k, v
+    [B, Hkv, Sb, D]: rank r's shard of the layout.  The ring is the
+    forward's: at step s rank r holds block j = (r - s) mod N together with
+    that block's fp32 accumulators dK_j, dV_j; it adds block j's terms into
+    its own dQ_r and its shard's terms into dK_j, dV_j (``ra_ring_step_backward``),
+    then passes the block and the accumulators to rank r + 1.  K and V move
+    while the step computes; the accumulators move after it (the step
+    updates them).  After the last step the block's finished dk, dv (bf16)
+    take one more hop, to the rank that owns that block.
+
+    ``step_fn(q, k, v, out, lse, dout, N, i, j, delta, dq_state, dk_state,
+    dv_state, first, last, causal, layout, scale, stream)`` returns (delta,
+    dq_state, dk_state, dv_state, dq, dk, dv); by default the library's kernel.
+    ``trace``, when given, receives (s, j) for every step.
+    """
+    import contextlib
+
+    import torch
+    import torch.distributed as dist
+    N = dist.get_world_size(group)
+    r = dist.get_rank(group)
+    step = step_fn or _library_step_backward
+    ctx = torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext()
+    with ctx:
+        return _ring_backward_loop(q, k, v, out, lse, dout, group, N, r, step, causal, layout,
+                                   scale, trace)
+
+
+def _ring_backward_loop(q, k, v, out, lse, dout, group, N, r, step, causal, layout, scale, trace):
+    import torch
+    f32 = torch.float32 if k.dtype != torch.float64 else torch.float64
+    kv = [k, v]
+    acc = [torch.empty(k.shape, dtype=f32, device=k.device),
+           torch.empty(v.shape, dtype=f32, device=v.device)]
+    spare_kv = [torch.empty_like(k), torch.empty_like(v)] if N > 1 else None
+    spare_acc = [torch.empty_like(acc[0]), torch.empty_like(acc[1])] if N > 1 else None
+    ex_kv = _Exchange(group, kv) if N > 1 else None
+    ex_acc = _Exchange(group, acc) if N > 1 else None
+    delta = dq_state = None
+    dq = dk = dv = None
+    for s in range(N):
+        j = (r - s) % N
+        first, last = s == 0, s == N - 1
+        handle = ex_kv.start(kv, spare_kv) if not last else None
+        delta, dq_state, dk_st, dv_st, dq, dk, dv = step(
+            q, kv[0], kv[1], out, lse, dout, N, r, j, delta, dq_state, acc[0], acc[1], first,
+            last, causal, layout, scale, None)
+        if trace is not None:
+            trace.append((s, j))
+        if not last:
+            acc = [dk_st, dv_st]
+            h_acc = ex_acc.start(acc, spare_acc)
+            ex_kv.finish(handle)
+            ex_acc.finish(h_acc)
+            kv, spare_kv = spare_kv, kv
+            acc, spare_acc = spare_acc, acc
+    if N > 1:
+        # the finished gradients of block r + 1 go home; block r's come in
+        ex_out = _Exchange(group, [dk, dv])
+        home = [torch.empty_like(dk), torch.empty_like(dv)]
+        ex_out.finish(ex_out.start([dk, dv], home))
+        dk, dv = home
+    return dq, dk, dv
+
+
+def _autograd_function():
+    import torch
+
+    class RingAttentionFn(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, q, k, v, group, causal, layout, scale):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            out, lse = ring_attention(q, k, v, group=group, causal=causal, layout=layout,
+                                      scale=scale)
+            ctx.save_for_backward(q, k, v, out, lse)
+            ctx.cfg = (group, causal, layout, scale)
+            return out
+
+        @staticmethod
+        def backward(ctx, dout):
+            q, k, v, out, lse = ctx.saved_tensors
+            group, causal, layout, scale = ctx.cfg
+            dq, dk, dv = ring_attention_backward(q, k, v, out, lse, dout.contiguous(),
+                                                 group=group, causal=causal, layout=layout,
+                                                 scale=scale)
+            return dq, dk, dv, None, None, None, None
+
+    return RingAttentionFn
+
+
+_FN = []
+
+
+def ring_attention_fn(q, k, v, group=None, causal: bool = False, layout=0, scale=None):
+    """``ring_attention`` with autograd: its backward is ``ring_attention_backward``
+    over the same group (every rank must run both, in the same order)."""
+    if not _FN:
+        _FN.append(_autograd_function())
+    return _FN[0].apply(q, k, v, group, causal, layout, scale)

@@ -223,6 +223,48 @@ int ra_ring_step(const void* q, const void* k, const void* v, float* state_o, fl
                  int j, int causal, int layout, float scale, int flags, void* stream);
 
 /*
+ * ra_ring_step_backward: one step of the backward of a ring whose devices are
+ * separate processes (or GPUs), the counterpart of ra_ring_step for
+ * training.  Device i keeps its query shard and, at ring step s, holds block
+ * j = (i - s) mod N together with that block's gradient accumulators, which
+ * travel with it (the glossary page's ring, "Como funciona a atencao em
+ * anel"; the backward is the chain rule of ra_backward's definition, folded
+ * block by block): this call adds block j's terms into the shard's dq and
+ * the shard's terms into the block's dk and dv.
+ *   q, out, dout [B, Hq, Sb, D] bf16 (read): shard i's queries, the
+ *       forward's output and dL/dout for them.  out is read on the first step
+ *       only.
+ *   lse [B, Hq, Sb] float32 (read): the forward's lse for the shard.
+ *   delta [B, Hq, Sb] float32 (caller-owned): written on the first step
+ *       (rowsum(dout * out)), read by every step.
+ *   k, v [B, Hkv, Sb, D] bf16 (read): block j.
+ *   dq_state [B, Hq, Sb, D] float32: the shard's running dq (scaled);
+ *   dk_state, dv_state [B, Hkv, Sb, D] float32: block j's running dk
+ *       (scaled) and dv, which the caller passes on with the block.  Read
+ *       unless flags has RA_STEP_FIRST (then they start at zero), written
+ *       unless flags has RA_STEP_LAST; may be NULL when both flags are set.
+ *   dq, dk, dv (bf16, written on the last step only, may be NULL otherwise):
+ *       the totals of the shard's dq and of block j's dk and dv; the block's
+ *       then travel one more hop, to the device that holds block j.
+ *   i, j, N, causal, layout, scale: as ra_ring_step.  Every device calls
+ *       with RA_STEP_FIRST at s = 0 and RA_STEP_LAST at s = N - 1.
+ * Masks, tiles and kernels are those of ra_backward's tensor-core kernels
+ * (bf16, D in {64, 128}; Sb % 256 == 0 for zigzag), compiled for one block:
+ * the dq kernel over the shard's query tiles, the dk/dv kernel over the
+ * block's key tiles.  A tile pair no query of the shard sees leaves the
+ * state as it was.  Asynchronous on `stream`; no atomics (the same bits on
+ * every call).
+ * Errors: RA_ERR_INVALID_ARG (shapes, i or j out of range, flags, a NULL
+ * pointer the flags need), RA_ERR_ALIGN, RA_ERR_UNSUPPORTED, RA_ERR_CUDA.  An
+ * empty problem (B == 0 or Sb == 0) is a no-op.
+ */
+int ra_ring_step_backward(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* dout, float* delta, float* dq_state,
+                          float* dk_state, float* dv_state, void* dq, void* dk, void* dv, int B,
+                          int Hq, int Hkv, int64_t Sb, int D, int N, int i, int j, int causal,
+                          int layout, float scale, int flags, void* stream);
+
+/*
  * ra_merge: fold partial result b into partial result a, in place.
  *   out_a [rows, D] (read, written)   lse_a [rows] float32 (read, written)
  *   out_b [rows, D] (read)            lse_b [rows] float32 (read)

@@ -50,4 +50,5 @@ from .attention import (  # noqa: F401
     attention_backward_key_rows,
     backward_uniform_scores,
     ring_attention_backward,
+    ring_step_backward_block,
 )

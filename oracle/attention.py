@@ -456,6 +456,48 @@ def ring_attention_backward(q, k, v, dout, N: int, causal: bool, striped, scale=
     return dq, dk, dv
 
 
+def ring_step_backward_block(q_i, k_j, v_j, dout_i, lse_i, delta_i, N: int, i: int, j: int,
+                             causal: bool, striped, scale=None):
+    """One step of ``ring_attention_backward`` as a device computes it,
+    float64: device i's query shard (q_i, dout_i [B, Hq, Sb, D], its forward
+    lse_i and delta_i = dO_t . O_t [B, Hq, Sb]) against the block j it holds
+    (k_j, v_j [B, Hkv, Sb, D]).  Returns (dq_i, dk_j, dv_j): the terms this
+    step adds to the shard's dq and to the block's travelling dk and dv, by
+    the same formulas (P = exp(scale q.k - lse) on the visible pairs, dS =
+    P (dO.v - delta)).  Summed over the ring's steps they give the whole
+    backward.
+    """
+    q_i = np.asarray(q_i, np.float64)
+    k_j = np.asarray(k_j, np.float64)
+    v_j = np.asarray(v_j, np.float64)
+    dout_i = np.asarray(dout_i, np.float64)
+    lse_i = np.asarray(lse_i, np.float64)
+    delta_i = np.asarray(delta_i, np.float64)
+    B, Hq, Sb, D = q_i.shape
+    Hkv = k_j.shape[1]
+    g = Hq // Hkv
+    sc = _scale(D, scale)
+    pos = positions(N * Sb, N, striped)
+    qpos, kpos = pos[i * Sb:(i + 1) * Sb], pos[j * Sb:(j + 1) * Sb]
+    vis = (kpos[None, :] <= qpos[:, None]) if causal else np.ones((Sb, Sb), dtype=bool)
+    dq = np.zeros_like(q_i)
+    dk = np.zeros_like(k_j)
+    dv = np.zeros_like(v_j)
+    if not vis.any():
+        return dq, dk, dv
+    for b in range(B):
+        for h in range(Hq):
+            Q, dO = q_i[b, h], dout_i[b, h]
+            K, V = k_j[b, h // g], v_j[b, h // g]
+            with np.errstate(invalid="ignore", over="ignore"):
+                P = np.where(vis, np.exp((Q @ K.T) * sc - lse_i[b, h][:, None]), 0.0)
+            dv[b, h // g] += P.T @ dO
+            dS = P * (dO @ V.T - delta_i[b, h][:, None])
+            dq[b, h] = sc * (dS @ K)
+            dk[b, h // g] += sc * (dS.T @ Q)
+    return dq, dk, dv
+
+
 # ------------------------------------------------------------- schedule
 def fold_schedule(S: int, N: int, causal: bool, striped: bool, Tq: int, Tk: int,
                   i_list=None, qt_list=None):

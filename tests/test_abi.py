@@ -288,3 +288,34 @@ def test_ring_step_host_validation(lib):
     assert call(layout=2, Sb=384) == ra.RA_ERR_UNSUPPORTED  # zigzag chunks must be whole tiles
     assert call(B=0) == ra.RA_OK                         # empty: nothing to do
     assert call(Sb=0, q=None) == ra.RA_OK
+
+
+def test_ring_step_backward_host_validation(lib):
+    """ra_ring_step_backward refuses bad arguments on the host, before any
+    CUDA call."""
+    p = ctypes.c_void_p(16 * 1024)  # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(16 * 1024 + 8)
+
+    def call(q=p, out=p, lse=p, dout=p, delta=p, dqs=p, dks=p, dvs=p, dq=p, dk=p, dv=p, B=1,
+             Hq=2, Hkv=1, Sb=256, D=128, N=4, i=1, j=0, layout=1, flags=0):
+        return ra.ra_ring_step_backward(q, p, p, out, lse, dout, delta, dqs, dks, dvs, dq, dk,
+                                        dv, B, Hq, Hkv, Sb, D, N, i, j, 1, layout, 0.0, flags,
+                                        None)
+
+    F, L = ra.RA_STEP_FIRST, ra.RA_STEP_LAST
+    assert call(i=4) == ra.RA_ERR_INVALID_ARG            # shard outside the ring
+    assert call(j=-1) == ra.RA_ERR_INVALID_ARG
+    assert call(Hq=3, Hkv=2) == ra.RA_ERR_INVALID_ARG    # Hq % Hkv
+    assert call(flags=4) == ra.RA_ERR_INVALID_ARG        # unknown flag
+    assert call(layout=3) == ra.RA_ERR_INVALID_ARG
+    assert call(delta=None) == ra.RA_ERR_INVALID_ARG     # delta is always needed
+    assert call(out=None, flags=F) == ra.RA_ERR_INVALID_ARG  # the first step forms delta
+    assert call(dks=None) == ra.RA_ERR_INVALID_ARG       # the block's state is read and written
+    assert call(dq=None, flags=L) == ra.RA_ERR_INVALID_ARG
+    assert call(dqs=odd) == ra.RA_ERR_ALIGN
+    assert call(D=96) == ra.RA_ERR_UNSUPPORTED           # tensor-core head dimensions only
+    assert call(layout=2, Sb=384) == ra.RA_ERR_UNSUPPORTED
+    assert call(B=0) == ra.RA_OK                         # empty: nothing to do
+    # out, the states and the outputs may be NULL where the flags do not use them
+    assert call(out=None, dq=None, dk=None, dv=None, D=96) == ra.RA_ERR_UNSUPPORTED
+    assert call(dqs=None, dks=None, dvs=None, flags=F | L, D=96) == ra.RA_ERR_UNSUPPORTED

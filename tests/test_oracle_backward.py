@@ -126,6 +126,43 @@ def test_ring_backward_equals_plain(N, causal, layout):
         np.testing.assert_allclose(oracle.to_token_order(g, N, layout), r, rtol=0, atol=1e-11)
 
 
+@pytest.mark.parametrize("N", [1, 3, 4])
+@pytest.mark.parametrize("causal,layout", [(False, 0), (True, 0), (True, 1), (True, 2)])
+def test_ring_steps_sum_to_the_plain_gradients(N, causal, layout):
+    """The one-step function a device applies (ring_step_backward_block), run
+    for every device i and step s with block j = (i - s) mod N, each device
+    seeing only its own shard and the block it holds, adds up to the plain
+    gradients (pinned above by finite differences and autograd)."""
+    if layout == 2 and N == 3:
+        N = 2  # zigzag needs an even number of chunks per shard below
+    B, Hq, Hkv, S, D = 2, 4, 2, 48, 8
+    q, k, v = rnd((B, Hq, S, D), 65), rnd((B, Hkv, S, D), 66), rnd((B, Hkv, S, D), 67)
+    dout = rnd((B, Hq, S, D), 68)
+    ref = oracle.attention_backward(q, k, v, dout, causal, chunk=20)
+    o, lse = oracle.full_attention(q, k, v, causal)
+    delta = (dout * o).sum(axis=-1)
+    sm = [oracle.to_shard_major(x, N, layout) for x in (q, k, v, dout)]
+    lse_sm = oracle.to_shard_major(lse[..., None], N, layout)[..., 0]
+    delta_sm = oracle.to_shard_major(delta[..., None], N, layout)[..., 0]
+    Sb = S // N
+    sh = lambda x, i: x[:, :, i * Sb:(i + 1) * Sb]
+    dq = np.zeros_like(sm[0])
+    dk = np.zeros_like(sm[1])
+    dv = np.zeros_like(sm[2])
+    for s in range(N):
+        for i in range(N):
+            j = (i - s) % N
+            a, b, c = oracle.ring_step_backward_block(
+                sh(sm[0], i), sh(sm[1], j), sh(sm[2], j), sh(sm[3], i), sh(lse_sm, i),
+                sh(delta_sm, i), N, i, j, causal, layout)
+            dq[:, :, i * Sb:(i + 1) * Sb] += a
+            dk[:, :, j * Sb:(j + 1) * Sb] += b
+            dv[:, :, j * Sb:(j + 1) * Sb] += c
+    for got, want in zip((dq, dk, dv), ref):
+        np.testing.assert_allclose(oracle.to_token_order(got, N, layout), want, rtol=0,
+                                   atol=1e-11)
+
+
 def test_ring_backward_scale_argument():
     """Scaling q by r and the scale by 1/r leaves every score unchanged; by
     the chain rule dQ then scales by 1/r while dK and dV are unchanged."""
