@@ -607,13 +607,17 @@ def ring_arm(args, wl):
     holds shard r of N = world size (the workload's layout), and each step is
     ring_attention -- N calls of ra_ring_step, with each K/V block passed to
     the next rank (NCCL send/recv between GPUs) while the current one is
-    folded.  The total problem is fixed as ranks are added (strong scaling);
-    value = the workload's FLOPs / the slowest rank's time."""
+    folded.  With --op backward a step is a training step: the forward ring,
+    then ring_attention_backward (N calls of ra_ring_step_backward, each
+    block's dk/dv accumulators passed on with it), FLOPs 3.5 times the
+    forward's (the forward plus the backward's usual 2.5).  The total problem
+    is fixed as ranks are added (strong scaling); value = the step's FLOPs /
+    the slowest rank's time."""
     import torch
     import torch.distributed as dist
     import exact_long_context_order_b300 as ra
     import ragen
-    from exact_long_context_order_b300.ring import ring_attention
+    from exact_long_context_order_b300.ring import ring_attention, ring_attention_backward
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
     if not dist.is_initialized():
@@ -641,8 +645,14 @@ def ring_arm(args, wl):
     lse = torch.empty((wl.B, wl.Hq, Sb), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    train = args.op == "backward"
+    dout = shard(ragen.TENSOR_DO, wl.Hq) if train else None
+
     def step():
         ring_attention(q, k, v, causal=wl.causal, layout=int(wl.striped), out=out, lse=lse)
+        if train:
+            ring_attention_backward(q, k, v, out, lse, dout, causal=wl.causal,
+                                    layout=int(wl.striped))
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -664,23 +674,30 @@ def ring_arm(args, wl):
     if rc != ra.RA_OK:
         raise SystemExit(f"device status after timed region: {ra.ra_strerror(rc)}")
     t_max = max_over_ranks(a.elapsed_time(b), device="cuda")
-    value = wl.flops() * args.steps / (t_max * 1e-3) / 1e12
+    step_flops = (3.5 if train else 1.0) * wl.flops()
+    value = step_flops * args.steps / (t_max * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "metric": ("attention training step TFLOP/s (bf16, forward + backward, 3.5x the "
+                       "forward's FLOPs)") if train else METRIC,
+            "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps,
             "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": dict(wl.describe(), parallelism=f"ring{world}", ring_devices=world,
                            tokens_per_rank=Sb, l2="inputs larger than L2 (no flush)",
-                           flops_per_step=wl.flops()),
+                           flops_per_step=step_flops, op="backward" if train else "forward"),
             "tokens_per_s": wl.B * wl.S * args.steps / (t_max * 1e-3),
             "frac_of_bf16_peak": value / world / float(peaks["bf16_tflops"]),
-            "gpu_launches": args.steps * world,
+            # per rank and ring step: the forward kernel; in training also the
+            # delta kernel (first step), the dq and the dk/dv kernels
+            "gpu_launches": args.steps * world * (world * 3 + 1 if train else world),
             "clocks": clk, "e2e": None,
             "how": "ring_attention per step: N ra_ring_step calls per rank, K/V blocks sent to "
-                   "the next rank while the current block is folded",
+                   "the next rank while the current block is folded" +
+                   ("; then ring_attention_backward: N ra_ring_step_backward calls per rank, "
+                    "each block's fp32 dk/dv accumulators sent on with it" if train else ""),
         }
         print(json.dumps(line), flush=True)
     dist.destroy_process_group()
