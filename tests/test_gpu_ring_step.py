@@ -181,7 +181,7 @@ def test_two_process_ring_on_one_gpu(cuda_ok, case):
                      rl[:, :, rank * Sb:(rank + 1) * Sb], "bf16", f"rank {rank}")
 
 
-def virtual_ring_backward(ra, tq, tk, tv, tout, tlse, tg, N, causal, layout):
+def virtual_ring_backward(ra, tq, tk, tv, tout, tlse, tg, N, causal, layout, scale=None):
     """The backward ring emulated in one process: at step s device i holds
     block j = (i - s) mod N and that block's accumulators, which the step
     updates and the next device receives.  Returns shard-major dq, dk, dv."""
@@ -200,7 +200,8 @@ def virtual_ring_backward(ra, tq, tk, tv, tout, tlse, tg, N, causal, layout):
                                         tlse[:, :, i * Sb:(i + 1) * Sb].contiguous(), sh(tg, i),
                                         N, i, j, delta=delta[i], dq_state=dq_st[i],
                                         dk_state=dk_st[j], dv_state=dv_st[j], first=s == 0,
-                                        last=s == N - 1, causal=causal, layout=layout)
+                                        last=s == N - 1, causal=causal, layout=layout,
+                                        scale=scale)
             delta[i], dq_st[i], dk_st[j], dv_st[j] = res[:4]
             if s == N - 1:
                 dq[i], dk[j], dv[j] = res[4:]
@@ -228,6 +229,20 @@ def test_virtual_ring_backward_equals_the_gradients(ra, B, Hq, Hkv, S, N, D, cau
     for name, g, r, e in zip(("dq", "dk", "dv"), got, ref, (bq, bk, None)):
         fro, worst = assert_grad_close(from_device(g), r, "bf16", f"ring backward {name}", e)
         print(f"ring backward {S} {N} {layout} {name}: normwise {fro:.2e}")
+
+
+def test_virtual_ring_backward_scale_argument(ra):
+    B, Hq, Hkv, S, N, D = 1, 4, 2, 1024, 4, 128
+    q, k, v = inputs(9850, B, Hq, Hkv, S, D, "bf16")
+    dout = grad_inputs(9850, B, Hq, S, D, "bf16")
+    tq, tk, tv, tg = (to_device(x, "bf16") for x in (q, k, v, dout))
+    out, lse = ra.forward(tq, tk, tv, N, causal=True, striped=1, scale=0.05)
+    got = virtual_ring_backward(ra, tq, tk, tv, out, lse, tg, N, True, 1, scale=0.05)
+    ra.check()
+    ref = backward_reference(q, k, v, dout, N, True, 1, "bf16", scale=0.05)
+    bq, bk = delta_error_bounds(q, k, v, dout, N, True, 1, "bf16", scale=0.05)
+    for name, g, r, e in zip(("dq", "dk", "dv"), got, ref, (bq, bk, None)):
+        assert_grad_close(from_device(g), r, "bf16", f"scaled ring backward {name}", e)
 
 
 def _train_rank(rank, world, port, case, q_out):
