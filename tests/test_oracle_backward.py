@@ -243,3 +243,22 @@ def test_key_rows_match_torch_autograd(causal):
             dv += b
         np.testing.assert_allclose(dk, tk.grad[0, kvh, keys].numpy(), rtol=0, atol=1e-11)
         np.testing.assert_allclose(dv, tv.grad[0, kvh, keys].numpy(), rtol=0, atol=1e-11)
+
+
+def test_ring_step_backward_scale_argument():
+    """The one-step function under a scale argument: scaling q by r and the
+    scale by 1/r leaves P unchanged, so dq scales by 1/r and dk, dv do not
+    change (the chain rule through s = scale q.k)."""
+    B, Hq, Hkv, Sb, D, N, i, j = 1, 2, 1, 8, 4, 4, 2, 1
+    q, k, v = rnd((B, Hq, Sb, D), 81), rnd((B, Hkv, Sb, D), 82), rnd((B, Hkv, Sb, D), 83)
+    dout = rnd((B, Hq, Sb, D), 84)
+    lse, delta = rnd((B, Hq, Sb), 85) + 3.0, rnd((B, Hq, Sb), 86)
+    r = 0.3 / (1 / math.sqrt(D))
+    a = oracle.ring_step_backward_block(q, k, v, dout, lse, delta, N, i, j, True, 1, scale=0.3)
+    b = oracle.ring_step_backward_block(q * r, k, v, dout, lse, delta, N, i, j, True, 1)
+    np.testing.assert_allclose(a[0], b[0] * r, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(a[2], b[2], rtol=0, atol=1e-12)
+    # a block no query of the shard sees (contiguous causal, j > i) adds nothing
+    z = oracle.ring_step_backward_block(q, k, v, dout, lse, delta, N, 1, 3, True, 0)
+    assert all(not x.any() for x in z)
