@@ -83,7 +83,7 @@ def test_one_step_is_the_block_partial(ra, B, Hq, Hkv, S, N, D, causal, layout, 
                  f"step i={i} j={j}")
 
 
-def virtual_ring(ra, tq, tk, tv, N, causal, layout):
+def virtual_ring(ra, tq, tk, tv, N, causal, layout, scale=None):
     """Every virtual device's N ring steps on buffers holding only its shard
     and the block it holds at that step; returns the shard-major output and
     lse."""
@@ -97,7 +97,8 @@ def virtual_ring(ra, tq, tk, tv, N, causal, layout):
             j = (i - s) % N
             st_o, st_l, out, lse = ra.ring_step(qi, _shard(tk, j, Sb), _shard(tv, j, Sb), N, i, j,
                                                 state_o=st_o, state_lse=st_l, first=s == 0,
-                                                last=s == N - 1, causal=causal, layout=layout)
+                                                last=s == N - 1, causal=causal, layout=layout,
+                                                scale=scale)
         outs.append(out)
         lses.append(lse)
     return torch.cat(outs, 2), torch.cat(lses, 2)
@@ -118,6 +119,16 @@ def test_virtual_ring_equals_full_attention(ra, B, Hq, Hkv, S, N, D, causal, lay
     ra.check()
     ro, rl = reference(q, k, v, N, causal, layout, "bf16")
     assert_close(from_device(out), from_device(lse), ro, rl, "bf16", "virtual ring")
+
+
+def test_virtual_ring_scale_argument(ra):
+    B, Hq, Hkv, S, N, D = 1, 4, 2, 1024, 4, 128
+    q, k, v = inputs(9650, B, Hq, Hkv, S, D, "bf16")
+    tq, tk, tv = (to_device(x, "bf16") for x in (q, k, v))
+    out, lse = virtual_ring(ra, tq, tk, tv, N, True, 1, scale=0.05)
+    ra.check()
+    ro, rl = reference(q, k, v, N, True, 1, "bf16", scale=0.05)
+    assert_close(from_device(out), from_device(lse), ro, rl, "bf16", "scaled virtual ring")
 
 
 def _free_port():
@@ -277,6 +288,7 @@ def _train_rank(rank, world, port, case, q_out):
 @pytest.mark.parametrize("case", [
     (9900, 1, 4, 2, 2048, 128, True, 1),   # striped
     (9901, 1, 2, 2, 2048, 128, True, 0),   # contiguous
+    (9902, 1, 2, 1, 2048, 128, True, 2),   # zigzag: Sb = 1024, two chunks of 512 per shard
 ])
 def test_two_process_training_step_on_one_gpu(cuda_ok, case):
     import torch.multiprocessing as mp
