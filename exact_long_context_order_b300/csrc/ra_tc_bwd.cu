@@ -644,8 +644,11 @@ constexpr int kVecOff = kDOOff + kDOStages * kTileBytes;  // per stage: -lse*log
 constexpr int kVecBytes = 2 * kT * 4;
 constexpr int kBarOff = kVecOff + 2 * kVecBytes;
 enum {
-    bKVFull = 0, bKVEmpty, bQFull, bQEmpty = bQFull + kQStages, bDOFull = bQEmpty + kQStages,
-    bDOEmpty = bDOFull + kDOStages, bVecFull = bDOEmpty + kDOStages, bVecEmpty = bVecFull + 2,
+    // a query tile's Q and dO land in the same stage and complete on one barrier,
+    // so each issuer's wait for its score GEMM's input also covers the input of
+    // its accumulation GEMM (the other of the two)
+    bKVFull = 0, bKVEmpty, bQDFull, bQDEmpty = bQDFull + kQStages,
+    bVecFull = bQDEmpty + kQStages, bVecEmpty = bVecFull + 2,
     // per query half h of the tile: S^T(h) done, P^T(h) written, dP^T(h) done, dS^T(h) written
     bSFull = bVecEmpty + 2, bPFull = bSFull + 2, bDPFull = bPFull + 2, bDsFull = bDPFull + 2,
     bAccFull = bDsFull + 2, bAccEmpty,
@@ -690,10 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(bKVFull), 1);
         mbar_init(bar(bKVEmpty), 2);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(bQFull + s), 1);
-            mbar_init(bar(bQEmpty + s), 2);
-            mbar_init(bar(bDOFull + s), 1);
-            mbar_init(bar(bDOEmpty + s), 2);
+            mbar_init(bar(bQDFull + s), 1);
+            mbar_init(bar(bQDEmpty + s), 2);
             mbar_init(bar(bVecFull + s), 32);
             mbar_init(bar(bVecEmpty + s), 8);
         }
@@ -766,20 +767,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(bar(bItemFull + (kk & 1)));
                 return true;
             };
-            auto load_ring = [&](int full, int empty, uint32_t off, const CUtensorMap* tm,
-                                 int row) -> bool {
+            // Q and dO of one query tile into stage g & 1, on one barrier
+            auto load_stage = [&](int row) -> bool {
                 const uint32_t st = g & 1, use = g >> 1;
-                if (use > 0 && !wait_bar(bar(empty + st), (use - 1) & 1, abort_flag, p.status,
-                                         wlim))
+                if (use > 0 && !wait_bar(bar(bQDEmpty + st), (use - 1) & 1, abort_flag,
+                                         p.status, wlim))
                     return false;
-                if (SELFTEST && g == 0 && full == bQFull) return true;  // Q(0) never comes
-                mbar_arrive_expect_tx(bar(full + st), kLoadBytes);
-                for (int bx = 0; bx < D / 64; ++bx)
-                    tma_load_2d(base + off + st * kTileBytes + bx * kBoxBytes, tm, bx * 64, row,
-                                bar(full + st), pol_q);
+                if (SELFTEST && g == 0) return true;  // Q(0) and dO(0) never come
+                mbar_arrive_expect_tx(bar(bQDFull + st), 2 * kLoadBytes);
+                for (int bx = 0; bx < D / 64; ++bx) {
+                    tma_load_2d(base + kQOff + st * kTileBytes + bx * kBoxBytes, &tm_q, bx * 64,
+                                row, bar(bQDFull + st), pol_q);
+                    tma_load_2d(base + kDOOff + st * kTileBytes + bx * kBoxBytes, &tm_do,
+                                bx * 64, row, bar(bQDFull + st), pol_q);
+                }
                 return true;
             };
-            uint32_t q_issued = 0, do_issued = 0;
+            uint32_t qd_issued = 0;
             long long item = (long long)atomicAdd(p.work, 1u);
             ok = publish(0, item);
             for (; ok && item < G.n_items; ++k) {
@@ -802,20 +806,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 KeyWalk w;
                 for (wstart(w, t); !w.done(G.rg); wnext(w, t), ++g) {
-                    const int row = (int)qrow0(t, w);
-                    if (!(ok = load_ring(bQFull, bQEmpty, kQOff, &tm_q, row))) break;
-                    q_issued = g + 1;
-                    if (!(ok = load_ring(bDOFull, bDOEmpty, kDOOff, &tm_do, row))) break;
-                    do_issued = g + 1;
+                    if (!(ok = load_stage((int)qrow0(t, w)))) break;
+                    qd_issued = g + 1;
                 }
             }
             if (!ok) {
                 // let every copy that may still be in flight land before exit
                 if (kv_loads > 0) drain_wait(bar(bKVFull), (kv_loads - 1) & 1, dlim);
-                for (uint32_t x = q_issued > 2 ? q_issued - 2 : 0; x < q_issued; ++x)
-                    drain_wait(bar(bQFull + (x & 1)), (x >> 1) & 1, dlim);
-                for (uint32_t x = do_issued > 2 ? do_issued - 2 : 0; x < do_issued; ++x)
-                    drain_wait(bar(bDOFull + (x & 1)), (x >> 1) & 1, dlim);
+                for (uint32_t x = qd_issued > 2 ? qd_issued - 2 : 0; x < qd_issued; ++x)
+                    drain_wait(bar(bQDFull + (x & 1)), (x >> 1) & 1, dlim);
             }
         }
     } else if (warp == 1 || warp == 2) {
@@ -835,17 +834,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sc_col = tmem + (is_s ? kColS : kColDP);
             const uint32_t acc_col = tmem + (is_s ? kColDV : kColDK);
             const uint32_t a_kv = base + (is_s ? kKOff : kVOff);
-            const int full_in = is_s ? bQFull : bDOFull;      // B of the score GEMM
-            const uint32_t off_in = is_s ? kQOff : kDOOff;
-            const int full_acc = is_s ? bDOFull : bQFull;     // B of the accumulation GEMM
-            const uint32_t off_acc = is_s ? kDOOff : kQOff;
+            const uint32_t off_in = is_s ? kQOff : kDOOff;    // B of the score GEMM
+            const uint32_t off_acc = is_s ? kDOOff : kQOff;   // B of the accumulation GEMM
             const int sig_full = is_s ? bSFull : bDPFull;
             const int sig_ready = is_s ? bPFull : bDsFull;
             uint32_t g = 0;
             int k = 0;
             bool ok = true;
             auto wait_in = [&](uint32_t gg) -> bool {
-                if (!wait_bar(bar(full_in + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status, wlim))
+                if (!wait_bar(bar(bQDFull + (gg & 1)), (gg >> 1) & 1, abort_flag, p.status, wlim))
                     return false;
                 tc_fence_after();
                 return true;
@@ -888,19 +885,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             !(ok = wait_bar(bar(bAccEmpty), (k - 1) & 1, abort_flag, p.status,
                                             wlim)))
                             break;
-                        // the accumulation GEMM's B stage (dO resp. Q) was loaded for
-                        // the other issuer's score GEMM: wait for it here too
-                        if (h == 0 && !(ok = wait_bar(bar(full_acc + (g & 1)), (g >> 1) & 1,
-                                                      abort_flag, p.status, wlim)))
-                            break;
                         tc_fence_after();
                         mma_tn_k64<D>(acc_col, sc_col + 64 * h,
                                       base + off_acc + (g & 1) * kTileBytes + h * kHalfBytes,
                                       n > 0 || h > 0);
-                        if (h == 1) {  // every MMA of this tile reading Q(n) and dO(n) is issued
-                            umma_commit(bar(bDOEmpty + (g & 1)));
-                            umma_commit(bar(bQEmpty + (g & 1)));
-                        }
+                        if (h == 1)  // every MMA of this tile reading Q(n) and dO(n) is issued
+                            umma_commit(bar(bQDEmpty + (g & 1)));
                         if (more) {
                             if (h == 0 && !(ok = wait_in(g + 1))) break;
                             issue_score(g + 1, h);
