@@ -522,9 +522,11 @@ int ra_check(void* stream);
  * a device; this entry point allocates nothing.  Its scratch, the kernel's
  * work-queue counter, lives in a 256-byte static __device__ array that every
  * device loading the library holds until the process exits.
- *   Arguments, layouts and results are those of ra_forward with
- *   dtype = RA_BF16; only the tensor-core kernel's shapes are accepted
- *   (D in {64, 128}; S/N a multiple of 256 for zigzag).
+ *   Arguments, layouts and results are those of ra_forward_ex with
+ *   dtype = RA_BF16 and RA_KERNEL_TC (the work-queue form: the stream-K form
+ *   ra_forward picks for few-item non-causal problems takes scratch); only
+ *   the tensor-core kernel's shapes are accepted (D in {64, 128}; S/N a
+ *   multiple of 256 for zigzag).
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress); make that first call outside CUDA-graph stream
  *   capture.  Each call zeroes the counter on `stream` before its kernel.
