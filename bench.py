@@ -33,19 +33,27 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "attention TFLOP/s & tokens/s (bf16, causal-adj) at S=128K; % of BF16 tensor peak"
-def kernel_name(wl, sm_count=148):
+def kernel_name(wl, sm_count=148, l2_bytes=126 * 10**6):
     """The tensor-core forward instantiation ra_forward runs on the workload:
     fwd_kernel<D, LOG, SELFTEST, RAGGED, MODE>, MODE the stream-K variant for
     non-causal problems with one to two work items per SM (items: pairs of
-    query tiles, by head pairs when the GQA group is even)."""
+    query tiles, by head pairs when the GQA group is even), else the ring
+    entered at block N-1 when the key/value blocks of the query shards the
+    grid holds at once exceed the L2 (not for contiguous causal shards), else
+    the ring order."""
     Sb = wl.S // wl.N
     nt = (Sb + 127) // 128
     g = wl.Hq // wl.Hkv
-    per = (g // 2) * wl.N * nt if g % 2 == 0 else g * wl.N * ((nt + 1) // 2)
+    per_shard = g // 2 if g % 2 == 0 else g
+    per = per_shard * wl.N * (nt if g % 2 == 0 else (nt + 1) // 2)
     items = wl.B * wl.Hkv * per
     streamk = (not wl.causal) and sm_count <= items < 2 * sm_count
     ragged = "true" if Sb % 128 else "false"
-    mode = "kModeStreamK" if streamk else "kModeRing"
+    grid = min(items, sm_count)
+    shards = min(wl.N, -(-grid // per_shard))
+    from_last = (not (wl.causal and int(wl.striped) == 0) and wl.N > 1
+                 and shards * 4 * Sb * wl.D > l2_bytes)
+    mode = "kModeStreamK" if streamk else ("kModeRingFromLast" if from_last else "kModeRing")
     return f"ra::tc::fwd_kernel<{wl.D}, false, false, {ragged}, {mode}>"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -731,6 +739,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     ra.lib()  # fail loudly if the library is missing
+    props = torch.cuda.get_device_properties(local)
 
     dtype = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     qs, kvs = wl.shapes()
@@ -872,7 +881,8 @@ def main():
         "gpu_launches": args.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": kernel_name(wl), "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "kernel": kernel_name(wl, props.multi_processor_count, props.L2_cache_size),
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "frac_of_sustained": achieved / peak_sus,
                      "launch_ms_mean": launch_avg_ms,
                      "launch_ms_median": float(np.median(per_launch_ms)),

@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -125,7 +126,13 @@ struct Params {
     unsigned int* part_flag;   // [n_items][2 slots][4 warps], zero at launch
 };
 
-enum Mode : int { kModeRing = 0, kModeStep = 1, kModeStreamK = 2 };
+enum Mode : int { kModeRing = 0, kModeStep = 1, kModeStreamK = 2, kModeRingFromLast = 3 };
+
+// The walk type of a mode: kModeRingFromLast enters every query shard's ring
+// at block N-1 (ring_entry), the other modes take the ring order.
+template <int MODE>
+using WalkT =
+    typename std::conditional<MODE == kModeRingFromLast, TileWalkFromLast, TileWalk>::type;
 
 // A work value: an item index, or in stream-K launches an item and the range
 // [b, e) of its fold positions, packed as item << 32 | b << 16 | e.
@@ -138,7 +145,7 @@ struct Work {
 // the one block a ring step holds, or fold positions [b, e) of a stream-K
 // segment (non-causal: position s*nt + kt is key tile kt of shard (i - s)).
 template <int MODE>
-__device__ __forceinline__ void walk_start(TileWalk& w, const ItemGeom& G, const Params& p,
+__device__ __forceinline__ void walk_start(WalkT<MODE>& w, const ItemGeom& G, const Params& p,
                                            const Item& it, const Work& wk) {
     if constexpr (MODE == kModeStep) {
         w.s = p.step_s;
@@ -161,13 +168,13 @@ __device__ __forceinline__ void walk_start(TileWalk& w, const ItemGeom& G, const
     }
 }
 template <int MODE>
-__device__ __forceinline__ bool walk_done(const TileWalk& w, const ItemGeom& G) {
+__device__ __forceinline__ bool walk_done(const WalkT<MODE>& w, const ItemGeom& G) {
     if constexpr (MODE == kModeStep) return w.kt >= w.nk;
     else if constexpr (MODE == kModeStreamK) return w.s * G.rg.nt + w.kt >= w.nk;
     else return w.done(G.rg);
 }
 template <int MODE>
-__device__ __forceinline__ void walk_next(TileWalk& w, const ItemGeom& G, const Item& it) {
+__device__ __forceinline__ void walk_next(WalkT<MODE>& w, const ItemGeom& G, const Item& it) {
     if constexpr (MODE == kModeStep) {
         ++w.kt;
     } else if constexpr (MODE == kModeStreamK) {
@@ -195,9 +202,10 @@ __device__ __forceinline__ Work decode_work(long long v) {
     return wk;
 }
 
-// MODE: kModeRing (the whole ring, items from the dynamic queue), kModeStep
-// (one step of a ring whose devices are separate processes) or kModeStreamK
-// (fixed contiguous work ranges per CTA; see Params).
+// MODE: kModeRing (the whole ring, items from the dynamic queue),
+// kModeRingFromLast (the same, every query shard entering at block N-1),
+// kModeStep (one step of a ring whose devices are separate processes) or
+// kModeStreamK (fixed contiguous work ranges per CTA; see Params).
 template <int D, bool LOG, bool SELFTEST, bool RAGGED, int MODE = kModeRing>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -318,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     bx * 64, row, bar(C::bQFull), pol_q);
                 }
                 const int64_t kvrow0 = (int64_t)(it.b * G.Hkv + it.kvh) * p.S;
-                TileWalk w;
+                WalkT<MODE> w;
                 for (walk_start<MODE>(w, G, p, it, wk); !walk_done<MODE>(w, G) && ok;
                      walk_next<MODE>(w, G, it)) {
                     // a ring step's buffer holds only the block it folds
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Work wk = decode_work<MODE>(item);
                 const Item it = decode_item(G, wk.item);
                 if (!(ok = wait_bar(bar(C::bQFull), k & 1, abort_flag, p.status, wlim))) break;
-                TileWalk w;
+                WalkT<MODE> w;
                 uint32_t n = 0;
                 for (walk_start<MODE>(w, G, p, it, wk); !walk_done<MODE>(w, G);
                      walk_next<MODE>(w, G, it), ++n) {
@@ -510,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = (t == 0) || it.valid1;
             float m_used = -INFINITY, l = 0.f;
             int n_logged = 0;
-            TileWalk w;
+            WalkT<MODE> w;
             uint32_t n = 0;
             for (walk_start<MODE>(w, G, p, it, wk); !walk_done<MODE>(w, G);
                  walk_next<MODE>(w, G, it), ++n, ++gt) {
@@ -865,6 +873,19 @@ static bool use_streamk(long long n_items, const FwdProblem& pr, int nt, int sm_
            fold_len <= 0xffff && n_items < (1ll << 31);
 }
 
+// L2 size of the current device, read once per device (0 if unknown).
+static long long device_l2_bytes() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) v = -1;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v > 0 ? v : 0;
+}
+
 // The stream-K scratch (the tails' partials and flags) comes from a memory
 // pool the library owns per device, allocated and freed on the launch's
 // stream, so launches on different streams never share it; freed blocks stay
@@ -965,10 +986,14 @@ static int launch_impl(const FwdProblem& pr, const FoldLog* flog, unsigned int* 
     if (cudaMemsetAsync(work, 0, sizeof(unsigned int), stream) != cudaSuccess) return RA_ERR_CUDA;
     auto kern = withhold_first_k ? fwd_kernel<D, false, true, RAGGED>
                                  : fwd_kernel<D, LOG, false, RAGGED>;
+    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
+    // large blocks: every query shard enters the ring at block N-1 (the
+    // logging and self-test variants keep the ring order)
+    if (!LOG && !withhold_first_k && ring_entry(P.G, grid, Sb, D, device_l2_bytes()))
+        kern = fwd_kernel<D, false, false, RAGGED, kModeRingFromLast>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return RA_ERR_CUDA;
-    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
     kern<<<(unsigned)grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, P);
     return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }

@@ -250,6 +250,27 @@ RA_HD ItemGeom make_item_geom(int B, int Hq, int Hkv, int N, int nt, int causal,
     return G;
 }
 
+// Whether the forward's query shards enter the ring at a common block
+// (TileWalkFromLast; host side).  In ring order the `grid` CTAs running
+// together hold items of about grid / per_shard query shards, and at a moment
+// each of these folds a different key/value shard (shard i folds i - s at
+// step s), so a block read by query shard i is wanted again by shard i + 1
+// one step later.  When those blocks' keys and values (4 * Sb * D bytes per
+// KV head) exceed the L2 they are evicted in between and every query shard
+// reads them from DRAM again.  Entered at block N-1, all query shards of a
+// level fold the same block at the same time (their steps have equal length
+// whenever the fold kind does not depend on j: striped and non-causal).  On
+// one GPU every block is resident from the start, so the entry point is free;
+// the fold order stays a rotation of the ring's cyclic order.
+inline int ring_entry(const ItemGeom& G, long long grid, int Sb, int D, long long l2_bytes) {
+    const bool contig_causal = G.rg.causal && G.rg.striped == kContiguous;
+    if (contig_causal || G.rg.N <= 1 || l2_bytes <= 0 || grid <= 0) return 0;
+    const long long per_shard = G.W / G.rg.N;
+    long long shards = (grid + per_shard - 1) / per_shard;
+    if (shards > G.rg.N) shards = G.rg.N;
+    return (double)shards * 4.0 * Sb * D > (double)l2_bytes ? 1 : 0;
+}
+
 struct Item {
     int b, kvh, i;
     int h[2], qt[2];
@@ -318,6 +339,34 @@ struct TileWalk {
         }
     }
     RA_HD bool done(const RingGeom& g) const { return s >= g.N; }
+    RA_HD void next(const RingGeom& g, const Item& it) {
+        if (++kt >= nk) advance_shard(g, it);
+    }
+};
+
+// The same fold list entered at a common block (ring_entry): key shards
+// j = N-1, N-2, ..., 0, i.e. ring steps s = (i - j) mod N from (i + 1) mod N
+// cyclically, each shard's live key tiles ascending.
+struct TileWalkFromLast {
+    int s, j, kt, nk;
+    RA_HD void start(const RingGeom& g, const Item& it) {
+        j = g.N; s = 0; kt = 0; nk = 0;
+        advance_shard(g, it);
+    }
+    RA_HD void advance_shard(const RingGeom& g, const Item& it) {
+        for (;;) {
+            if (--j < 0) return;
+            s = it.i - j;
+            if (s < 0) s += g.N;
+            int nk0, nk1, d;
+            shard_span(g, it.i, j, it.qt[0], &nk0, &d);
+            shard_span(g, it.i, j, it.qt[1], &nk1, &d);
+            nk = nk0 > nk1 ? nk0 : nk1;
+            kt = 0;
+            if (nk > 0) return;
+        }
+    }
+    RA_HD bool done(const RingGeom&) const { return j < 0; }
     RA_HD void next(const RingGeom& g, const Item& it) {
         if (++kt >= nk) advance_shard(g, it);
     }

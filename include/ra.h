@@ -108,7 +108,13 @@ enum { RA_FOLD_FULL = 0, RA_FOLD_INCL = 1, RA_FOLD_STRICT = 2 };
  * schedule and the numerator/denominator fold; aiunderstanding.org,
  * "Approfondimento tecnico": running max and normaliser with rescaling).
  * Under causal masking whole shards and key tiles with no visible pair are
- * skipped, never computed.
+ * skipped, never computed.  When the key/value shards that the query shards
+ * in flight at once would read together exceed the L2 (striped, zigzag and
+ * non-causal layouts at very long S, e.g. 1M tokens in 64 shards), the
+ * tensor-core kernel enters every query shard's ring at shard N-1: query
+ * shard i then folds j = N-1, N-2, ..., 0, the same cyclic order from ring
+ * step (i + 1) mod N, so that all of them read one key/value shard at a
+ * time.  Only the rounding of the fold can differ.
  * Errors: RA_ERR_INVALID_ARG, RA_ERR_ALIGN (q, k, v, out, lse not 16-byte
  * aligned), RA_ERR_UNSUPPORTED (D > 256, device not sm_103, or a shape that
  * no kernel takes: the tensor-core kernel needs B*Hq*S and B*Hkv*S below 2^31
@@ -345,7 +351,9 @@ int ra_ulysses_exchange(const void* src, void* dst, int B, int H, int64_t S, int
  * that are absent.  kind is RA_FOLD_FULL (every pair visible), RA_FOLD_INCL
  * (pairs with local key row <= local query row) or RA_FOLD_STRICT (local
  * key row < local query row).  The tensor-core kernel folds every query
- * tile in exactly this order (ra_fold_log records it).
+ * tile in exactly this order (ra_fold_log records it), or in ra_forward's
+ * long-sequence case in this order rotated to start at ring step
+ * (i + 1) mod N (see ra_forward).
  *   items: int32[cap][6] or NULL (then only *n_items is set).
  *   striped is the layout (RA_LAYOUT_*).  Requires tile >= 2; a shard's last
  *   tile may be partial (ceil(Sb/tile) tiles), except under zigzag, which
@@ -400,7 +408,9 @@ int ra_plan_backward(int64_t S, int N, int causal, int striped, int tile, int j,
  *        written by the caller.
  *   counts: device int32[B*Hq*N*nt]: number of live folds recorded per tile.
  *   max_entries >= N * nt.
- * The logging variant computes the same outputs as ra_forward.
+ * The logging variant always folds in ring order, so it computes the same
+ * outputs as ra_forward except where ra_forward enters the ring at shard
+ * N-1 (there they agree up to rounding).
  * Errors: as ra_forward, plus RA_ERR_UNSUPPORTED outside the tensor-core
  * kernel's envelope and RA_ERR_INVALID_ARG for an empty problem.
  */
