@@ -347,12 +347,14 @@ def ring_step_backward(q, k, v, out, lse, dout, N: int, i: int, j: int, delta=No
 
 
 def backward(q, k, v, out, lse, dout, N: int, causal: bool = False, striped: bool = False,
-             scale=None, kernel: str = "auto", workspace=None, stream=None):
+             scale=None, kernel: str = "auto", workspace=None, stream=None, dq=None, dk=None,
+             dv=None):
     """Gradients (dq, dk, dv) of ``forward`` over shard-major torch CUDA tensors.
 
     q, k, v, out and lse are the forward's inputs and outputs, dout = dL/dout
     (like out).  The workspace (a uint8 CUDA tensor of at least
-    ra_backward_workspace bytes) is allocated here when not given.
+    ra_backward_workspace bytes) is allocated here when not given, and so are
+    dq (like q), dk and dv (like k) when not given (contiguous, q's dtype).
     """
     import torch
     B, Hq, S, D = q.shape
@@ -372,9 +374,12 @@ def backward(q, k, v, out, lse, dout, N: int, causal: bool = False, striped: boo
     _check(rc, "ra_backward_workspace")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, like in ((dq, q), (dk, k), (dv, v)):
+        if t.dtype != q.dtype or t.shape != like.shape or not t.is_contiguous():
+            raise ValueError("dq must be like q, dk and dv like k (contiguous, q's dtype)")
     rc = ra_backward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq),
                         _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, Hq, Hkv, S, D,
                         N, int(causal), int(striped), float(scale or 0.0), dtype,

@@ -40,8 +40,10 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -202,7 +204,7 @@ constexpr uint32_t kItemReaders = 10;  // two MMA issuers and eight softmax warp
 // SELFTEST: the failure-detection self test (the first K tile is never
 // loaded, every wait is bounded by p.timeout_cycles).  STEP: one step of a
 // ring whose devices are separate processes (see Params).
-template <int D, bool SELFTEST, bool STEP = false>
+template <int D, bool SELFTEST, bool STEP = false, bool FROM_LAST = false>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -279,16 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         it.valid1 = 0;
         return it;
     };
-    // the item's key tiles: its fold list, or in a ring step block step_j's
-    auto wstart = [&](TileWalk& w, const Item& it) {
+    // the item's key tiles: its fold list (entered at block N-1 with
+    // FROM_LAST), or in a ring step block step_j's
+    using Walk = typename std::conditional<FROM_LAST, TileWalkFromLast, TileWalk>::type;
+    auto wstart = [&](Walk& w, const Item& it) {
         if constexpr (STEP) step_key_walk(p, it.qt[0], w);
         else w.start(G.rg, it);
     };
-    auto wdone = [&](const TileWalk& w) -> bool {
+    auto wdone = [&](const Walk& w) -> bool {
         if constexpr (STEP) return w.kt >= w.nk;
         else return w.done(G.rg);
     };
-    auto wnext = [&](TileWalk& w, const Item& it) {
+    auto wnext = [&](Walk& w, const Item& it) {
         if constexpr (STEP) ++w.kt;
         else w.next(G.rg, it);
     };
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bar(bQFull), pol_q);
                 }
                 const int64_t kvrow0 = (int64_t)(t.b * G.Hkv + t.kvh) * p.S;
-                TileWalk w;
+                Walk w;
                 for (wstart(w, it); !wdone(w) && ok; wnext(w, it), ++tiles) {
                     const int64_t jrow = STEP ? 0 : (int64_t)w.j * p.Sb;
                     const int row = (int)(kvrow0 + jrow + (int64_t)w.kt * kT);
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Item it = walk_item(decode_qtile(G, item));
                 if (!(ok = wait_bar(bar(bQFull), k & 1, abort_flag, p.status, wlim)))
                     break;
-                TileWalk w;
+                Walk w;
                 uint32_t n = 0;
                 for (wstart(w, it); !wdone(w); wnext(w, it), ++n) {
                     if (is_a) {
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float nl2 = row_ok ? -p.lse[row] * kLog2e : 0.f;
             const float dl = row_ok ? p.delta[row] : 0.f;
             const uint64_t nl2x2 = f2_pack(nl2, nl2), ndl2 = f2_pack(-dl, -dl);
-            TileWalk w;
+            Walk w;
             uint32_t n = 0;
             for (wstart(w, it); !wdone(w); wnext(w, it), ++g, ++n) {
                 const int kind = STEP ? fold_kind(p.ring, p.step_i, p.step_j, t.qt, w.kt)
@@ -1177,6 +1181,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ host side
+// Whether the dq kernel's query tiles enter the ring at block N-1.  Its items
+// are query tiles of one head, g per (shard, tile), so the grid holds about
+// grid / g query shards at once; in ring order these read as many different
+// key/value blocks (4 * Sb * D bytes each per KV head).  When those exceed the
+// L2, every query tile walks blocks N-1, ..., 0 instead (TileWalkFromLast), as
+// the forward does, and the grid reads one block at a time.  Contiguous
+// causal shards keep their global-tile order, which already shares blocks.
+static bool dq_from_last(const TileGeom& G, long long grid, int Sb, int D, long long l2_bytes) {
+    if ((G.rg.causal && G.rg.striped == kContiguous) || G.rg.N <= 1 || l2_bytes <= 0)
+        return false;
+    long long shards = (grid + G.g - 1) / G.g;
+    if (shards > G.rg.N) shards = G.rg.N;
+    return (double)shards * 4.0 * Sb * D > (double)l2_bytes;
+}
+
+// L2 size of the current device, read once per device (0 if unknown).
+static long long l2_bytes_of_device() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0) v = -1;
+        cache[dev].store(v, std::memory_order_relaxed);
+    }
+    return v > 0 ? v : 0;
+}
+
 // kernel 0: dq_kernel over query tiles; kernel 1: dkv_kernel over key tiles
 static int launch_one(const BwdProblem& pr, int which, unsigned int* status, unsigned int* work,
                       int sm_count, cudaStream_t stream, long long timeout_cycles = 0) {
@@ -1212,10 +1244,12 @@ static int launch_one(const BwdProblem& pr, int which, unsigned int* status, uns
                     : (which ? (st ? dkv_kernel<128, true> : dkv_kernel<128, false>)
                              : (st ? dq_kernel<128, true> : dq_kernel<128, false>));
     const int smem = which ? dkv::kSmemBytes : dqk::kSmemBytes;
+    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
+    if (which == 0 && !st && dq_from_last(P.G, grid, Sb, pr.D, l2_bytes_of_device()))
+        kern = pr.D == 64 ? dq_kernel<64, false, false, true> : dq_kernel<128, false, false, true>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return RA_ERR_CUDA;
-    const long long grid = P.G.n_items < sm_count ? P.G.n_items : sm_count;
     kern<<<(unsigned)grid, kThreads, smem, stream>>>(mq, mdo, mk, mv, P);
     return cudaGetLastError() == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }

@@ -459,9 +459,11 @@ int ra_watchdog_selftest(const void* q, const void* k, const void* v, void* out,
  *   dq_t = scale sum_u dS_tu k_u      dk_u = scale sum_t dS_tu q_t
  * and a key/value head's gradient sums over the query heads that read it.
  * The fold follows the ring: dq of query shard i accumulates over key/value
- * shards j = (i - s) mod N in the forward's order, and the accumulators of
- * dk and dv of shard j travel with the block round the ring in its cyclic
- * order, entering it at device 0 (ra_plan_backward lists the order).
+ * shards j = (i - s) mod N in the forward's order (entered at shard N-1 on
+ * the tensor-core path when the blocks the query tiles in flight read at
+ * once exceed the L2, as in ra_forward), and the accumulators of dk and dv
+ * of shard j travel with the block round the ring in its cyclic order,
+ * entering it at device 0 (ra_plan_backward lists the order).
  * Shards and tiles without a visible pair are skipped.
  * Kernels: the tcgen05 tensor-core backward for bf16, D in {64, 128} (any Sb
  * for contiguous and striped shards, Sb % 256 == 0 for zigzag), else the fp32

@@ -11,6 +11,8 @@
   - uniform scores (K = 0, random q, v, dout): every row of dv and sampled
     rows of dk against the oracle's prefix-sum closed form, and dq exactly 0.
     All tiles, masks and ring steps run; only the score values are trivial.
+* long_1m (8 query heads on one KV head, S=1048576 in 64 striped shards):
+  every gradient element written, and stratified dq rows against the oracle.
 Bounds: tests/helpers.py TOL_BWD plus the delta term of delta_error_bounds.
 """
 import math
@@ -123,7 +125,39 @@ def torch_rows(t, b, h, rows):
 
 def test_backward_gqa_128k_sampled_dq_rows(gqa_128k_grads):
     wl, (q, k, v, dout), (dq, dk, dv) = gqa_128k_grads
-    rows = sample_rows(wl.seed + 1, wl.B, wl.Hq, wl.S, wl.N, 96)
+    _check_dq_rows(wl, q, k, v, dout, dq, 96)
+
+
+def test_backward_long_1m_sampled_dq_rows(ra):
+    """1M tokens (8 query heads on one KV head, 64 striped shards): the dq
+    kernel's query tiles enter the ring at block N-1 here (its concurrent
+    blocks exceed the L2).  NaN-filled gradients must be written everywhere,
+    and stratified dq rows match the per-row oracle."""
+    import torch
+    wl = WORKLOADS["long_1m"]
+    q, k, v, dout = _host_inputs(wl, (ragen.TENSOR_Q, ragen.TENSOR_K, ragen.TENSOR_V,
+                                      ragen.TENSOR_DO))
+    tq, tk, tv, tg = (to_device(x, "bf16") for x in (q, k, v, dout))
+    out, lse = ra.forward(tq, tk, tv, wl.N, causal=wl.causal, striped=wl.striped)
+    nan = float("nan")
+    dq = torch.full_like(tq, nan)
+    dk = torch.full_like(tk, nan)
+    dv = torch.full_like(tv, nan)
+    ra.backward(tq, tk, tv, out, lse, tg, wl.N, causal=wl.causal, striped=wl.striped,
+                dq=dq, dk=dk, dv=dv)
+    ra.check()
+    del tq, tk, tv, tg, out, lse
+    for t in (dq, dk, dv):
+        flat = t.view(-1, wl.D)
+        for r0 in range(0, flat.shape[0], 1 << 22):
+            assert bool(torch.isfinite(flat[r0:r0 + (1 << 22)]).all())
+    _check_dq_rows(wl, q, k, v, dout, dq, 48)
+
+
+def _check_dq_rows(wl, q, k, v, dout, dq, n_rows):
+    """Sampled dq rows against the per-row oracle, within TOL_BWD plus the
+    delta term of each row's error bound."""
+    rows = sample_rows(wl.seed + 1, wl.B, wl.Hq, wl.S, wl.N, n_rows)
     g = wl.Hq // wl.Hkv
     sc = 1.0 / math.sqrt(wl.D)
     pos = oracle.positions(wl.S, wl.N, wl.striped)
@@ -156,7 +190,7 @@ def test_backward_gqa_128k_sampled_dq_rows(gqa_128k_grads):
     errs = np.array(errs)
     worst = int(np.argmax(errs - bound))
     assert (errs <= bound).all(), (rows[worst], errs[worst], bound[worst], norms[worst])
-    print(f"gqa_128k dq: {len(rows)} rows, worst error/|row| "
+    print(f"{wl.name} dq: {len(rows)} rows, worst error/|row| "
           f"{float((errs / np.maximum(norms, 1e-30)).max()):.2e}")
 
 
