@@ -84,4 +84,9 @@ WORKLOADS = {
                              1, 32, 8, 131072, 16, 64, True, 1),
     "long_1m": Workload(4, "bf16_causal_gqa_B1_Hq8_Hkv1_S1048576_N64_D128_striped", "bf16",
                         1, 8, 1, 1048576, 64, 128, True, True),
+    # parity case for the forward's common ring entry at a size whose rows the
+    # oracle checks by the shard: 16 shards of 24576 tokens, whose keys and
+    # values (24 MiB per shard) together exceed the L2
+    "long_shards_384k": Workload(8, "bf16_causal_gqa_B1_Hq2_Hkv1_S393216_N16_D128_striped",
+                                 "bf16", 1, 2, 1, 393216, 16, 128, True, 1),
 }

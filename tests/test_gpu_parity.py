@@ -342,6 +342,8 @@ FULL_SIZE = [
     ("gqa_128k", 4096, [], ((0, 31), (0, 1))),
     ("gqa_128k_ragged", 768, [], None),
     ("long_1m", 4096, [], None),
+    # the common ring entry: every row of one head in the first and last shards
+    ("long_shards_384k", 1024, [], ((1,), (0, 15))),
 ]
 
 

@@ -127,6 +127,8 @@ L2 = 126 * 1000 * 1000
     # 1M tokens, 8 query heads on one KV head, 64 shards of 16384: the grid
     # holds 37 query shards reading 37 blocks of 8 MiB at once
     ("long_1m", (1, 8, 1, 64, 128, 1, 1, 148, 16384, 128), 1),
+    # 2 query heads on one KV head, 16 shards of 24576: 16 blocks of 24 MiB
+    ("long_shards_384k", (1, 2, 1, 16, 192, 1, 1, 148, 24576, 128), 1),
     # contiguous causal keeps its own order (global query tiles)
     ("long_1m_contiguous", (1, 8, 1, 64, 128, 1, 0, 148, 16384, 128), 0),
 ])
