@@ -134,3 +134,24 @@ L2 = 126 * 1000 * 1000
 ])
 def test_ring_entry_rule(harness, name, args, want):
     assert harness(*args, L2) == want, name
+
+
+def test_bench_names_the_kernel_the_rule_picks(harness):
+    """bench.py reports the forward instantiation by restating the host rule
+    in Python; for every named workload it must agree with ring_entry."""
+    import bench
+    import ragen
+    sms = 148
+    for name, wl in ragen.WORKLOADS.items():
+        if wl.dtype != "bf16":
+            continue
+        Sb = wl.S // wl.N
+        nt = (Sb + 127) // 128
+        g = wl.Hq // wl.Hkv
+        items = wl.B * wl.Hkv * wl.N * ((g // 2) * nt if g % 2 == 0 else g * ((nt + 1) // 2))
+        kname = bench.kernel_name(wl, sms, L2)
+        if "kModeStreamK" in kname:
+            continue
+        want = harness(wl.B, wl.Hq, wl.Hkv, wl.N, nt, int(wl.causal), int(wl.striped),
+                       min(items, sms), Sb, wl.D, L2)
+        assert ("kModeRingFromLast" in kname) == bool(want), name
